@@ -1,0 +1,395 @@
+"""Pins of the CPU oracle against facts that the pages and mathematics fix (no GPU needed).
+
+Each test checks the oracle against something other than itself: a textbook construction or
+table, a library routine, a closed form, an invariant, or brute force on small inputs.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.integrate
+import scipy.linalg
+
+from oracle import attention, codec
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line)
+    return rows
+
+
+# ------------------------------------------------------------------ rotation
+def test_splitmix64_published_outputs():
+    want = [int(x, 16) for x in _golden_rows("splitmix64_seed0.txt")]
+    assert codec.splitmix64(0, 3) == want
+
+
+def test_signs_are_pm1_and_balanced():
+    s = codec.wht_signs(0)
+    assert s.dtype == np.float32 and set(np.unique(s)) <= {-1.0, 1.0}
+    assert 40 < (s > 0).sum() < 88          # a fair coin over 128 draws
+    assert not np.array_equal(s, codec.wht_signs(1))
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_butterfly_is_sylvester_hadamard(dtype):
+    """Butterfly applied to the unit vectors reproduces scipy's Sylvester H_128 exactly."""
+    H = codec.hadamard_butterfly(np.eye(128, dtype=dtype))   # row j = H e_j = column j of H
+    ref = scipy.linalg.hadamard(128).astype(dtype)
+    assert np.array_equal(H.T, ref)
+    assert np.array_equal(H @ H.T, 128 * np.eye(128, dtype=dtype))
+
+
+def test_rotation_of_unit_vector_is_signed_hadamard_column():
+    s = codec.wht_signs(0)
+    ref = scipy.linalg.hadamard(128).astype(np.float32)
+    for j in (0, 5, 77, 127):
+        e = np.zeros(128, np.float32)
+        e[j] = 1.0
+        y = codec.rotate(e, s)
+        assert np.array_equal(y, (ref[:, j] * s[j]) * codec.C_WHT)
+
+
+def test_rotation_constant_bits():
+    assert np.float32(codec.C_WHT).view(np.uint32) == 0x3DB504F3
+
+
+def test_rotation_orthogonal_and_invertible():
+    rng = np.random.default_rng(1)
+    s = codec.wht_signs(3)
+    x = rng.standard_normal((64, 128)).astype(np.float32)
+    y = codec.rotate(x, s)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x.astype(np.float64), axis=1), rtol=1e-6)
+    xr = codec.unrotate(y, s)
+    assert np.max(np.abs(xr - x)) <= 2.0 ** -20 * np.max(np.abs(x)) * 8
+    # float64 version agrees with the float32 one to float32 rounding
+    assert np.allclose(codec.rotate64(x, s), y, rtol=0, atol=1e-5)
+
+
+def test_sumsq128_tree():
+    rng = np.random.default_rng(2)
+    # small integers: every partial sum is exact, so the tree equals the exact sum
+    v = rng.integers(-50, 50, (16, 128)).astype(np.float32)
+    assert np.array_equal(codec.sumsq128(v), (v.astype(np.int64) ** 2).sum(1).astype(np.float32))
+    x = rng.standard_normal((16, 128)).astype(np.float32)
+    exact = (x.astype(np.float64) ** 2).sum(1)
+    assert np.allclose(codec.sumsq128(x), exact, rtol=8 * 2.0 ** -24 * 8)
+    # a dropped or doubled block would be caught here
+    e = np.zeros(128, np.float32)
+    e[127] = 3.0
+    assert codec.sumsq128(e) == 9.0
+
+
+# ------------------------------------------------------------------ Q4G32
+def test_q4_on_grid_round_trip_is_lossless():
+    """Inputs already on a grid z + s*c (fp16 z, power-of-two s, codes using 0 and 15)."""
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        z = np.float16(rng.uniform(-4, 4)).astype(np.float32)
+        s = np.float32(2.0 ** rng.integers(-6, 0))
+        codes = rng.integers(0, 16, (4, 32))
+        codes[:, 0] = 0
+        codes[:, 1] = 15
+        y = (z + s * codes.astype(np.float32)).astype(np.float32).reshape(128)
+        c, sc, zc = codec.q4g32_encode(y)
+        assert np.array_equal(c, codes.reshape(128).astype(np.uint8))
+        assert np.all(sc.astype(np.float32) == s) and np.all(zc.astype(np.float32) == z)
+        assert np.array_equal(codec.q4g32_decode(c, sc, zc), y)
+
+
+def test_q4_constant_group():
+    y = np.full(128, 0.3, np.float32)
+    c, s, z = codec.q4g32_encode(y)
+    assert np.all(c == 0) and np.all(s == 0)
+    assert np.all(codec.q4g32_decode(c, s, z) == np.float16(0.3).astype(np.float32))
+
+
+def test_q4_codes_are_nearest_grid_points():
+    """Brute force: each code minimises |y - (z + s*c)| over c in 0..15 (ties excluded)."""
+    rng = np.random.default_rng(4)
+    y = (rng.standard_normal((200, 128)) * rng.uniform(0.1, 10, (200, 1))).astype(np.float32)
+    c, s, z = codec.q4g32_encode(y)
+    sg = np.repeat(s.astype(np.float64), 32, axis=-1)
+    zg = np.repeat(z.astype(np.float64), 32, axis=-1)
+    grid = zg[..., None] + sg[..., None] * np.arange(16)
+    dist = np.abs(y.astype(np.float64)[..., None] - grid)
+    best = dist.argmin(-1)
+    tie = np.sort(dist, -1)[..., 1] - np.sort(dist, -1)[..., 0] < 1e-6 * sg
+    assert np.array_equal(c[~tie], best[~tie])
+    # error bound: half a step plus the fp16 rounding of the zero and the scale
+    err = np.abs(codec.q4g32_decode(c, s, z) - y)
+    assert np.all(err <= 0.5 * sg + 2.0 ** -10 * (np.abs(zg) + 15 * sg) + 1e-6)
+
+
+def test_q4_scale_and_zero_formula_brute_force():
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal(128).astype(np.float32)
+    c, s, z = codec.q4g32_encode(y)
+    for gi in range(4):
+        g = y[32 * gi:32 * gi + 32]
+        assert z[gi] == np.float16(float(g.min()))
+        want = np.float16(np.float32(np.float32(g.max()) - np.float32(g.min())) / np.float32(15))
+        assert s[gi] == want
+
+
+# ------------------------------------------------------------------ Lloyd-Max / TQ3
+def test_lloyd_max_matches_textbook_table():
+    rows = _golden_rows("lloyd_max_gaussian_8.txt")
+    levels = np.array([float(x) for x in rows[0].split()])
+    thresholds = np.array([float(x) for x in rows[1].split()])
+    c, b = codec.lloyd_max_gaussian(8)
+    assert np.allclose(c[4:], levels, atol=1.5e-4)
+    assert np.allclose(c[:4], -levels[::-1], atol=1.5e-4)
+    assert np.allclose(b[3:], thresholds, atol=1.5e-4)
+
+
+def test_lloyd_max_fixed_point_conditions_by_quadrature():
+    """Centroid condition checked with numerical integration, independent of the closed form."""
+    c, b = codec.lloyd_max_gaussian(8)
+    edges = np.concatenate(([-np.inf], b, [np.inf]))
+    pdf = lambda x: math.exp(-0.5 * x * x) / math.sqrt(2 * math.pi)
+    for k in range(8):
+        m0 = scipy.integrate.quad(pdf, edges[k], edges[k + 1], epsabs=1e-14)[0]
+        m1 = scipy.integrate.quad(lambda x: x * pdf(x), edges[k], edges[k + 1], epsabs=1e-14)[0]
+        assert abs(m1 / m0 - c[k]) < 1e-9
+    assert np.allclose(b, 0.5 * (c[:-1] + c[1:]), atol=1e-15)
+    assert np.allclose(c, -c[::-1], atol=1e-12)
+
+
+def test_tq3_codebook_is_fp16_scaled_lloyd_max():
+    cent, bnd = codec.tq3_codebook()
+    c64, _ = codec.lloyd_max_gaussian(8)
+    assert cent.dtype == np.float16
+    assert np.allclose(cent.astype(np.float64), c64 / math.sqrt(128), rtol=2.0 ** -11)
+    assert np.all(np.diff(cent.astype(np.float32)) > 0)
+    assert np.all((bnd > cent[:-1].astype(np.float32)) & (bnd < cent[1:].astype(np.float32)))
+
+
+def test_tq3_codes_are_nearest_centroid_and_norms():
+    rng = np.random.default_rng(6)
+    proj = rng.standard_normal((128, 128)).astype(np.float32)
+    y = rng.standard_normal((100, 128)).astype(np.float32) * 3
+    code, bits, n, gamma = codec.tq3_qjl_encode(y, proj)
+    cent, _ = codec.tq3_codebook()
+    c32 = cent.astype(np.float32)
+    nrm = np.linalg.norm(y.astype(np.float64), axis=1)
+    assert np.allclose(n.astype(np.float64), nrm, rtol=2.0 ** -10)
+    u = y.astype(np.float64) / nrm[:, None]
+    d = np.abs(u[..., None] - c32.astype(np.float64))
+    best = d.argmin(-1)
+    sd = np.sort(d, -1)
+    clear = sd[..., 1] - sd[..., 0] > 1e-6
+    assert np.array_equal(code[clear], best[clear])
+    r = u - c32[code]
+    assert np.allclose(gamma.astype(np.float64), np.linalg.norm(r, axis=1), rtol=2.0 ** -10, atol=1e-6)
+    t = r @ proj.T.astype(np.float64)
+    far = np.abs(t) > 1e-5
+    assert np.array_equal(bits[far], t[far] >= 0)
+
+
+def test_qjl_estimator_is_unbiased():
+    """E_S[sqrt(pi/2)/m * |r| * <S q, sign(S r)>] = <q, r> for Gaussian S (QJL)."""
+    rng = np.random.default_rng(7)
+    q = rng.standard_normal(128)
+    r = rng.standard_normal(128) * 0.1
+    est = []
+    for _ in range(2000):
+        S = rng.standard_normal((128, 128))
+        est.append(codec.QJL_CONST * np.linalg.norm(r) * (S @ q) @ np.sign(S @ r))
+    est = np.array(est)
+    se = est.std() / math.sqrt(len(est))
+    assert abs(est.mean() - q @ r) < 3.5 * se
+
+
+def test_tq3_estimate_tracks_true_inner_product():
+    rng = np.random.default_rng(8)
+    proj = rng.standard_normal((128, 128)).astype(np.float32)
+    y = rng.standard_normal((400, 128)).astype(np.float32)
+    q = rng.standard_normal(128)
+    code, bits, n, gamma = codec.tq3_qjl_encode(y, proj)
+    est = codec.tq3_qjl_dot64(q, code, bits, n, gamma, proj)
+    true = y.astype(np.float64) @ q
+    assert np.corrcoef(est, true)[0, 1] > 0.97
+    assert abs(np.mean(est - true)) < 4 * np.std(est - true) / math.sqrt(len(true))
+
+
+# ------------------------------------------------------------------ Sinkhorn invariants
+def test_sinkhorn_recovers_planted_column_scales():
+    rng = np.random.default_rng(9)
+    a = rng.standard_normal((1024, 128))
+    a /= np.sqrt((a ** 2).mean(0))               # unit column RMS
+    cscale = np.exp(rng.uniform(np.log(0.2), np.log(5), 128))
+    x = (a * cscale).astype(np.float32)
+    sig = codec.sinkhorn_sigma(x).astype(np.float64)
+    ratio = sig / cscale
+    assert np.std(ratio) / np.mean(ratio) < 0.03
+
+
+def test_sinkhorn_balanced_input_gives_unit_sigma():
+    rng = np.random.default_rng(10)
+    x = rng.standard_normal((1024, 128)).astype(np.float32)
+    sig = codec.sinkhorn_sigma(x).astype(np.float64)
+    assert np.all(np.abs(sig - 1) < 0.12)
+
+
+def test_sinkhorn_balanced_block_has_unit_column_rms():
+    rng = np.random.default_rng(11)
+    x = (rng.standard_normal((512, 128)) * np.exp(rng.uniform(-2, 2, 128))).astype(np.float32)
+    sig = codec.sinkhorn_sigma(x).astype(np.float64)
+    bal = x / sig
+    rows = np.sqrt((bal.astype(np.float64) ** 2).mean(1, keepdims=True))
+    cols = np.sqrt(((bal / rows) ** 2).mean(0))
+    assert np.all(np.abs(cols - 1) < 0.05)
+
+
+# ------------------------------------------------------------------ attention
+def _cache(window, T, B=1, H=1, Hq=2, kfmt=attention.Q4G32, seed=0, sink=False, proj=None):
+    cfg = attention.OracleConfig(n_layers=1, n_kv_heads=H, n_q_heads=Hq, max_batch=B,
+                                 max_seq_len=T, window=window, k_format=kfmt, sinkhorn=sink,
+                                 seed=seed)
+    return attention.OracleCache(cfg, proj)
+
+
+@pytest.mark.parametrize("L", [1, 7, 100, 128])
+def test_window_covering_context_is_plain_attention(L):
+    rng = np.random.default_rng(12)
+    c = _cache(128, 256)
+    k = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    ref = attention.plain_attention64(q[0], k[0, 0], v[0, 0])
+    assert np.allclose(out[0], ref, rtol=0, atol=1e-12)
+
+
+def _brute_force_unit(cache, q, L):
+    """Token-by-token loop with Python floats: dequantise, rotate q, exp, normalise."""
+    cfg = cache.cfg
+    s = cache.signs.astype(np.float64)
+    W = cfg.window
+    Lq = max(0, L - W) if W > 0 else L
+    outs = []
+    for qh in q:
+        qt = codec.hadamard_butterfly(qh.astype(np.float64) * s) * float(codec.C_WHT)
+        ws, vals = [], []
+        for t in range(L):
+            if t < Lq:
+                code = cache.k["code"][0, 0, 0, t]
+                kv = [float(cache.k["zero"][0, 0, 0, t, j // 32]) +
+                      float(np.float32(cache.k["scale"][0, 0, 0, t, j // 32]) * np.float32(code[j]))
+                      for j in range(128)]
+                lg = sum(qt[j] * kv[j] for j in range(128)) / math.sqrt(128)
+                vc = cache.v["code"][0, 0, 0, t]
+                vr = np.array([float(cache.v["zero"][0, 0, 0, t, j // 32]) +
+                               float(np.float32(cache.v["scale"][0, 0, 0, t, j // 32]) * np.float32(vc[j]))
+                               for j in range(128)])
+                vals.append(s * (codec.hadamard_butterfly(vr) * float(codec.C_WHT)))
+            else:
+                kw = cache.ring_k[0, 0, 0, t % W].astype(np.float64)
+                lg = sum(float(qh[j]) * kw[j] for j in range(128)) / math.sqrt(128)
+                vals.append(cache.ring_v[0, 0, 0, t % W].astype(np.float64))
+            ws.append(lg)
+        m = max(ws)
+        e = [math.exp(w - m) for w in ws]
+        z = sum(e)
+        outs.append(sum(ei / z * vi for ei, vi in zip(e, vals)))
+    return np.array(outs)
+
+
+@pytest.mark.parametrize("window,L", [(4, 9), (0, 6), (2, 2), (8, 3)])
+def test_decode_matches_brute_force_on_tiny_inputs(window, L):
+    rng = np.random.default_rng(13)
+    c = _cache(window, 16, seed=5)
+    k = (rng.standard_normal((1, 1, L, 128)) * 2).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    assert np.allclose(out[0], _brute_force_unit(c, q[0], L), rtol=0, atol=1e-10)
+
+
+def test_bulk_append_equals_token_by_token():
+    rng = np.random.default_rng(14)
+    k = rng.standard_normal((2, 2, 40, 128)).astype(np.float32)
+    v = rng.standard_normal((2, 2, 40, 128)).astype(np.float32)
+    a = _cache(16, 64, B=2, H=2, Hq=4)
+    b = _cache(16, 64, B=2, H=2, Hq=4)
+    a.append(0, k, v, np.array([3, 10]))
+    for t in range(40):
+        b.append(0, k[:, :, t:t + 1], v[:, :, t:t + 1], np.array([3 + t, 10 + t]))
+    for name in ("code", "scale", "zero"):
+        assert np.array_equal(a.k[name], b.k[name]) and np.array_equal(a.v[name], b.v[name])
+    assert np.array_equal(a.ring_k, b.ring_k) and np.array_equal(a.ring_v, b.ring_v)
+
+
+def test_empty_sequence_gives_zero_output():
+    c = _cache(128, 16)
+    out = c.decode(0, np.ones((1, 2, 128), np.float32), np.array([0]))
+    assert np.all(out == 0)
+
+
+def test_rotation_reduces_q4_error_with_outlier_channels():
+    """[KV] TLDR: the Walsh-Hadamard rotation before 4-bit avoids the loss of flat q4 on outliers."""
+    rng = np.random.default_rng(15)
+    k = rng.standard_normal((512, 128)).astype(np.float32)
+    k[:, :4] *= 10
+    s = codec.wht_signs(0)
+    flat = codec.q4g32_decode(*codec.q4g32_encode(k))
+    rot = codec.unrotate(codec.q4g32_decode(*codec.q4g32_encode(codec.rotate(k, s))), s)
+    err_flat = np.mean((flat - k) ** 2)
+    err_rot = np.mean((rot - k) ** 2)
+    assert err_rot < 0.7 * err_flat
+
+
+def test_quantised_attention_tracks_full_precision():
+    rng = np.random.default_rng(16)
+    L = 600
+    k = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    c = _cache(0, L)
+    c.append(0, k, v, np.array([0]))
+    out = c.decode(0, q, np.array([L]))[0]
+    ref = attention.plain_attention64(q[0], k[0, 0], v[0, 0])
+    assert np.corrcoef(out.ravel(), ref.ravel())[0, 1] > 0.95
+
+
+# ------------------------------------------------------------------ bytes ([QC] tables)
+def test_compression_ratio_is_6_4():
+    """[QC]: 6.4x KV compression = 32 bits / (4 + (16 + 16) / 32) bits per value."""
+    cfg = attention.OracleConfig(1, 1, 1, 1, 1)
+    per_value_bits = attention.payload_bytes_per_token_head(cfg) * 8 / (2 * 128)
+    assert per_value_bits == 5.0 and 32 / per_value_bits == 6.4
+
+
+def test_fp32_kv_at_32k_is_7_17_gb():
+    """[QC] PPL table: FP32 KV memory at 32K for Llama 3.2 3B (28 layers, 8 kv heads) 7.17 GB."""
+    b = attention.fp32_kv_bytes(28, 8, 32768)
+    assert b == 7_516_192_768
+    assert round(b / 2 ** 20 / 1000, 2) == 7.17
+
+
+def test_progressive_window_costs_0_03_gb():
+    """[QC] PPL table: 4-bit + progressive 2.33 GB vs 4-bit flat 2.30 GB -> window ~0.03 GB."""
+    cfg = attention.OracleConfig(n_layers=28, n_kv_heads=8, n_q_heads=24, max_batch=1,
+                                 max_seq_len=32768, window=128)
+    w = attention.window_bytes(cfg)
+    assert w == 28 * 8 * 128 * 128 * 4 * 2
+    assert round(w / 1e9, 2) == 0.03
+
+
+def test_tq_record_is_4_25_bits_and_compresses_over_4_5x():
+    """[TQ] comparison table: compression >= 4.5x at ~3.5 bits; our key record is 4.25 bits."""
+    assert attention.REC_BYTES[attention.TQ3_QJL] * 8 / 128 == 4.25
+    assert 16 / 3.5 >= 4.5
+    assert 32 / 4.25 > 4.5
