@@ -1,0 +1,407 @@
+"""Benchmark of one decode step of quantized-KV attention plus the append of one token per layer.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Default workload: Llama-3.2-3B-shaped decode at 32K context (28 layers, 24 query / 8 kv heads,
+batch 1, Q4G32 with a 128-token FP32 window).  One step = append the newest token of every layer
+(one launch over all layers) + decode attention over every layer (one launch over all layers).
+The cache (1.2 GB for the default workload) is larger than L2, so every step streams it from HBM.
+
+Prints one JSON line.  ``value`` = cached tokens attended per second, device-timed with CUDA events
+over K steps on resident inputs; ``e2e`` = the same through the public API with the step's inputs
+copied from pinned host memory and the output copied back inside the timed region.
+With --impl reference the CPU oracle is timed instead (a bounded sample of each step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")   # the CPU oracle is timed on one core
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from kv_cache_quantization_append_gb300 import QuantKVCache, lib, synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "kvq_internal.cuh"):
+        with open(os.path.join(ROOT, "kv_cache_quantization_append_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm_bandwidth_gbs"):
+                if key in d:
+                    return float(d[key]), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_traffic(workload: str):
+    """dram read+write bytes per decode launch from the committed ncu summary, if the kernel
+    source is unchanged since that capture (else None)."""
+    p = os.path.join(PROFILES, "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """nvidia-smi sampling (200 ms) during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 7:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[3 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------ workload set-up
+def workload_cfg(name: str):
+    w = synth.WORKLOADS[name]
+    layers = w.get("alloc_layers", w["n_layers"])
+    if "ctx_range" in w:
+        lens = synth.ragged_lengths(*w["ctx_range"], n=w["batch"], seed=w["len_seed"])
+    else:
+        lens = np.full(w["batch"], w["ctx"], np.int32)
+    return w, layers, lens
+
+
+def build_cache(name: str, device="cuda"):
+    """Allocate and prefill the cache of a workload; returns (cache, lens, block_table)."""
+    w, layers, lens = workload_cfg(name)
+    B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
+    cap = int(-(-(int(lens.max()) + 64) // 64) * 64)
+    kf = lib.KVQ_TQ3_QJL if w["k_format"] == "tq3_qjl" else lib.KVQ_Q4G32
+    bt = None
+    n_pages = 0
+    if w.get("page_tokens"):
+        # paged pool sized to the real lengths (+ one prefill chunk per sequence), shuffled
+        extra = w.get("prefill_chunk", 0)
+        cap = int(-(-(int(lens.max()) + extra + 64) // 64) * 64)
+        maxpps = cap // 64
+        need = [int(-(-(int(L) + extra) // 64)) for L in lens]
+        n_pages = sum(need)
+        perm = np.random.default_rng(11).permutation(n_pages)
+        table = np.full((B, maxpps), 0, np.int32)
+        o = 0
+        for b in range(B):
+            table[b, :need[b]] = perm[o:o + need[b]]
+            o += need[b]
+        bt = torch.as_tensor(table, device=device).contiguous()
+    proj = synth.qjl_projection(w["qjl_seed"]) if kf == lib.KVQ_TQ3_QJL else None
+    cfg = lib.make_config(layers, H, Hq, B, cap, window=w["window"], n_pages=n_pages, k_format=kf,
+                          sinkhorn=w["sinkhorn"], in_dtype=lib.KVQ_IN_BF16 if w["in_dtype"] == "bf16" else lib.KVQ_IN_F32,
+                          seed=w["wht_seed"])
+    cache = QuantKVCache(cfg, device, bt, proj)
+    # prefill positions [0, L_b - 1) in chunks; the newest token is written by every step
+    T_pre = lens - 1
+    chunk = 4096
+    for layer in range(layers):
+        if w["sinkhorn"]:
+            n_cal = w.get("calib_tokens", 1024)
+            kc, vc = synth.kv_tokens(w, layer, 1, H, 0, n_cal, device=device)
+            cache.calibrate(layer, kc[0].contiguous(), vc[0].contiguous())
+        for t0 in range(0, int(T_pre.max()), chunk):
+            n = min(chunk, int(T_pre.max()) - t0)
+            full = T_pre >= t0 + n
+            k, v = synth.kv_tokens(w, layer, B, H, t0, n, device=device)
+            if full.any():
+                pos = torch.as_tensor(np.where(full, t0, -1).astype(np.int32), device=device)
+                cache.append(layer, k, v, pos)
+            for b in np.nonzero(~full & (T_pre > t0))[0]:
+                m = int(T_pre[b]) - t0
+                pos = torch.as_tensor(np.where(np.arange(B) == b, t0, -1).astype(np.int32), device=device)
+                cache.append(layer, k[:, :, :m].contiguous(), v[:, :, :m].contiguous(), pos)
+    torch.cuda.synchronize()
+    if cache.status() != 0:
+        raise RuntimeError("device status set during prefill")
+    return cache, w, layers, lens
+
+
+def algorithmic_bytes(w, layers, lens) -> int:
+    """Bytes the decode step must move: packed records of the quantised tokens, the FP32 window,
+    q and out (per launch over all layers)."""
+    W = w["window"]
+    rec = (68 if w["k_format"] == "tq3_qjl" else 80) + 80
+    H, Hq = w["n_kv_heads"], w["n_q_heads"]
+    per_layer = 0
+    for L in lens:
+        L = int(L)
+        Lq = max(0, L - W) if W > 0 else L
+        per_layer += H * (Lq * rec + (L - Lq) * 1024)
+    per_layer += len(lens) * Hq * 128 * (2 + 4)
+    return per_layer * layers
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    cache, w, layers, lens = build_cache(args.workload, dev)
+    B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
+    dt = torch.bfloat16 if w["in_dtype"] == "bf16" else torch.float32
+    nbuf = 8
+    qs = [torch.stack([synth.queries(w, l, B, Hq, step=i, device=dev) for l in range(layers)]) for i in range(nbuf)]
+    kvs = [synth.kv_tokens(w, l, B, H, int(lens.max()) - 1, 1, device=dev) for l in range(layers)]
+    knew = torch.stack([k for k, _ in kvs]).contiguous()    # [L][B][H][1][128]
+    vnew = torch.stack([v for _, v in kvs]).contiguous()
+    pos = torch.as_tensor((lens - 1).astype(np.int32), device=dev)
+    seq = torch.as_tensor(lens.astype(np.int32), device=dev)
+    out = torch.empty(layers, B, Hq, 128, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        cache.append(-1, knew, vnew, pos)
+        cache.decode(-1, qs[i % nbuf], seq, out)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    # device-timed region: events around every decode launch, and around the whole loop
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            cache.append(-1, knew, vnew, pos)
+            ev[i][0].record(stream)
+            cache.decode(-1, qs[i % nbuf], seq, out)
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    if cache.status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    # end-to-end through the public API: host inputs in, host output out, every step
+    q_h = [q.cpu().pin_memory() for q in qs]
+    k_h, v_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(qs[0])
+    k_d, v_d = torch.empty_like(knew), torch.empty_like(vnew)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        q_d.copy_(q_h[i % nbuf], non_blocking=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        q_d.copy_(q_h[i % nbuf], non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        cache.append(-1, k_d, v_d, pos)
+        cache.decode(-1, q_d, seq, out)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+
+    tokens_per_step = float(lens.sum()) * world   # sequence lengths summed; every layer attends them
+    ms_step = total_ms / args.steps
+    value = tokens_per_step / (ms_step / 1e3)
+    alg = algorithmic_bytes(w, layers, lens)
+    dec_avg_s = statistics.mean(dec_ms) / 1e3
+    peak, peak_src = hbm_peak()
+    achieved = alg / dec_avg_s / 1e9
+    traffic = measured_traffic(args.workload)
+    result = None
+    if rank == 0:
+        result = {
+            "metric": "quantized-KV decode attention: cached tokens/s (decode of all layers + append of one token per layer)",
+            "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "q4/fp16-mma,f32-accum" if w["k_format"] == "q4g32" else "tq3+qjl/q4,f32-accum",
+            "data": "synthetic (seeded N(0,1) with outlier channels, shapes of the workload; no weights)",
+            "config": {"workload": args.workload, "layers": layers, "batch": int(w["batch"]),
+                       "n_q_heads": Hq, "n_kv_heads": H, "seq_len_sum": int(lens.sum()),
+                       "window": w["window"], "k_format": w["k_format"], "v_format": w["v_format"],
+                       "sinkhorn": bool(w["sinkhorn"]), "parallelism": f"replicas x{world}",
+                       "l2": f"cache of {cache.buffer.numel() / 1e9:.2f} GB streamed each step (> 126 MB L2)"},
+            "hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+                         "kernel": "decode_kernel (all layers, one launch)",
+                         "decode_us_avg": dec_avg_s * 1e6},
+            "e2e": {"value": tokens_per_step / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
+                    "h2d_bytes_per_step": int(qs[0].numel() * qs[0].element_size() + 2 * knew.numel() * knew.element_size()),
+                    "d2h_bytes_per_step": int(out.numel() * 4), "ms_per_step": e2e_ms / args.steps},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+    return result, cache, w, layers, lens
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_unit_time(w, lens, budget_s: float, which_units, bf16=True):
+    """Time the oracle's decode of sample units (encode excluded); returns (seconds per unit, n)."""
+    from oracle import attention
+
+    H, Hq = w["n_kv_heads"], w["n_q_heads"]
+    g = Hq // H
+    times = []
+    spent = 0.0
+    proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
+    for (layer, b) in which_units:
+        L = int(lens[b])
+        ocfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=g, max_batch=1, max_seq_len=L,
+                                      window=w["window"], k_format=w["k_format"], sinkhorn=w["sinkhorn"],
+                                      seed=w["wht_seed"])
+        ora = attention.OracleCache(ocfg, proj)
+        k, v = synth.kv_tokens(w, layer, 1, 1, 0, L, device="cpu")
+        ora.append(0, k.float().numpy(), v.float().numpy(), np.array([0]))
+        q = synth.queries(w, layer, 1, g, device="cpu").float().numpy()
+        t = time.perf_counter()
+        ora.decode(0, q, np.array([L]))
+        dt = time.perf_counter() - t
+        times.append(dt)
+        spent += dt
+        if spent >= budget_s:
+            break
+    return statistics.mean(times), len(times)
+
+
+def cpu_baseline(w, layers, lens, budget_s=12.0):
+    units = [(l % max(1, w["n_layers"]), int(b)) for l in range(64) for b in range(len(lens))][:64]
+    per_unit, n = oracle_unit_time(w, lens, budget_s, units)
+    n_units = layers * len(lens) * w["n_kv_heads"]
+    # unit times scale with length; normalise by the sampled lengths
+    sampled_tokens = sum(int(lens[b]) for (_, b) in units[:n]) / n
+    step_s = per_unit / sampled_tokens * (float(lens.sum()) / len(lens)) * n_units
+    value = float(lens.sum()) / step_s
+    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"numpy oracle decode of {n} (layer, kv-head) units of {int(sampled_tokens)} tokens, "
+                      f"scaled to the {n_units} units of one step; encode not timed"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    w, layers, lens = workload_cfg(args.workload)
+    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(w, layers, lens, budget_s=budget)
+        if i >= args.warmup:
+            vals.append(cb["value"])
+    value = statistics.mean(vals)
+    step_s = float(lens.sum()) / value
+    cb["value"] = value
+    return {"impl": "reference", "metric": "quantized-KV decode attention: cached tokens/s (decode of all layers + append of one token per layer)",
+            "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 attention, f32 codec", "data": "synthetic",
+            "config": {"workload": args.workload, "layers": layers, "batch": int(w["batch"])},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="llama3.2-3b-32k", choices=list(synth.WORKLOADS))
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        res = run_reference(args)
+        if res is not None:
+            print(json.dumps(res))
+        return
+    res, cache, w, layers, lens = run_gpu(args)
+    if res is not None:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(w, layers, lens)
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,191 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) quantized KV cache: append and decode attention.
+ *
+ * What the library computes (sources named by page title and section):
+ *   [QC] "Beyond RAG: load the whole document on your laptop" (quant.cpp summary):
+ *        the 128 most recent tokens stay FP32, everything else is 4-bit ("how it works"
+ *        paragraph; PPL / KV-memory table row "4-bit + progressive"); a batched write of the
+ *        quantized K cache is bit-identical to per-token writes (v3.2 batched-prefill note).
+ *   [KV] "Running Bonsai ternary 27B at 120K context in under 10 GB of VRAM" (KVarN port):
+ *        Walsh-Hadamard transform plus Sinkhorn variance balancing before 4-bit ("TLDR"
+ *        paragraph); separate K and V cache types (--cache-type-k / --cache-type-v).
+ *   [TQ] "LLM memory saving: weights vs KV-cache quantization (2026)": random rotation, a
+ *        per-coordinate optimal scalar quantiser and a 1-bit QJL sketch of the residual for an
+ *        unbiased inner product ("method comparison" table, "key idea" row); attention logits
+ *        computed directly on low-bit keys ("inference cost" row).
+ *
+ * Conventions for every entry point
+ *   - All functions are host functions.  Pointers documented as "device" must point to memory of
+ *     the CUDA device that was current at kv_cache_init; the caller owns every buffer (the cache,
+ *     inputs, outputs, scratch, the block table).  No entry point allocates or frees memory.
+ *   - Device pointers must be 16-byte aligned (KVQ_ERR_ALIGN otherwise).
+ *   - Work is enqueued asynchronously on ``stream`` (a cudaStream_t; NULL = legacy default
+ *     stream).  Entry points return after launching; none synchronises except kv_status.
+ *   - Invalid arguments return a KVQ_ERR_* code and launch nothing.  Inconsistencies only the
+ *     device can see (a block-table entry out of range, a position past capacity, a pipeline wait
+ *     that gave up) set bits in the cache's device status word, read with kv_status.
+ *   - head_dim is 128; n_q_heads is a multiple of n_kv_heads with a GQA group of 1..4 query heads
+ *     per kv-head; page_tokens is 64; window is 0 or a multiple of 8 up to 1024.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* NULL pointer, bad size, layer or batch out of range */
+  KVQ_ERR_UNSUPPORTED = 2,   /* config outside the supported shapes (see conventions above) */
+  KVQ_ERR_ALIGN = 3,         /* a device pointer is not 16-byte aligned */
+  KVQ_ERR_CAPACITY = 4,      /* buffer too small for the config (cache or scratch) */
+  KVQ_ERR_CUDA = 5,          /* a CUDA runtime call failed (launch, attribute, copy) */
+  KVQ_ERR_NOT_INIT = 6,      /* cache struct not initialised by kv_cache_init */
+};
+
+/* bits of the device status word (kv_status) */
+enum {
+  KVQ_DEV_BAD_PAGE = 1u,       /* block-table entry outside [0, n_pages): the token was skipped */
+  KVQ_DEV_POS_RANGE = 2u,      /* pos + n_tokens > max_seq_len: the sequence was skipped */
+  KVQ_DEV_SEQLEN_RANGE = 4u,   /* seq_lens[b] < 0 or > max_seq_len: treated as empty */
+  KVQ_DEV_TIMEOUT = 8u,        /* a copy-pipeline wait gave up after ~1 s: output is incomplete */
+};
+
+/* ---------------------------------------------------------------- formats */
+enum {
+  KVQ_Q4G32 = 1,     /* 4-bit asymmetric codes, groups of 32 channels, fp16 scale and zero (K, V) */
+  KVQ_TQ3_QJL = 3,   /* keys only: 3-bit Lloyd-Max codes of the unit vector, fp16 norm, 128 QJL
+                        residual sign bits and fp16 residual norm */
+};
+enum { KVQ_IN_F32 = 0, KVQ_IN_BF16 = 1 };
+
+typedef struct kvq_config {
+  int32_t n_layers;      /* layers held by this cache */
+  int32_t n_kv_heads;
+  int32_t n_q_heads;     /* multiple of n_kv_heads; n_q_heads / n_kv_heads in 1..4 */
+  int32_t head_dim;      /* 128 */
+  int32_t max_batch;     /* sequences the cache holds */
+  int32_t max_seq_len;   /* capacity per sequence (tokens) */
+  int32_t window;        /* most recent tokens also kept in FP32; 0 = flat 4-bit ([QC]: 128) */
+  int32_t page_tokens;   /* 64 */
+  int32_t n_pages;       /* physical pages per layer; 0 = max_batch * ceil(max_seq_len / 64) */
+  int32_t k_format;      /* KVQ_Q4G32 or KVQ_TQ3_QJL */
+  int32_t v_format;      /* KVQ_Q4G32 */
+  int32_t sinkhorn;      /* 1 = per-channel balancing scales (Q4G32 K and V only) */
+  int32_t group;         /* 32 */
+  int32_t in_dtype;      /* KVQ_IN_F32 or KVQ_IN_BF16: dtype of k, v, q and calibration inputs */
+  uint64_t seed;         /* seed of the rotation's random signs (SplitMix64 stream) */
+} kvq_config;
+
+/* Host-side handle, filled by kv_cache_init; plain data, may be copied. */
+typedef struct kvq_cache {
+  kvq_config cfg;
+  void* dev;                    /* the cache buffer (device), caller-owned */
+  uint64_t bytes;               /* its size */
+  const int32_t* block_table;   /* device int32 [max_batch][max_pages_per_seq] */
+  int32_t max_pages_per_seq;    /* ceil(max_seq_len / page_tokens) */
+  int32_t n_pages;              /* physical pages per layer actually used */
+  int32_t device;               /* CUDA device ordinal at init */
+  uint32_t magic;               /* set by kv_cache_init */
+} kvq_cache;
+
+/*
+ * Memory layout of the cache buffer (offsets 256-byte aligned, in this order):
+ *   header     status word, rotation signs (float[128] of +-1), TQ3 codebook and its decode table,
+ *              QJL projection (transposed, float[128][128], TQ3 keys only), Sinkhorn scales
+ *              sigma_k, sigma_v (fp16 [n_layers][n_kv_heads][128], 1.0 until calibrated),
+ *              identity block table (used when kv_cache_init gets none)
+ *   ring_k     float [n_layers][max_batch][n_kv_heads][window][128]   slot = position % window
+ *   ring_v     same
+ *   pages      [n_layers][n_pages][n_kv_heads][page_bytes]; one page = 64 tokens of one
+ *              (layer, kv-head), regions in order:
+ *     K main   Q4G32: 64 B per token, TQ3_QJL: 48 B codes per token then 16 B sign bits per token
+ *     V main   64 B per token
+ *     K meta   Q4G32: per token fp16 {scale[4], zero[4]};  TQ3_QJL: fp16 norm[64], fp16 gamma[64]
+ *     V meta   fp16 scale[4][64] then fp16 zero[4][64]   (group-major)
+ *   Q4G32 record (64 B): the 32 halfwords are indexed (r, G), r = 0..7, G = 0..3, halfword at byte
+ *     8r + 2G holds channels 32G + 4r .. 32G + 4r + 3 of the rotated (and balanced) vector as
+ *     nibbles, lowest channel in the lowest nibble.
+ *   TQ3 record: code of channel j at bits 3j .. 3j+2 of the 48-byte little-endian stream; sign
+ *     bit i (= (S r)_i >= 0) at bit i of the 16-byte stream.
+ */
+
+/* Closed-form size of the cache buffer for ``cfg``; 0 if the config is invalid or unsupported. */
+size_t kv_cache_bytes(const kvq_config* cfg);
+
+/*
+ * Lay out a cache in the caller's device buffer ``dev_mem`` (``bytes`` >= kv_cache_bytes(cfg)),
+ * write the header (signs from cfg->seed, codebook, QJL projection, unit Sinkhorn scales,
+ * identity block table) and clear the status word.  Page and ring contents are not cleared.
+ *   block_table      device int32 [max_batch][max_pages_per_seq] mapping (sequence, logical page)
+ *                    to a physical page in [0, n_pages); NULL = contiguous identity table.  The
+ *                    caller keeps it alive and may rewrite it between calls.
+ *   qjl_proj_host    host float [128][128] row-major i.i.d. N(0,1) projection S of the QJL sketch;
+ *                    required when k_format == KVQ_TQ3_QJL, ignored otherwise.
+ * Synchronises ``stream`` before returning (the header copies are complete on return).
+ */
+int kv_cache_init(kvq_cache* cache, const kvq_config* cfg, void* dev_mem, size_t bytes,
+                  const int32_t* block_table, const float* qjl_proj_host, void* stream);
+
+/*
+ * KVarN calibration ([KV] TLDR): for each kv-head of ``layer`` (or every layer when layer == -1)
+ * rotate the raw calibration block, run 8 Sinkhorn row/column RMS balancing iterations and store
+ * the per-channel scale sigma (fp16) for K and for V.  Must precede the quantised appends of that
+ * layer.  Inputs (device, cfg.in_dtype): k_calib, v_calib [L?][n_kv_heads][n_tokens][128] with the
+ * leading layer axis present when layer == -1.  n_tokens in 1..4096.  ``scratch`` (device, at
+ * least kv_calibrate_scratch_bytes) holds the float working copies.  Needs cfg.sinkhorn == 1.
+ */
+size_t kv_calibrate_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t n_tokens);
+int kv_calibrate(kvq_cache* cache, int32_t layer, const void* k_calib, const void* v_calib,
+                 int32_t n_tokens, void* scratch, size_t scratch_bytes, void* stream);
+
+/*
+ * Append ``n_tokens`` new K/V vectors to each of the first ``batch`` sequences at positions
+ * pos[b] .. pos[b] + n_tokens - 1 ([QC] "how it works"; v3.2 note: one call with n_tokens = T
+ * writes exactly the bytes of T calls with n_tokens = 1).  Every token is rotated, balanced
+ * (if calibrated) and quantised into its page; the last min(n_tokens, window) tokens are also
+ * written raw (float) into the window ring.
+ *   layer      0..n_layers-1, or -1 for all layers (k, v then carry a leading layer axis)
+ *   k, v       device, cfg.in_dtype, [L?][batch][n_kv_heads][n_tokens][128], contiguous
+ *   pos        device int32 [batch]; pos[b] < 0 leaves sequence b untouched (lets a caller
+ *              append ragged chunks to a subset of the batch)
+ */
+int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* v,
+                    const int32_t* pos, int32_t batch, int32_t n_tokens, void* stream);
+
+/*
+ * One decode step of attention for the first ``batch`` sequences over their cached tokens:
+ * positions [0, L - window) through the quantised pages (logits in rotated space), positions
+ * [L - window, L) through the FP32 ring, one softmax with scale 1/sqrt(128), L = seq_lens[b]
+ * (tokens already appended, the current one included).  An empty sequence (L = 0) gives zeros.
+ *   layer      0..n_layers-1, or -1 for all layers (q, out then carry a leading layer axis)
+ *   q          device, cfg.in_dtype, [L?][batch][n_q_heads][128]; query head j uses kv-head
+ *              j / (n_q_heads / n_kv_heads)
+ *   out        device float [L?][batch][n_q_heads][128]
+ *   seq_lens   device int32 [batch]
+ *   scratch    device, >= kv_decode_scratch_bytes(cache, layer, batch) bytes, zero-filled before
+ *              its first use; every successful call leaves its counters at zero again.  Calls
+ *              that share a scratch buffer must not overlap on the GPU.
+ * Splits the token axis over all SMs, runs a bulk-copy pipeline per SM and merges the partial
+ * softmax states inside the same launch; results do not depend on timing (fixed merge order).
+ */
+size_t kv_decode_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t batch);
+int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* out,
+                        const int32_t* seq_lens, int32_t batch, void* scratch,
+                        size_t scratch_bytes, void* stream);
+
+/* Read and clear the device status word (synchronises ``stream``); *flags gets KVQ_DEV_* bits. */
+int kv_status(kvq_cache* cache, uint32_t* flags, void* stream);
+
+/* Static string for a KVQ_* status code. */
+const char* kv_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVQ_H */

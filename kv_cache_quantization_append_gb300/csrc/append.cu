@@ -1,0 +1,202 @@
+// Append kernel: rotate, balance and quantise new K/V vectors into their pages, and keep the
+// most recent ones raw in the window ring.
+//
+// [QC] "how it works": 4-bit everywhere except a 128-token FP32 window; v3.2 note: a batched
+// write equals per-token writes bit for bit (here each token's record depends on that token only,
+// and the ring is written only for the last `window` tokens of a call, so no two threads of one
+// call write the same slot).
+// [KV] TLDR: Walsh-Hadamard rotation, then Sinkhorn per-channel balancing, then 4-bit.
+// [TQ] "key idea" row: random rotation, per-coordinate optimal scalar quantiser, 1-bit QJL
+// sketch of the residual.
+//
+// One warp per (layer, sequence, kv-head, token, K|V) vector; lane l holds channels 4l..4l+3.
+// Every floating-point step is one IEEE operation (explicit _rn intrinsics: no contraction), in
+// the order the codec defines, so codes are reproducible bit for bit.
+#include <cfloat>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int WARPS = 8;
+
+__device__ __forceinline__ uint32_t h16(__half h) { return (uint32_t)__half_as_ushort(h); }
+
+// Q4G32: per group of 32 channels exact min/max, fp16 scale (max-min)/15 and zero min, codes
+// clamp(rint((y - zero) / scale), 0, 15); 0 when the scale is 0.
+__device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, uint8_t* rec, __half& s16,
+                                          __half& z16) {
+  float mn = fminf(fminf(y[0], y[1]), fminf(y[2], y[3]));
+  float mx = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) {  // lanes 8G .. 8G+7 hold group G
+    mn = fminf(mn, __shfl_xor_sync(FULL, mn, m));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, m));
+  }
+  s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
+  z16 = __float2half_rn(mn);
+  const float s = __half2float(s16), z = __half2float(z16);
+  uint32_t hw = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    int c = 0;
+    if (s > 0.0f) c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(y[e], z), s)), 0), 15);
+    hw |= (uint32_t)c << (4 * e);
+  }
+  // halfword (r, G) = channels 32G + 4r .. +3 is stored at byte 8r + 2G; lane r gathers G = 0..3
+  const int r = lane & 7;
+  const uint32_t h0 = __shfl_sync(FULL, hw, r);
+  const uint32_t h1 = __shfl_sync(FULL, hw, r + 8);
+  const uint32_t h2 = __shfl_sync(FULL, hw, r + 16);
+  const uint32_t h3 = __shfl_sync(FULL, hw, r + 24);
+  if (lane < 8) *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+}
+
+__global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
+  __shared__ uint32_t sbits[WARPS][12];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const long long total = (long long)a.n_layers_call * a.batch * a.Hkv * a.T * 2;
+  const long long wid = (long long)blockIdx.x * WARPS + wl;
+  if (wid >= total) return;
+  const int kv = (int)(wid & 1);
+  long long rest = wid >> 1;
+  const int t = (int)(rest % a.T);
+  rest /= a.T;
+  const int h = (int)(rest % a.Hkv);
+  rest /= a.Hkv;
+  const int b = (int)(rest % a.batch);
+  const int ll = (int)(rest / a.batch);
+  const int layer = a.layer0 + ll;
+  const int H = a.Hkv;
+
+  const int p0 = a.pos[b];
+  if (p0 < 0) return;  // sequence not part of this append
+  if ((long long)p0 + a.T > a.max_seq_len) {
+    if (lane == 0 && t == 0 && kv == 0 && h == 0) atomicOr(a.p.status, KVQ_DEV_POS_RANGE);
+    return;
+  }
+  const int p = p0 + t;
+  const size_t vec = (((size_t)ll * a.batch + b) * H + h) * a.T + t;
+  const float4 xin = load4_in(kv ? a.v : a.k, vec * D + 4 * lane, a.in_bf16);
+
+  // raw copy into the window ring for the last `window` tokens of this call
+  if (a.W > 0 && t >= a.T - a.W) {
+    float* ring = kv ? a.p.ringv : a.p.ringk;
+    const size_t slot = (size_t)(p % a.W);
+    float* dst = ring + ((((size_t)layer * a.max_batch + b) * H + h) * a.W + slot) * D + 4 * lane;
+    *reinterpret_cast<float4*>(dst) = xin;
+  }
+
+  const int lp = p / PAGE, tin = p % PAGE;
+  const int phys = a.block_table[(size_t)b * a.L.max_pages_per_seq + lp];
+  if (phys < 0 || phys >= a.L.n_pages) {
+    if (lane == 0) atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
+    return;
+  }
+  uint8_t* pg = a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + h) * (size_t)a.L.page_bytes;
+
+  // rotation y = c * H (s . x): sign flip (exact), butterfly, one multiply by c
+  const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+  float y0 = __fmul_rn(xin.x, sg.x), y1 = __fmul_rn(xin.y, sg.y);
+  float y2 = __fmul_rn(xin.z, sg.z), y3 = __fmul_rn(xin.w, sg.w);
+  hadamard_warp(y0, y1, y2, y3, lane);
+  float y[4] = {__fmul_rn(y0, C_WHT), __fmul_rn(y1, C_WHT), __fmul_rn(y2, C_WHT), __fmul_rn(y3, C_WHT)};
+
+  if (kv == 0 && a.k_format == KVQ_TQ3_QJL) {
+    // ---- TurboQuant key: unit vector, 3-bit Lloyd-Max codes, residual QJL signs
+    const CodebookDev* cb = a.p.cb;
+    const float n = __fsqrt_rn(sumsq_warp(y[0], y[1], y[2], y[3]));
+    const float inv = __fdiv_rn(1.0f, fmaxf(n, FLT_MIN));
+    float r[4];
+    uint32_t c12 = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float u = __fmul_rn(y[e], inv);
+      int code = 0;
+#pragma unroll
+      for (int k = 0; k < 7; ++k) code += (cb->bnd[k] <= u) ? 1 : 0;
+      r[e] = __fsub_rn(u, __half2float(cb->cent[code]));
+      c12 |= (uint32_t)code << (3 * e);
+    }
+    const float gamma = __fsqrt_rn(sumsq_warp(r[0], r[1], r[2], r[3]));
+    // t_i = sum_{j = 0..127 in order} S[i][j] * r_j for i = 4*lane + e
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float4* st = reinterpret_cast<const float4*>(a.p.qjl_t) + lane;
+#pragma unroll 2
+    for (int jq = 0; jq < D / 4; ++jq) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * jq + e;
+        const float rj = __shfl_sync(FULL, r[e], jq);
+        const float4 s4 = st[j * (D / 4)];
+        acc[0] = __fadd_rn(acc[0], __fmul_rn(s4.x, rj));
+        acc[1] = __fadd_rn(acc[1], __fmul_rn(s4.y, rj));
+        acc[2] = __fadd_rn(acc[2], __fmul_rn(s4.z, rj));
+        acc[3] = __fadd_rn(acc[3], __fmul_rn(s4.w, rj));
+      }
+    }
+    uint32_t word = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) word |= (acc[e] >= 0.0f ? 1u : 0u) << (4 * (lane & 7) + e);
+#pragma unroll
+    for (int m = 1; m < 8; m <<= 1) word |= __shfl_xor_sync(FULL, word, m);
+    // 3-bit codes: channel j at bits 3j..3j+2 of a 384-bit stream; lane holds bits 12*lane..+11
+    if (lane < 12) sbits[wl][lane] = 0u;
+    __syncwarp();
+    const int bit = 12 * lane, w0 = bit >> 5, sh = bit & 31;
+    atomicOr(&sbits[wl][w0], c12 << sh);
+    if (sh > 20) atomicOr(&sbits[wl][w0 + 1], c12 >> (32 - sh));
+    __syncwarp();
+    uint8_t* rec = pg + (size_t)tin * 48;
+    if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = sbits[wl][lane];
+    uint32_t* sgn = reinterpret_cast<uint32_t*>(pg + 48 * PAGE + (size_t)tin * 16);
+    if ((lane & 7) == 0) sgn[lane >> 3] = word;
+    if (lane == 0) {
+      __half* meta = reinterpret_cast<__half*>(pg + a.L.off_kmeta);
+      meta[tin] = __float2half_rn(n);
+      meta[PAGE + tin] = __float2half_rn(gamma);
+    }
+    return;
+  }
+
+  // ---- Q4G32 (optionally Sinkhorn-balanced: y / sigma per channel)
+  if (a.sinkhorn) {
+    const __half* sig = (kv ? a.p.sigv : a.p.sigk) + ((size_t)layer * H + h) * D + 4 * lane;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(y[e], __half2float(sig[e]));
+  }
+  __half s16, z16;
+  uint8_t* rec = pg + (kv ? a.L.off_vmain : 0) + (size_t)tin * 64;
+  q4_encode(y, lane, rec, s16, z16);
+  if (kv == 0) {
+    // K meta: per token {scale[4], zero[4]} fp16
+    const uint32_t s0 = __shfl_sync(FULL, h16(s16), 0), s1 = __shfl_sync(FULL, h16(s16), 8);
+    const uint32_t s2 = __shfl_sync(FULL, h16(s16), 16), s3 = __shfl_sync(FULL, h16(s16), 24);
+    const uint32_t z0 = __shfl_sync(FULL, h16(z16), 0), z1 = __shfl_sync(FULL, h16(z16), 8);
+    const uint32_t z2 = __shfl_sync(FULL, h16(z16), 16), z3 = __shfl_sync(FULL, h16(z16), 24);
+    if (lane == 0)
+      *reinterpret_cast<uint4*>(pg + a.L.off_kmeta + (size_t)tin * 16) =
+          make_uint4(s0 | (s1 << 16), s2 | (s3 << 16), z0 | (z1 << 16), z2 | (z3 << 16));
+  } else if ((lane & 7) == 0) {
+    // V meta: group-major scale[4][64] then zero[4][64]
+    __half* meta = reinterpret_cast<__half*>(pg + a.L.off_vmeta);
+    const int G = lane >> 3;
+    meta[G * PAGE + tin] = s16;
+    meta[4 * PAGE + G * PAGE + tin] = z16;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
+  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * a.T * 2;
+  const long long blocks = (warps + WARPS - 1) / WARPS;
+  if (blocks <= 0) return cudaSuccess;
+  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  append_kernel<<<(unsigned)blocks, WARPS * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

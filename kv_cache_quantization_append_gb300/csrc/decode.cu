@@ -1,0 +1,945 @@
+// Decode attention over the quantised KV cache (one launch per call).
+//
+// What it computes ([QC] "how it works" + PPL table; [KV] TLDR; [TQ] "key idea" and "inference
+// cost" rows): for every (layer, sequence b, kv-head h) and each of its g query heads,
+//   softmax over t < L of  q.k_t / sqrt(128)  applied to v_t,
+// where tokens t < L - window are read from the packed pages and scored in rotated space
+// (q~ = c H (s . q) [. sigma_k]), and the last `window` tokens come raw from the FP32 ring.
+//
+// Design for GB300 (one CTA per SM, 8 consumer warps + 1 producer warp):
+//  * The work of a call is a list of "steps" -- one 64-token page or one 8-slot window chunk of one
+//    (layer, sequence, kv-head) unit -- cut into equal contiguous ranges, one per CTA, so every SM
+//    streams the same number of bytes whatever the sequence lengths (ragged batches included).
+//  * The producer warp streams each step into a 16-stage shared-memory ring with
+//    cp.async.bulk (the 1D TMA path) completing on mbarriers; stage k goes to consumer warp k % 8.
+//  * Consumer warps dequantise nibbles to fp16 in registers (exponent-bias trick: OR a nibble into
+//    the mantissa of 1024.0, subtract exactly) and run the logits and P.V as tensor-core
+//    mma.sync m16n8k16 (fp32 accumulate): GQA query heads are the N axis (hi and lo halves of q
+//    in adjacent columns), per-group scales and zero points are folded out of the products.
+//  * Each warp keeps an online-softmax state per unit and, when it leaves the unit, writes a
+//    partial record (max, sum, accumulator) to scratch and bumps the unit's arrival counter; the
+//    last arrival merges the records in a fixed order (deterministic), undoes the rotation of the
+//    quantised part and combines it with the window part.  No spin-wait on other CTAs.
+#include <cfloat>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr int NCW = 8;                       // consumer warps
+constexpr int NTHREADS = (NCW + 1) * 32;
+constexpr int NSTAGE = 16;
+constexpr int STAGE_BYTES = 10240;           // max page (Q4/Q4) and window chunk (8 KB)
+constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
+constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
+constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
+
+// shared-memory carve-up (bytes)
+constexpr int SM_STAGES = 0;
+constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
+constexpr int SM_DESC = SM_BARS + 2 * NSTAGE * 8;
+constexpr int SM_Q = SM_DESC + NSTAGE * 16;                       // [NCW][4][128] float
+constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;               // [NCW][4][128] float (TQ)
+constexpr int SM_QSUM = SM_SQ + NCW * MAX_GQA * D * 4;            // [NCW][4][4] float
+constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                    // [64][32] u32 (TQ)
+constexpr int SM_SEQ = SM_LUT + 64 * 32 * 4;                      // 3 int arrays of batch+1
+constexpr int SM_FIXED = SM_SEQ;
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false (and the status bit set) if the phase did not complete within ~1 s.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try(bar, parity)) return true;
+    if (globaltimer() - t0 > WAIT_NS) {
+      atomicOr(status, KVQ_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// Eight nibbles of w (bytes B0..B3, each = channel 2k low nibble, 2k+1 high nibble) -> four exact
+// fp16 pairs: (n0, n4), (n1, n5), (n2, n6), (n3, n7) where n_m is the m-th nibble.  A nibble ORed
+// into the mantissa of 1024.0 gives 1024 + c (or 1024 + 16c for a high nibble) exactly; the
+// subtraction / scaled fma back to c is exact in fp16.
+__device__ __forceinline__ void nib8(uint32_t w, uint32_t& p04, uint32_t& p15, uint32_t& p26, uint32_t& p37) {
+  const uint32_t M = 0x64006400u;
+  const __half2 k1024 = __float2half2_rn(1024.0f);
+  const __half2 k16 = __float2half2_rn(0.0625f);
+  const __half2 k64 = __float2half2_rn(-64.0f);
+  const uint32_t w8 = w >> 8;
+  p04 = h2u(__hsub2(u2h((w & 0x000F000Fu) | M), k1024));
+  p15 = h2u(__hfma2(u2h((w & 0x00F000F0u) | M), k16, k64));
+  p26 = h2u(__hsub2(u2h((w8 & 0x000F000Fu) | M), k1024));
+  p37 = h2u(__hfma2(u2h((w8 & 0x00F000F0u) | M), k16, k64));
+}
+
+__device__ __forceinline__ uint32_t split_pick(float v, bool lo) {
+  const __half hi = __float2half_rn(v);
+  return lo ? (uint32_t)__half_as_ushort(__float2half_rn(v - __half2float(hi))) : (uint32_t)__half_as_ushort(hi);
+}
+
+struct Seq {
+  const int* S;    // steps per sequence
+  const int* pre;  // exclusive prefix of S, [batch + 1]
+  const int* L;    // validated lengths
+};
+
+struct Pos {
+  int ll, b, h, local;
+};
+
+__device__ __forceinline__ Pos locate(long long x, long long S_layer, int B, int H, const Seq& sq) {
+  Pos p;
+  p.ll = (int)(x / S_layer);
+  const long long r = x - (long long)p.ll * S_layer;
+  int lo = 0, hi = B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((long long)H * sq.pre[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  p.b = lo;
+  const int r2 = (int)(r - (long long)H * sq.pre[lo]);
+  p.h = r2 / sq.S[lo];
+  p.local = r2 - p.h * sq.S[lo];
+  return p;
+}
+
+// ------------------------------------------------------------------ per-warp state
+struct QuantState {
+  uint32_t qb[8][2];   // B fragments of q~ (K logits), hi/lo interleaved columns
+  uint32_t sb[8][2];   // B fragments of S q~ (TQ sign dot)
+  float qsum[4];       // per-group sum of q~ for head (lane & 3)  (Q4 zero-point term)
+  float acc[8][4];     // P.V accumulators, m-tile j (16 channels), C fragment
+  float zacc[4];       // sum_t p_t z_{t,G}: rows = groups, cols = heads
+  float m, l;          // running max / partial sum for head (lane & 3)
+};
+
+struct WinState {
+  float q[MAX_GQA][4];
+  float acc[MAX_GQA][4];
+  float m[MAX_GQA], l[MAX_GQA];
+};
+
+template <int KF>
+struct Kernel {
+  const DecodeArgs& a;
+  uint8_t* smem;
+  int lane, warp;
+  int B, H, W, g, Hq;
+  long long S_layer, S;
+  long long nct;  // CTAs that own steps: min(gridDim.x, S), each owns at least one
+  Seq sq;
+
+  __device__ Kernel(const DecodeArgs& args, uint8_t* s) : a(args), smem(s) {}
+
+  __device__ __forceinline__ long long steps_before(int ll, int b, int h) const {
+    return (long long)ll * S_layer + (long long)H * sq.pre[b] + (long long)h * sq.S[b];
+  }
+  // CTA whose contiguous step range holds step x; the ranges split S steps over nct CTAs
+  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * nct - 1) / S); }
+
+  // ---------------------------------------------------------------- unit set-up
+  __device__ void load_q(int u, QuantState& st, WinState& ws, int kind) {
+    const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+    const int layer = a.layer0 + ll;
+    const size_t qbase = (((size_t)ll * B + b) * Hq + (size_t)h * g) * D;
+    if (kind == KIND_WINDOW) {
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (hh < g) x = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
+        ws.q[hh][0] = x.x * LOGIT_SCALE;
+        ws.q[hh][1] = x.y * LOGIT_SCALE;
+        ws.q[hh][2] = x.z * LOGIT_SCALE;
+        ws.q[hh][3] = x.w * LOGIT_SCALE;
+        ws.acc[hh][0] = ws.acc[hh][1] = ws.acc[hh][2] = ws.acc[hh][3] = 0.f;
+        ws.m[hh] = -INFINITY;
+        ws.l[hh] = 0.f;
+      }
+      return;
+    }
+    float* qs = reinterpret_cast<float*>(smem + SM_Q) + warp * MAX_GQA * D;
+    float* sqs = reinterpret_cast<float*>(smem + SM_SQ) + warp * MAX_GQA * D;
+    float* qsum = reinterpret_cast<float*>(smem + SM_QSUM) + warp * 16;
+    const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+#pragma unroll
+    for (int hh = 0; hh < MAX_GQA; ++hh) {
+      float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
+      if (hh < g) {
+        const float4 x = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
+        y0 = x.x * sg.x;
+        y1 = x.y * sg.y;
+        y2 = x.z * sg.z;
+        y3 = x.w * sg.w;
+      }
+      hadamard_warp(y0, y1, y2, y3, lane);
+      float sc[4] = {C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE};
+      if (a.sinkhorn) {
+        const __half* sig = a.p.sigk + ((size_t)layer * H + h) * D + 4 * lane;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] *= __half2float(sig[e]);
+      }
+      y0 *= sc[0];
+      y1 *= sc[1];
+      y2 *= sc[2];
+      y3 *= sc[3];
+      *reinterpret_cast<float4*>(qs + hh * D + 4 * lane) = make_float4(y0, y1, y2, y3);
+      float s = (y0 + y1) + (y2 + y3);
+      s += __shfl_xor_sync(FULL, s, 1);
+      s += __shfl_xor_sync(FULL, s, 2);
+      s += __shfl_xor_sync(FULL, s, 4);
+      if ((lane & 7) == 0) qsum[hh * 4 + (lane >> 3)] = s;
+    }
+    __syncwarp();
+    if (KF == KVQ_TQ3_QJL) {
+      // S q~ for each head: lane computes projections 4*lane .. 4*lane+3
+      const float4* st = reinterpret_cast<const float4*>(a.p.qjl_t) + lane;
+      for (int hh = 0; hh < g; ++hh) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int j = 0; j < D; ++j) {
+          const float qj = qs[hh * D + j];
+          const float4 s4 = st[j * (D / 4)];
+          acc.x += s4.x * qj;
+          acc.y += s4.y * qj;
+          acc.z += s4.z * qj;
+          acc.w += s4.w * qj;
+        }
+        *reinterpret_cast<float4*>(sqs + hh * D + 4 * lane) = acc;
+      }
+      __syncwarp();
+    }
+    const int r = lane >> 2, i = lane & 3;
+    const int head = r >> 1;
+    const bool lo = r & 1;
+    const bool hv = head < g;
+    const float* qh = qs + head * D;
+    const float* sh = sqs + head * D;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      int d0, d1, d2, d3;
+      if (KF == KVQ_TQ3_QJL) {
+        // codes: k-step kk holds channels 32i + 4kk + {0,1 | 2,3}
+        d0 = 32 * i + 4 * kk;
+        d1 = d0 + 1;
+        d2 = d0 + 2;
+        d3 = d0 + 3;
+      } else {
+        // Q4: k-step (G, e) = (kk >> 1, kk & 1) holds channels 32G + 8i + {0,4 | 1,5} + 2e
+        const int G = kk >> 1, e = kk & 1;
+        d0 = 32 * G + 8 * i + 2 * e;
+        d1 = d0 + 4;
+        d2 = d0 + 1;
+        d3 = d0 + 5;
+      }
+      const uint32_t v0 = hv ? split_pick(qh[d0], lo) : 0u, v1 = hv ? split_pick(qh[d1], lo) : 0u;
+      const uint32_t v2 = hv ? split_pick(qh[d2], lo) : 0u, v3 = hv ? split_pick(qh[d3], lo) : 0u;
+      st.qb[kk][0] = v0 | (v1 << 16);
+      st.qb[kk][1] = v2 | (v3 << 16);
+      if (KF == KVQ_TQ3_QJL) {
+        // signs: k-step kk holds projections 32i + 2kk + {0, 16 | 1, 17}
+        const int p0 = 32 * i + 2 * kk;
+        const uint32_t s0 = hv ? split_pick(sh[p0], lo) : 0u, s1 = hv ? split_pick(sh[p0 + 16], lo) : 0u;
+        const uint32_t s2 = hv ? split_pick(sh[p0 + 1], lo) : 0u, s3 = hv ? split_pick(sh[p0 + 17], lo) : 0u;
+        st.sb[kk][0] = s0 | (s1 << 16);
+        st.sb[kk][1] = s2 | (s3 << 16);
+      }
+    }
+#pragma unroll
+    for (int G = 0; G < 4; ++G) st.qsum[G] = (i < g) ? qsum[i * 4 + G] : 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) st.acc[j][0] = st.acc[j][1] = st.acc[j][2] = st.acc[j][3] = 0.f;
+    st.zacc[0] = st.zacc[1] = st.zacc[2] = st.zacc[3] = 0.f;
+    st.m = -INFINITY;
+    st.l = 0.f;
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- window chunk (raw fp32)
+  __device__ void window_step(const uint8_t* stage, int ntok, WinState& ws) {
+    const float* Ks = reinterpret_cast<const float*>(stage);
+    const float* Vs = Ks + WCHUNK * D;
+    float part[32];
+#pragma unroll
+    for (int t = 0; t < WCHUNK; ++t) {
+      const float4 k4 = *reinterpret_cast<const float4*>(Ks + t * D + 4 * lane);
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh)
+        part[4 * t + hh] = ws.q[hh][0] * k4.x + ws.q[hh][1] * k4.y + ws.q[hh][2] * k4.z + ws.q[hh][3] * k4.w;
+    }
+    // transpose-reduce 32 partial dots over 32 lanes: lane l ends with value index l = 4t + hh
+#pragma unroll
+    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+      const bool up = lane & o;
+#pragma unroll
+      for (int k = 0; k < n / 2; ++k) {
+        const float send = up ? part[k] : part[k + n / 2];
+        const float keep = up ? part[k + n / 2] : part[k];
+        part[k] = keep + __shfl_xor_sync(FULL, send, o);
+      }
+    }
+    const int t = lane >> 2, hh = lane & 3;
+    const float lg = (t < ntok && hh < g) ? part[0] : -INFINITY;
+    float mc = lg;
+    mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 4));
+    mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 8));
+    mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 16));
+    float alpha[MAX_GQA];
+    float mown = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < MAX_GQA; ++k) {
+      const float mk = __shfl_sync(FULL, mc, k);
+      const float mn = fmaxf(ws.m[k], mk);
+      alpha[k] = (mn == -INFINITY) ? 1.f : exp2f(ws.m[k] - mn);
+      ws.m[k] = mn;
+      if (hh == k) mown = mn;
+    }
+    const float p = (lg == -INFINITY) ? 0.f : exp2f(lg - mown);
+    float ps = p;
+    ps += __shfl_xor_sync(FULL, ps, 4);
+    ps += __shfl_xor_sync(FULL, ps, 8);
+    ps += __shfl_xor_sync(FULL, ps, 16);
+#pragma unroll
+    for (int k = 0; k < MAX_GQA; ++k) {
+      ws.l[k] = ws.l[k] * alpha[k] + __shfl_sync(FULL, ps, k);
+      ws.acc[k][0] *= alpha[k];
+      ws.acc[k][1] *= alpha[k];
+      ws.acc[k][2] *= alpha[k];
+      ws.acc[k][3] *= alpha[k];
+    }
+#pragma unroll
+    for (int tt = 0; tt < WCHUNK; ++tt) {
+      if (tt < ntok) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Vs + tt * D + 4 * lane);
+#pragma unroll
+        for (int k = 0; k < MAX_GQA; ++k) {
+          const float pt = __shfl_sync(FULL, p, 4 * tt + k);
+          ws.acc[k][0] += pt * v4.x;
+          ws.acc[k][1] += pt * v4.y;
+          ws.acc[k][2] += pt * v4.z;
+          ws.acc[k][3] += pt * v4.w;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- quantised page
+  __device__ void quant_step(const uint8_t* stage, int ntok, QuantState& st) {
+    const int r = lane >> 2, i = lane & 3;
+    const uint8_t* kmain = stage;
+    const uint8_t* vmain = stage + a.L.off_vmain;
+    const uint8_t* kmeta = stage + a.L.off_kmeta;
+    const __half* vscale = reinterpret_cast<const __half*>(stage + a.L.off_vmeta);
+    const __half* vzero = vscale + 4 * PAGE;
+    const bool headok = i < g;
+
+    // ---- logits for the page: thread holds tokens 16mt + r and 16mt + r + 8, head i
+    float lg[4][2];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const int ta = 16 * mt + r, tb = ta + 8;
+      if (KF == KVQ_TQ3_QJL) {
+        float cacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + SM_LUT) + lane;
+        const uint32_t* ca = reinterpret_cast<const uint32_t*>(kmain + ta * 48 + 12 * i);
+        const uint32_t* cbp = reinterpret_cast<const uint32_t*>(kmain + tb * 48 + 12 * i);
+        const uint32_t wa[4] = {ca[0], ca[1], ca[2], 0u};
+        const uint32_t wb[4] = {cbp[0], cbp[1], cbp[2], 0u};
+        uint32_t pa[16], pb[16];
+#pragma unroll
+        for (int pp = 0; pp < 16; ++pp) {
+          const int bit = 6 * pp, wi = bit >> 5, sh = bit & 31;
+          const uint32_t ia = __funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u;
+          const uint32_t ib = __funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u;
+          pa[pp] = lut[ia * 32];
+          pb[pp] = lut[ib * 32];
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma16816(cacc, pa[2 * kk], pb[2 * kk], pa[2 * kk + 1], pb[2 * kk + 1], st.qb[kk][0], st.qb[kk][1]);
+        const uint32_t sa = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * PAGE + ta * 16 + 4 * i);
+        const uint32_t sbw = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * PAGE + tb * 16 + 4 * i);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          // half2 index k' = 2kk + eps holds bits (k', k'+16) as +-1.0
+          const int k0 = 2 * kk, k1 = 2 * kk + 1;
+          const uint32_t a0 = ((sa << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
+          const uint32_t a1 = ((sbw << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
+          const uint32_t a2 = ((sa << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
+          const uint32_t a3 = ((sbw << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
+          mma16816(sacc, a0, a1, a2, a3, st.sb[kk][0], st.sb[kk][1]);
+        }
+        const __half* nrm = reinterpret_cast<const __half*>(kmeta);
+        const float na = __half2float(nrm[ta]), nb = __half2float(nrm[tb]);
+        const float ga = __half2float(nrm[PAGE + ta]), gb = __half2float(nrm[PAGE + tb]);
+        const float la = na * ((cacc[0] + cacc[1]) + QJL_CONST * ga * (sacc[0] + sacc[1]));
+        const float lb = nb * ((cacc[2] + cacc[3]) + QJL_CONST * gb * (sacc[2] + sacc[3]));
+        lg[mt][0] = (headok && ta < ntok) ? la : -INFINITY;
+        lg[mt][1] = (headok && tb < ntok) ? lb : -INFINITY;
+      } else {
+        const uint4 ka = *reinterpret_cast<const uint4*>(kmain + ta * 64 + 16 * i);
+        const uint4 kb = *reinterpret_cast<const uint4*>(kmain + tb * 64 + 16 * i);
+        float acc[4][4];
+#pragma unroll
+        for (int G = 0; G < 4; ++G) {
+          acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+          // group G's 8 channels of this thread: halfwords (2i, G) and (2i+1, G)
+          const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
+          const uint32_t wa = __byte_perm((G < 2) ? ka.x : ka.y, (G < 2) ? ka.z : ka.w, sel);
+          const uint32_t wb = __byte_perm((G < 2) ? kb.x : kb.y, (G < 2) ? kb.z : kb.w, sel);
+          uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+          nib8(wa, a04, a15, a26, a37);
+          nib8(wb, b04, b15, b26, b37);
+          mma16816(acc[G], a04, b04, a15, b15, st.qb[2 * G][0], st.qb[2 * G][1]);
+          mma16816(acc[G], a26, b26, a37, b37, st.qb[2 * G + 1][0], st.qb[2 * G + 1][1]);
+        }
+        const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
+        const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
+        const float2 sa01 = __half22float2(u2h(ma.x)), sa23 = __half22float2(u2h(ma.y));
+        const float2 za01 = __half22float2(u2h(ma.z)), za23 = __half22float2(u2h(ma.w));
+        const float2 sb01 = __half22float2(u2h(mb.x)), sb23 = __half22float2(u2h(mb.y));
+        const float2 zb01 = __half22float2(u2h(mb.z)), zb23 = __half22float2(u2h(mb.w));
+        float la = za01.x * st.qsum[0] + za01.y * st.qsum[1] + za23.x * st.qsum[2] + za23.y * st.qsum[3];
+        float lb = zb01.x * st.qsum[0] + zb01.y * st.qsum[1] + zb23.x * st.qsum[2] + zb23.y * st.qsum[3];
+        la += sa01.x * (acc[0][0] + acc[0][1]) + sa01.y * (acc[1][0] + acc[1][1]) +
+              sa23.x * (acc[2][0] + acc[2][1]) + sa23.y * (acc[3][0] + acc[3][1]);
+        lb += sb01.x * (acc[0][2] + acc[0][3]) + sb01.y * (acc[1][2] + acc[1][3]) +
+              sb23.x * (acc[2][2] + acc[2][3]) + sb23.y * (acc[3][2] + acc[3][3]);
+        lg[mt][0] = (headok && ta < ntok) ? la : -INFINITY;
+        lg[mt][1] = (headok && tb < ntok) ? lb : -INFINITY;
+      }
+    }
+
+    // ---- online softmax update for head i (rows r = 0..7 share it)
+    float mx = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(lg[mt][0], lg[mt][1]));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+    const float mnew = fmaxf(st.m, mx);
+    const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(st.m - mnew);
+    st.m = mnew;
+    float pr[4][2];
+    float psum = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        pr[mt][k] = (lg[mt][k] == -INFINITY) ? 0.f : exp2f(lg[mt][k] - mnew);
+        psum += pr[mt][k];
+      }
+    }
+    st.l = st.l * alpha + psum;
+    // accumulator columns 2i, 2i+1 are heads 2i, 2i+1: fetch their alpha from lanes (r, 2i), (r, 2i+1)
+    const float al0 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i) & 3));
+    const float al1 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i + 1) & 3));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      st.acc[j][0] *= al0;
+      st.acc[j][1] *= al1;
+      st.acc[j][2] *= al0;
+      st.acc[j][3] *= al1;
+    }
+    st.zacc[0] *= al0;
+    st.zacc[1] *= al1;
+    st.zacc[2] *= al0;
+    st.zacc[3] *= al1;
+
+    // ---- P.V: k-step = 16 tokens; this thread's B column is head r (r < g), tokens 2i, 2i+1, +8, +9
+    const bool colok = r < g;
+    const int src0 = 4 * (2 * i) + (r & 3), src1 = 4 * (2 * i + 1) + (r & 3);
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      const float pa0 = __shfl_sync(FULL, pr[mt][0], src0);  // token 16mt + 2i
+      const float pb0 = __shfl_sync(FULL, pr[mt][1], src0);  // token 16mt + 2i + 8
+      const float pa1 = __shfl_sync(FULL, pr[mt][0], src1);  // token 16mt + 2i + 1
+      const float pb1 = __shfl_sync(FULL, pr[mt][1], src1);  // token 16mt + 2i + 9
+      const int t0 = 16 * mt + 2 * i;
+      const bool full = ntok >= 16 * (mt + 1);
+      const bool okA0 = t0 < ntok, okA1 = t0 + 1 < ntok, okB0 = t0 + 8 < ntok, okB1 = t0 + 9 < ntok;
+      const uint32_t pA = colok ? h2u(__floats2half2_rn(pa0, pa1)) : 0u;
+      const uint32_t pB = colok ? h2u(__floats2half2_rn(pb0, pb1)) : 0u;
+      // z-term: rows = groups r (< 4), k = tokens: A = z, B = unscaled p
+      uint32_t zA = 0u, zB = 0u;
+      if (r < 4) {
+        zA = *reinterpret_cast<const uint32_t*>(vzero + r * PAGE + t0);
+        zB = *reinterpret_cast<const uint32_t*>(vzero + r * PAGE + t0 + 8);
+        if (!full) {
+          zA &= (okA0 ? 0x0000FFFFu : 0u) | (okA1 ? 0xFFFF0000u : 0u);
+          zB &= (okB0 ? 0x0000FFFFu : 0u) | (okB1 ? 0xFFFF0000u : 0u);
+        }
+      }
+      mma16816(st.zacc, zA, 0u, zB, 0u, pA, pB);
+      // V codes of the four tokens for channel rows r: 8 bytes = halfwords (r, G = 0..3)
+      const uint2 va = *reinterpret_cast<const uint2*>(vmain + t0 * 64 + 8 * r);
+      const uint2 vb = *reinterpret_cast<const uint2*>(vmain + (t0 + 1) * 64 + 8 * r);
+      const uint2 vc = *reinterpret_cast<const uint2*>(vmain + (t0 + 8) * 64 + 8 * r);
+      const uint2 vd = *reinterpret_cast<const uint2*>(vmain + (t0 + 9) * 64 + 8 * r);
+#pragma unroll
+      for (int G = 0; G < 4; ++G) {
+        // B operand for group G: p * scale (fp16), zero outside the valid tokens
+        uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * PAGE + t0);
+        uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * PAGE + t0 + 8);
+        uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
+        uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
+        if (!full) {
+          bA &= (okA0 ? 0x0000FFFFu : 0u) | (okA1 ? 0xFFFF0000u : 0u);
+          bB &= (okB0 ? 0x0000FFFFu : 0u) | (okB1 ? 0xFFFF0000u : 0u);
+        }
+        const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
+        const uint32_t wab = __byte_perm((G < 2) ? va.x : va.y, (G < 2) ? vb.x : vb.y, sel);
+        const uint32_t wcd = __byte_perm((G < 2) ? vc.x : vc.y, (G < 2) ? vd.x : vd.y, sel);
+        uint32_t ab0, ab1, ab2, ab3, cd0, cd1, cd2, cd3;
+        nib8(wab, ab0, ab1, ab2, ab3);  // channel 32G + 4r + {0, 1, 2, 3}, tokens (t0, t0 + 1)
+        nib8(wcd, cd0, cd1, cd2, cd3);  // same channels, tokens (t0 + 8, t0 + 9)
+        mma16816(st.acc[2 * G], ab0, ab1, cd0, cd1, bA, bB);
+        mma16816(st.acc[2 * G + 1], ab2, ab3, cd2, cd3, bA, bB);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- records and merge
+  __device__ __forceinline__ float* record(int u, int c, int w) const {
+    return a.records + ((size_t)(u + c) * NCW + w) * REC_FLOATS;
+  }
+
+  __device__ void write_window(float* rec, const WinState& ws) {
+#pragma unroll
+    for (int hh = 0; hh < MAX_GQA; ++hh)
+      if (hh < g && ws.l[hh] > 0.f)
+        *reinterpret_cast<float4*>(rec + 16 + MAX_GQA * D + hh * D + 4 * lane) =
+            make_float4(ws.acc[hh][0], ws.acc[hh][1], ws.acc[hh][2], ws.acc[hh][3]);
+  }
+
+  __device__ void write_quant(float* rec, QuantState& st) {
+    const int r = lane >> 2, i = lane & 3;
+    // fold the zero-point term into the accumulators: acc[h][c] += zterm[G(c)][h]
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      const float z0 = __shfl_sync(FULL, st.zacc[0], 4 * G + i);
+      const float z1 = __shfl_sync(FULL, st.zacc[1], 4 * G + i);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        st.acc[2 * G + e][0] += z0;
+        st.acc[2 * G + e][1] += z1;
+        st.acc[2 * G + e][2] += z0;
+        st.acc[2 * G + e][3] += z1;
+      }
+    }
+    float l = st.l;
+    l += __shfl_xor_sync(FULL, l, 4);
+    l += __shfl_xor_sync(FULL, l, 8);
+    l += __shfl_xor_sync(FULL, l, 16);
+    // heads 2i, 2i+1 in columns; channel of m-tile 2G+e row r is 32G + 4r + 2e, row r+8 adds 1
+    const bool anyl = __shfl_sync(FULL, l, 0) > 0.f || __shfl_sync(FULL, l, 1) > 0.f ||
+                      __shfl_sync(FULL, l, 2) > 0.f || __shfl_sync(FULL, l, 3) > 0.f;
+    if (anyl) {
+#pragma unroll
+      for (int cidx = 0; cidx < 2; ++cidx) {
+        const int hh = 2 * i + cidx;
+        if (hh < g) {
+          float* dst = rec + 16 + hh * D;
+#pragma unroll
+          for (int G = 0; G < 4; ++G)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c0 = 32 * G + 4 * r + 2 * e;
+              dst[c0] = st.acc[2 * G + e][cidx];
+              dst[c0 + 1] = st.acc[2 * G + e][2 + cidx];
+            }
+        }
+      }
+    }
+    st.l = l;  // every lane with head i now has the full sum
+  }
+
+  // header: [Qm[4], Ql[4], Wm[4], Wl[4]]
+  __device__ void write_header(float* rec, bool hasq, const QuantState& st, bool hasw, const WinState& ws) {
+    const int k = lane & 3;
+    const float qm = __shfl_sync(FULL, st.m, k);
+    const float ql = __shfl_sync(FULL, st.l, k);
+    float wm = ws.m[0], wl = ws.l[0];
+#pragma unroll
+    for (int kk = 1; kk < MAX_GQA; ++kk)
+      if (k == kk) {
+        wm = ws.m[kk];
+        wl = ws.l[kk];
+      }
+    float v;
+    if (lane < 4) v = hasq ? qm : -INFINITY;
+    else if (lane < 8) v = hasq ? ql : 0.f;
+    else if (lane < 12) v = hasw ? wm : -INFINITY;
+    else v = hasw ? wl : 0.f;
+    if (lane < 16) rec[lane] = v;
+  }
+
+  __device__ void merge(int u) {
+    const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+    const int layer = a.layer0 + ll;
+    const long long sb = steps_before(ll, b, h);
+    const int cf = owner(sb), cl = owner(sb + sq.S[b] - 1);
+    for (int hh = 0; hh < g; ++hh) {
+      float part[2][4];
+      float Mx[2], Lx[2];
+#pragma unroll
+      for (int kind = 0; kind < 2; ++kind) {  // 0 = quantised (rotated space), 1 = window
+        const int mo = kind ? 8 : 0, lo = kind ? 12 : 4;
+        const int ao = 16 + (kind ? MAX_GQA * D : 0) + hh * D + 4 * lane;
+        float M = -INFINITY;
+        for (int c = cf; c <= cl; ++c)
+          for (int w = 0; w < NCW; ++w) {
+            const float* rec = record(u, c, w);
+            if (__ldcg(rec + lo + hh) > 0.f) M = fmaxf(M, __ldcg(rec + mo + hh));
+          }
+        float L = 0.f;
+        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c = cf; c <= cl; ++c)
+          for (int w = 0; w < NCW; ++w) {
+            const float* rec = record(u, c, w);
+            const float l = __ldcg(rec + lo + hh);
+            if (l > 0.f) {
+              const float f = exp2f(__ldcg(rec + mo + hh) - M);
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(rec + ao));
+              L += l * f;
+              A.x += f * x.x;
+              A.y += f * x.y;
+              A.z += f * x.z;
+              A.w += f * x.w;
+            }
+          }
+        Mx[kind] = M;
+        Lx[kind] = L;
+        part[kind][0] = A.x;
+        part[kind][1] = A.y;
+        part[kind][2] = A.z;
+        part[kind][3] = A.w;
+      }
+      if (Lx[0] > 0.f) {
+        // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
+        if (a.sinkhorn) {
+          const __half* sig = a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) part[0][e] *= __half2float(sig[e]);
+        }
+        hadamard_warp(part[0][0], part[0][1], part[0][2], part[0][3], lane);
+        const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+        part[0][0] *= C_WHT * sg.x;
+        part[0][1] *= C_WHT * sg.y;
+        part[0][2] *= C_WHT * sg.z;
+        part[0][3] *= C_WHT * sg.w;
+      }
+      const float M = fmaxf(Lx[0] > 0.f ? Mx[0] : -INFINITY, Lx[1] > 0.f ? Mx[1] : -INFINITY);
+      const float f0 = Lx[0] > 0.f ? exp2f(Mx[0] - M) : 0.f;
+      const float f1 = Lx[1] > 0.f ? exp2f(Mx[1] - M) : 0.f;
+      const float den = Lx[0] * f0 + Lx[1] * f1;
+      const float inv = den > 0.f ? 1.f / den : 0.f;
+      float4 o;
+      o.x = (part[0][0] * f0 + part[1][0] * f1) * inv;
+      o.y = (part[0][1] * f0 + part[1][1] * f1) * inv;
+      o.z = (part[0][2] * f0 + part[1][2] * f1) * inv;
+      o.w = (part[0][3] * f0 + part[1][3] * f1) * inv;
+      *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * Hq + (size_t)h * g + hh) * D + 4 * lane) = o;
+    }
+  }
+
+  // publish this warp's record for unit u and merge if it was the last one
+  __device__ void arrive(int u) {
+    const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+    const long long sb = steps_before(ll, b, h);
+    const int ncta = owner(sb + sq.S[b] - 1) - owner(sb) + 1;
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) {
+      __threadfence();
+      old = atomicAdd(a.counters + u, 1);
+    }
+    old = __shfl_sync(FULL, old, 0);
+    if (old == NCW * ncta - 1) {
+      __threadfence();
+      merge(u);
+      if (lane == 0) a.counters[u] = 0;
+    }
+  }
+
+  __device__ void emit_empty(int u, int c) {
+    float* rec = record(u, c, warp);
+    if (lane < 16) rec[lane] = ((lane & 7) < 4) ? -INFINITY : 0.f;
+    arrive(u);
+  }
+};
+
+template <int KF>
+__global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  Kernel<KF> K(a, smem);
+  const int tid = threadIdx.x;
+  K.warp = tid >> 5;
+  K.lane = tid & 31;
+  K.B = a.batch;
+  K.H = a.Hkv;
+  K.W = a.W;
+  K.g = a.g;
+  K.Hq = a.Hkv * a.g;
+  const int B = a.batch, H = a.Hkv, W = a.W;
+  int* sS = reinterpret_cast<int*>(smem + SM_SEQ);
+  int* sPre = sS + (B + 1);
+  int* sL = sPre + (B + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM_BARS);
+  uint64_t* empty = full + NSTAGE;
+  int4* desc = reinterpret_cast<int4*>(smem + SM_DESC);
+
+  // ---- per-sequence step counts: window chunks first, then quantised pages
+  for (int b = tid; b < B; b += NTHREADS) {
+    int L = a.seq_lens[b];
+    if (L < 0 || L > a.max_seq_len) {
+      if (blockIdx.x == 0) atomicOr(a.p.status, KVQ_DEV_SEQLEN_RANGE);
+      L = 0;
+    }
+    const int Lq = W > 0 ? max(0, L - W) : L;
+    const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
+    sL[b] = L;
+    sS[b] = nw + (Lq + PAGE - 1) / PAGE;
+  }
+  __syncthreads();
+  if (K.warp == 0) {
+    const int lane = K.lane;
+    const int per = (B + 31) / 32, b0 = lane * per, b1 = min(B, b0 + per);
+    int s = 0;
+    for (int b = b0; b < b1; ++b) s += sS[b];
+    int incl = s;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULL, incl, o);
+      if (lane >= o) incl += y;
+    }
+    int run = incl - s;
+    for (int b = b0; b < b1; ++b) {
+      sPre[b] = run;
+      run += sS[b];
+    }
+    if (lane == 31) sPre[B] = incl;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NSTAGE; ++i) {
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (KF == KVQ_TQ3_QJL) {
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + SM_LUT);
+    for (int idx = tid; idx < 64 * 32; idx += NTHREADS) lut[idx] = a.p.cb->lut[idx >> 5];
+  }
+  __syncthreads();
+  K.sq.S = sS;
+  K.sq.pre = sPre;
+  K.sq.L = sL;
+
+  // empty sequences produce zeros (no step belongs to them)
+  if (blockIdx.x == 0) {
+    for (int b = K.warp; b < B; b += NCW + 1)
+      if (sL[b] == 0)
+        for (int ll = 0; ll < a.n_layers_call; ++ll)
+          for (int hq = 0; hq < K.Hq; ++hq)
+            *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * K.Hq + hq) * D + 4 * K.lane) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  K.S_layer = (long long)H * sPre[B];
+  K.S = K.S_layer * a.n_layers_call;
+  if (K.S == 0) return;
+  K.nct = min((long long)gridDim.x, K.S);
+  if (blockIdx.x >= K.nct) return;
+  const long long x0 = (long long)blockIdx.x * K.S / K.nct;
+  const long long x1 = (long long)(blockIdx.x + 1) * K.S / K.nct;
+  const int n = (int)(x1 - x0);
+
+  if (K.warp == NCW) {
+    // ======================= producer
+    if (K.lane == 0) {
+      Pos ps = locate(x0, K.S_layer, B, H, K.sq);
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int slot = k % NSTAGE;
+        if (k >= NSTAGE && !mbar_wait(empty + slot, ((k / NSTAGE) - 1) & 1, a.p.status)) break;
+        const int u = (ps.ll * B + ps.b) * H + ps.h;
+        const int layer = a.layer0 + ps.ll;
+        const int L = sL[ps.b];
+        const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
+        uint8_t* dst = smem + SM_STAGES + slot * STAGE_BYTES;
+        if (ps.local < nw) {
+          const int s0 = ps.local * WCHUNK;
+          const int ntok = min(WCHUNK, min(L, W) - s0);
+          desc[slot] = make_int4(u, KIND_WINDOW, ntok, ps.local);
+          const size_t ro = ((((size_t)layer * a.max_batch + ps.b) * H + ps.h) * W + s0) * D;
+          mbar_arrive_tx(full + slot, 2 * WCHUNK * D * 4);
+          bulk_g2s(dst, a.p.ringk + ro, WCHUNK * D * 4, full + slot);
+          bulk_g2s(dst + WCHUNK * D * 4, a.p.ringv + ro, WCHUNK * D * 4, full + slot);
+        } else {
+          const int pi = ps.local - nw;
+          const int Lq = max(0, L - W);
+          const int Lqq = W > 0 ? Lq : L;
+          int ntok = min(PAGE, Lqq - pi * PAGE);
+          const int phys = a.block_table[(size_t)ps.b * a.max_pages_per_seq + pi];
+          if (phys < 0 || phys >= a.L.n_pages) {
+            atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
+            desc[slot] = make_int4(u, KIND_QUANT, 0, ps.local);
+            mbar_arrive(full + slot);
+          } else {
+            desc[slot] = make_int4(u, KIND_QUANT, ntok, ps.local);
+            const uint8_t* src =
+                a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + ps.h) * (size_t)a.L.page_bytes;
+            mbar_arrive_tx(full + slot, a.L.page_bytes);
+            bulk_g2s(dst, src, a.L.page_bytes, full + slot);
+          }
+        }
+        ++issued;
+        if (k + 1 < n) {
+          ps.local++;
+          if (ps.local == sS[ps.b]) {
+            ps.local = 0;
+            if (++ps.h == H) {
+              ps.h = 0;
+              do {
+                if (++ps.b == B) {
+                  ps.b = 0;
+                  ps.ll++;
+                }
+              } while (sS[ps.b] == 0);
+            }
+          }
+        }
+      }
+      // never leave the CTA with a copy still landing in shared memory
+      for (int k = max(0, issued - NSTAGE); k < issued; ++k)
+        mbar_wait(full + (k % NSTAGE), (k / NSTAGE) & 1, a.p.status);
+    }
+    return;
+  }
+
+  // ======================= consumers
+  const Pos pf = locate(x0, K.S_layer, B, H, K.sq);
+  const Pos pl = locate(x1 - 1, K.S_layer, B, H, K.sq);
+  const int u_first = (pf.ll * B + pf.b) * H + pf.h;
+  const int u_last = (pl.ll * B + pl.b) * H + pl.h;
+  const int c = blockIdx.x;
+  QuantState st;
+  WinState ws;
+  int cur = -1, kind = -1;
+  bool hasq = false, hasw = false;
+  int u_next = u_first;
+  auto unit_steps = [&](int u) { return sS[(u / H) % B]; };
+  auto finish = [&](int u) {
+    float* rec = K.record(u, c, K.warp);
+    if (kind == KIND_QUANT) K.write_quant(rec, st);
+    if (kind == KIND_WINDOW) K.write_window(rec, ws);
+    K.write_header(rec, hasq, st, hasw, ws);
+    K.arrive(u);
+  };
+  for (int k = K.warp; k < n; k += NCW) {
+    const int slot = k % NSTAGE;
+    if (!mbar_wait(full + slot, (k / NSTAGE) & 1, a.p.status)) break;
+    const int4 d = desc[slot];
+    if (d.x != cur) {
+      if (cur >= 0) finish(cur);
+      for (int u = (cur >= 0 ? cur + 1 : u_next); u < d.x; ++u)
+        if (unit_steps(u) > 0) K.emit_empty(u, c);
+      cur = d.x;
+      u_next = cur + 1;
+      kind = -1;
+      hasq = hasw = false;
+    }
+    if (d.y != kind) {
+      if (kind == KIND_WINDOW) K.write_window(K.record(cur, c, K.warp), ws);
+      K.load_q(cur, st, ws, d.y);
+      kind = d.y;
+      if (kind == KIND_WINDOW) hasw = true;
+      else hasq = true;
+    }
+    const uint8_t* stage = smem + SM_STAGES + slot * STAGE_BYTES;
+    if (d.z > 0) {
+      if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws);
+      else K.quant_step(stage, d.z, st);
+    }
+    __syncwarp();
+    if (K.lane == 0) mbar_arrive(empty + slot);
+  }
+  if (cur >= 0) finish(cur);
+  for (int u = (cur >= 0 ? cur + 1 : u_next); u <= u_last; ++u)
+    if (unit_steps(u) > 0) K.emit_empty(u, c);
+}
+
+}  // namespace
+
+size_t decode_scratch_bytes(int n_units, int n_ctas) {
+  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + n_ctas) * NCW * REC_FLOATS * sizeof(float);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
+  const size_t smem = SM_FIXED + 3 * (size_t)(a.batch + 1) * sizeof(int);
+  cudaError_t e;
+  if (a.k_format == KVQ_TQ3_QJL) {
+    e = cudaFuncSetAttribute(decode_kernel<KVQ_TQ3_QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_kernel<KVQ_TQ3_QJL><<<a.n_ctas, NTHREADS, smem, s>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(decode_kernel<KVQ_Q4G32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_kernel<KVQ_Q4G32><<<a.n_ctas, NTHREADS, smem, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

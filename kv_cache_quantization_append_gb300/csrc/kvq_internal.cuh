@@ -1,0 +1,155 @@
+// Internal definitions shared by the translation units of libkvq: buffer layout, kernel
+// parameter blocks, and small device helpers (warp Walsh-Hadamard butterfly, input loads).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int D = 128;           // head_dim
+constexpr int PAGE = 64;         // tokens per page
+constexpr int WCHUNK = 8;        // window slots per pipeline stage
+constexpr int MAX_WINDOW = 1024;
+constexpr int MAX_GQA = 4;
+constexpr int MAX_BATCH = 1024;
+constexpr uint32_t MAGIC = 0x4b565131u;  // "KVQ1"
+constexpr unsigned FULL = 0xffffffffu;
+
+// float32 round-to-nearest of 2^-3.5 = 1/sqrt(128)
+constexpr float C_WHT = 0.0883883461356163f;
+// log2(e) / sqrt(128): logits are kept in base-2 units so the softmax uses exp2
+constexpr float LOGIT_SCALE = 0.127517431974411f;
+// sqrt(pi / 2) / 128: QJL inner-product estimator constant for m = 128 projections
+constexpr float QJL_CONST = 0.009791516698896885f;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t off_status, off_signs, off_cb, off_qjl, off_sigk, off_sigv, off_bt;
+  size_t off_ringk, off_ringv, off_pages, total;
+  int max_pages_per_seq, n_pages;
+  int page_bytes, off_vmain, off_kmeta, off_vmeta, kmeta_bytes;  // within a page
+};
+
+// codebook block inside the header
+struct CodebookDev {
+  __half cent[8];        // TQ3 centroids (ascending)
+  float bnd[8];          // 7 boundaries (midpoints), [7] unused
+  uint32_t lut[64];      // half2 (cent[i & 7], cent[i >> 3]) for a pair of 3-bit codes
+};
+
+bool compute_layout(const kvq_config& c, Layout* L);
+
+struct DevPtrs {
+  unsigned* status;
+  const float* signs;
+  const CodebookDev* cb;
+  const float* qjl_t;     // transposed projection: qjl_t[j][i] = S[i][j]
+  __half* sigk;           // [L][H][128]
+  __half* sigv;
+  float* ringk;
+  float* ringv;
+  uint8_t* pages;
+};
+
+DevPtrs dev_ptrs(const kvq_cache& c, const Layout& L);
+
+// ---------------------------------------------------------------- launchers
+struct AppendArgs {
+  DevPtrs p;
+  Layout L;
+  const int32_t* block_table;
+  const void* k;
+  const void* v;
+  const int32_t* pos;
+  int layer0, n_layers_call, batch, max_batch, T, Hkv, W, max_seq_len, k_format, sinkhorn, in_bf16;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+
+struct CalibArgs {
+  DevPtrs p;
+  const void* kc;
+  const void* vc;
+  float* work;            // [n_layers_call][Hkv][2][ntok][128]
+  int layer0, n_layers_call, Hkv, ntok, in_bf16;
+};
+cudaError_t launch_calibrate(const CalibArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  DevPtrs p;
+  Layout L;
+  const int32_t* block_table;
+  const void* q;
+  float* out;
+  const int32_t* seq_lens;
+  int* counters;
+  float* records;
+  int layer0, n_layers_call, batch, max_batch, Hkv, g, W, max_seq_len, k_format, sinkhorn, in_bf16;
+  int max_pages_per_seq, n_units, n_ctas;
+};
+int decode_ctas(int device);
+size_t decode_scratch_bytes(int n_units, int n_ctas);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+__device__ __forceinline__ float4 load4_in(const void* base, size_t elem_off, int bf16) {
+  if (bf16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem_off);
+    float4 r;
+    r.x = __uint_as_float(u.x << 16);
+    r.y = __uint_as_float(u.x & 0xffff0000u);
+    r.z = __uint_as_float(u.y << 16);
+    r.w = __uint_as_float(u.y & 0xffff0000u);
+    return r;
+  }
+  return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
+}
+
+// Unnormalised Hadamard butterfly over a warp: lane l holds elements 4l..4l+3.  Stages
+// h = 1, 2 inside the lane, h = 4..64 across lanes (xor 1..16); every add/sub rounds once.
+__device__ __forceinline__ void hadamard_warp(float& x0, float& x1, float& x2, float& x3, int lane) {
+  float a0 = __fadd_rn(x0, x1), a1 = __fsub_rn(x0, x1);
+  float a2 = __fadd_rn(x2, x3), a3 = __fsub_rn(x2, x3);
+  x0 = __fadd_rn(a0, a2);
+  x2 = __fsub_rn(a0, a2);
+  x1 = __fadd_rn(a1, a3);
+  x3 = __fsub_rn(a1, a3);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float y0 = __shfl_xor_sync(FULL, x0, m);
+    const float y1 = __shfl_xor_sync(FULL, x1, m);
+    const float y2 = __shfl_xor_sync(FULL, x2, m);
+    const float y3 = __shfl_xor_sync(FULL, x3, m);
+    if (lane & m) {
+      x0 = __fsub_rn(y0, x0);
+      x1 = __fsub_rn(y1, x1);
+      x2 = __fsub_rn(y2, x2);
+      x3 = __fsub_rn(y3, x3);
+    } else {
+      x0 = __fadd_rn(x0, y0);
+      x1 = __fadd_rn(x1, y1);
+      x2 = __fadd_rn(x2, y2);
+      x3 = __fadd_rn(x3, y3);
+    }
+  }
+}
+
+// Fixed-order float32 sum of squares of a warp-held 128-vector: per lane
+// ((x0^2 + x1^2) + (x2^2 + x3^2)), then halving over lanes (xor 16, 8, 4, 2, 1).  Every lane
+// ends with the same value.
+__device__ __forceinline__ float sumsq_warp(float x0, float x1, float x2, float x3) {
+  float s = __fadd_rn(__fadd_rn(__fmul_rn(x0, x0), __fmul_rn(x1, x1)),
+                      __fadd_rn(__fmul_rn(x2, x2), __fmul_rn(x3, x3)));
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) s = __fadd_rn(s, __shfl_xor_sync(FULL, s, m));
+  return s;
+}
+#endif
+
+}  // namespace kvq

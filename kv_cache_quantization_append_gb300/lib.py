@@ -1,0 +1,175 @@
+"""ctypes binding of libkvq (the C ABI in include/kvq.h): argument marshalling only.
+
+Every function here has the name of the C entry point it calls and does nothing but check tensor
+properties, take ``data_ptr()`` and the current CUDA stream, and translate status codes into
+exceptions.  All computation happens in the library's CUDA kernels; there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libkvq.so")
+
+KVQ_Q4G32 = 1
+KVQ_TQ3_QJL = 3
+KVQ_IN_F32 = 0
+KVQ_IN_BF16 = 1
+
+DEV_BAD_PAGE = 1
+DEV_POS_RANGE = 2
+DEV_SEQLEN_RANGE = 4
+DEV_TIMEOUT = 8
+
+EXPORTS = ("kv_cache_bytes", "kv_cache_init", "kv_calibrate_scratch_bytes", "kv_calibrate",
+           "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention", "kv_status",
+           "kv_strerror")
+
+
+class kvq_config(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("max_batch", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
+                ("window", ctypes.c_int32), ("page_tokens", ctypes.c_int32),
+                ("n_pages", ctypes.c_int32), ("k_format", ctypes.c_int32),
+                ("v_format", ctypes.c_int32), ("sinkhorn", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
+                ("seed", ctypes.c_uint64)]
+
+
+class kvq_cache(ctypes.Structure):
+    _fields_ = [("cfg", kvq_config), ("dev", ctypes.c_void_p), ("bytes", ctypes.c_uint64),
+                ("block_table", ctypes.c_void_p), ("max_pages_per_seq", ctypes.c_int32),
+                ("n_pages", ctypes.c_int32), ("device", ctypes.c_int32), ("magic", ctypes.c_uint32)]
+
+
+class KVQError(RuntimeError):
+    pass
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkvq.so; raises if it has not been built (there is no CPU fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise KVQError(f"libkvq.so not built ({path}); run __graft_entry__.build() first")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ, U32P = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.POINTER(ctypes.c_uint32)
+    cfgp, cachep = ctypes.POINTER(kvq_config), ctypes.POINTER(kvq_cache)
+    sig = {
+        "kv_cache_bytes": (SZ, [cfgp]),
+        "kv_cache_init": (ctypes.c_int, [cachep, cfgp, P, SZ, P, P, P]),
+        "kv_calibrate_scratch_bytes": (SZ, [cachep, I32, I32]),
+        "kv_calibrate": (ctypes.c_int, [cachep, I32, P, P, I32, P, SZ, P]),
+        "kv_quant_append": (ctypes.c_int, [cachep, I32, P, P, P, I32, I32, P]),
+        "kv_decode_scratch_bytes": (SZ, [cachep, I32, I32]),
+        "kv_decode_attention": (ctypes.c_int, [cachep, I32, P, P, P, I32, P, SZ, P]),
+        "kv_status": (ctypes.c_int, [cachep, U32P, P]),
+        "kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise KVQError(f"libkvq: {load().kv_strerror(rc).decode()} (code {rc})")
+
+
+def _stream(stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    if t is None:
+        return ctypes.c_void_p(0)
+    if not t.is_cuda:
+        raise KVQError("device tensor expected")
+    if not t.is_contiguous():
+        raise KVQError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def make_config(n_layers, n_kv_heads, n_q_heads, max_batch, max_seq_len, window=128, n_pages=0,
+                k_format=KVQ_Q4G32, v_format=KVQ_Q4G32, sinkhorn=False, in_dtype=KVQ_IN_BF16,
+                seed=0) -> kvq_config:
+    return kvq_config(n_layers, n_kv_heads, n_q_heads, 128, max_batch, max_seq_len, window, 64,
+                      n_pages, k_format, v_format, int(bool(sinkhorn)), 32, in_dtype, seed)
+
+
+def kv_cache_bytes(cfg: kvq_config) -> int:
+    return int(load().kv_cache_bytes(ctypes.byref(cfg)))
+
+
+def kv_cache_init(cfg: kvq_config, dev_mem: torch.Tensor, block_table: torch.Tensor | None = None,
+                  qjl_proj: np.ndarray | None = None, stream=None) -> kvq_cache:
+    cache = kvq_cache()
+    proj = None
+    if qjl_proj is not None:
+        proj = np.ascontiguousarray(qjl_proj, dtype=np.float32)
+    pp = ctypes.c_void_p(proj.ctypes.data) if proj is not None else ctypes.c_void_p(0)
+    _check(load().kv_cache_init(ctypes.byref(cache), ctypes.byref(cfg), _ptr(dev_mem),
+                                dev_mem.numel() * dev_mem.element_size(), _ptr(block_table), pp,
+                                _stream(stream)))
+    return cache
+
+
+def kv_calibrate_scratch_bytes(cache: kvq_cache, layer: int, n_tokens: int) -> int:
+    return int(load().kv_calibrate_scratch_bytes(ctypes.byref(cache), layer, n_tokens))
+
+
+def kv_calibrate(cache: kvq_cache, layer: int, k_calib: torch.Tensor, v_calib: torch.Tensor,
+                 scratch: torch.Tensor, stream=None):
+    n_tokens = k_calib.shape[-2]
+    _check(load().kv_calibrate(ctypes.byref(cache), layer, _ptr(k_calib), _ptr(v_calib), n_tokens,
+                               _ptr(scratch), scratch.numel() * scratch.element_size(),
+                               _stream(stream)))
+
+
+def kv_quant_append(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch.Tensor,
+                    pos: torch.Tensor, stream=None):
+    """k, v: [L?][B][Hkv][T][128]; pos: int32 [B] on the device."""
+    if pos.dtype != torch.int32:
+        raise KVQError("pos must be int32")
+    B, T = k.shape[-4], k.shape[-2]
+    _check(load().kv_quant_append(ctypes.byref(cache), layer, _ptr(k), _ptr(v), _ptr(pos), B, T,
+                                  _stream(stream)))
+
+
+def kv_decode_scratch_bytes(cache: kvq_cache, layer: int, batch: int) -> int:
+    return int(load().kv_decode_scratch_bytes(ctypes.byref(cache), layer, batch))
+
+
+def kv_decode_attention(cache: kvq_cache, layer: int, q: torch.Tensor, out: torch.Tensor,
+                        seq_lens: torch.Tensor, scratch: torch.Tensor, stream=None):
+    """q: [L?][B][Hq][128]; out: float32 like q; seq_lens: int32 [B]; scratch: zeroed bytes."""
+    if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
+        raise KVQError("seq_lens must be int32 and out float32")
+    B = q.shape[-3]
+    _check(load().kv_decode_attention(ctypes.byref(cache), layer, _ptr(q), _ptr(out), _ptr(seq_lens),
+                                      B, _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                      _stream(stream)))
+
+
+def kv_status(cache: kvq_cache, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().kv_status(ctypes.byref(cache), ctypes.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def kv_strerror(code: int) -> str:
+    return load().kv_strerror(code).decode()

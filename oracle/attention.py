@@ -109,6 +109,8 @@ class OracleCache:
         B, H, T, _ = k.shape
         for b in range(B):
             p0 = int(pos[b])
+            if p0 < 0:              # sequence not part of this append
+                continue
             assert p0 + T <= cfg.max_seq_len
             sl = slice(p0, p0 + T)
             for h in range(H):

@@ -1,0 +1,104 @@
+"""Read a cache buffer back into the oracle's per-position arrays (test helper, layout only).
+
+Follows the buffer layout documented in include/kvq.h: 256-byte aligned regions, the header first,
+then ring_k, ring_v and the pages; the offsets below are derived from the end of the buffer, which
+is exactly the pages region.  No arithmetic of the method happens here -- only bit unpacking.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+P = 64
+
+
+def _a256(x: int) -> int:
+    return (x + 255) & ~255
+
+
+def regions(cfg, total: int) -> dict:
+    tq = cfg.k_format == 3
+    kmeta = 4 if tq else 16
+    page_bytes = 128 * P + kmeta * P + 16 * P
+    maxpps = -(-cfg.max_seq_len // P)
+    n_pages = cfg.n_pages or cfg.max_batch * maxpps
+    pages = cfg.n_layers * n_pages * cfg.n_kv_heads * page_bytes
+    assert pages % 256 == 0
+    off_pages = total - pages
+    ring = _a256(cfg.n_layers * cfg.max_batch * cfg.n_kv_heads * cfg.window * 128 * 4)
+    off_ringv = off_pages - ring
+    off_ringk = off_ringv - ring
+    off_bt = off_ringk - _a256(cfg.max_batch * maxpps * 4)
+    sig = _a256(cfg.n_layers * cfg.n_kv_heads * 128 * 2)
+    off_sigv = off_bt - sig
+    off_sigk = off_sigv - sig
+    return dict(page_bytes=page_bytes, n_pages=n_pages, maxpps=maxpps, off_pages=off_pages,
+                off_ringk=off_ringk, off_ringv=off_ringv, off_sigk=off_sigk, off_sigv=off_sigv,
+                kmeta=kmeta, off_bt=off_bt)
+
+
+def _gather(buf: torch.Tensor, starts: np.ndarray, n: int) -> np.ndarray:
+    idx = torch.as_tensor(starts, dtype=torch.int64, device=buf.device)[:, None] + \
+        torch.arange(n, dtype=torch.int64, device=buf.device)[None, :]
+    return buf[idx.reshape(-1)].reshape(len(starts), n).cpu().numpy()
+
+
+def _q4_codes(rec: np.ndarray) -> np.ndarray:
+    """rec [T][64] bytes -> codes [T][128]: halfword (r, G) at byte 8r + 2G = channels 32G+4r..+3."""
+    hw = rec.reshape(-1, 8, 4, 2).astype(np.uint16)
+    hw = hw[..., 0] | (hw[..., 1] << 8)                        # [T][r][G]
+    nib = (hw[..., None] >> (4 * np.arange(4, dtype=np.uint16))) & 15   # [T][r][G][e]
+    return nib.transpose(0, 2, 1, 3).reshape(-1, 128).astype(np.uint8)   # channel 32G + 4r + e
+
+
+def _tq3_codes(rec: np.ndarray) -> np.ndarray:
+    bits = np.unpackbits(rec, axis=1, bitorder="little")[:, :384].reshape(-1, 128, 3)
+    return (bits[..., 0] | (bits[..., 1] << 1) | (bits[..., 2] << 2)).astype(np.uint8)
+
+
+def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
+              block_table: np.ndarray | None = None) -> dict:
+    """Quantised records of positions [0, n_tokens) of one (layer, sequence, kv-head)."""
+    R = regions(cfg, buf.numel())
+    if block_table is None:
+        block_table = np.arange(cfg.max_batch * R["maxpps"]).reshape(cfg.max_batch, R["maxpps"])
+    pos = np.arange(n_tokens)
+    phys = block_table[b, pos // P].astype(np.int64)
+    pg = R["off_pages"] + ((layer * R["n_pages"] + phys) * cfg.n_kv_heads + h) * R["page_bytes"]
+    tin = pos % P
+    out = {}
+    kmeta0 = pg + 128 * P
+    vmeta0 = kmeta0 + R["kmeta"] * P
+    if cfg.k_format == 3:
+        out["k_code"] = _tq3_codes(_gather(buf, pg + tin * 48, 48))
+        sg = _gather(buf, pg + 48 * P + tin * 16, 16)
+        out["k_bits"] = np.unpackbits(sg, axis=1, bitorder="little").astype(bool)
+        out["k_norm"] = _gather(buf, kmeta0 + tin * 2, 2).view(np.float16)[:, 0]
+        out["k_gamma"] = _gather(buf, kmeta0 + 2 * P + tin * 2, 2).view(np.float16)[:, 0]
+    else:
+        out["k_code"] = _q4_codes(_gather(buf, pg + tin * 64, 64))
+        m = _gather(buf, kmeta0 + tin * 16, 16).view(np.float16)
+        out["k_scale"], out["k_zero"] = m[:, :4], m[:, 4:]
+    out["v_code"] = _q4_codes(_gather(buf, pg + 64 * P + tin * 64, 64))
+    sc = np.stack([_gather(buf, vmeta0 + (G * P + tin) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
+    zr = np.stack([_gather(buf, vmeta0 + 512 + (G * P + tin) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
+    out["v_scale"], out["v_zero"] = sc, zr
+    return out
+
+
+def read_ring(buf: torch.Tensor, cfg, layer: int, b: int, h: int):
+    R = regions(cfg, buf.numel())
+    n = cfg.window * 128 * 4
+    o = (((layer * cfg.max_batch + b) * cfg.n_kv_heads + h) * cfg.window) * 128 * 4
+    k = buf[R["off_ringk"] + o: R["off_ringk"] + o + n].cpu().numpy().view(np.float32).reshape(cfg.window, 128)
+    v = buf[R["off_ringv"] + o: R["off_ringv"] + o + n].cpu().numpy().view(np.float32).reshape(cfg.window, 128)
+    return k, v
+
+
+def read_sigma(buf: torch.Tensor, cfg):
+    R = regions(cfg, buf.numel())
+    n = cfg.n_layers * cfg.n_kv_heads * 128 * 2
+    sk = buf[R["off_sigk"]: R["off_sigk"] + n].cpu().numpy().view(np.float16).reshape(cfg.n_layers, cfg.n_kv_heads, 128)
+    sv = buf[R["off_sigv"]: R["off_sigv"] + n].cpu().numpy().view(np.float16).reshape(cfg.n_layers, cfg.n_kv_heads, 128)
+    return sk, sv

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded inputs.
+
+Codes, scales, zeros, norms, sign bits, Sinkhorn scales and ring contents must match bit for bit;
+attention outputs within 2e-3 of max |out| of the float64 oracle, per layer.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from kv_cache_quantization_append_gb300 import synth
+
+from . import harness, layout
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(w, layer, B, H, Hq, T, t0=0):
+    k, v = synth.kv_tokens(w, layer, B, H, t0, T, device="cuda")
+    return k, v
+
+
+def _decode_both(gpu, ora, layer, q, seq_lens_np):
+    sl = torch.as_tensor(seq_lens_np, dtype=torch.int32, device="cuda")
+    out = gpu.decode(layer, q, sl)
+    torch.cuda.synchronize()
+    assert gpu.status() == 0
+    want = ora.decode(layer, harness.to_np(q), seq_lens_np)
+    return harness.to_np(out), want
+
+
+def test_tiny_reference_workload(gpu_lib):
+    """1 layer, 4 query heads on 1 kv head, 512 tokens, fp32, K channels 0-3 x10, window 128."""
+    w = synth.WORKLOADS["tiny"]
+    gpu, ora, _ = harness.make_pair(1, 1, 4, 1, 512, window=128, in_dtype="f32", seed=0)
+    k, v = _inputs(w, 0, 1, 1, 4, 512)
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu.append(0, k, v, pos)
+    ora.append(0, harness.to_np(k), harness.to_np(v), np.array([0]))
+    harness.compare_codes(gpu, ora, 0, 0, 0, 512)
+    harness.compare_ring(gpu, ora, 0, 0, 0, 512)
+    q = synth.queries(w, 0, 1, 4, device="cuda")
+    got, want = _decode_both(gpu, ora, 0, q, np.array([512]))
+    harness.assert_attention_close(got, want)
+
+
+def test_bulk_append_equals_token_by_token(gpu_lib):
+    """[QC] v3.2: a T-token append writes exactly the bytes of T single-token appends."""
+    w = synth.WORKLOADS["llama3.2-3b-32k"]
+    a, _, _ = harness.make_pair(1, 2, 6, 2, 400, window=128)
+    b, _, _ = harness.make_pair(1, 2, 6, 2, 400, window=128)
+    k, v = _inputs(w, 0, 2, 2, 6, 300)
+    a.append(0, k, v, torch.tensor([5, 50], dtype=torch.int32, device="cuda"))
+    for t in range(300):
+        b.append(0, k[:, :, t:t + 1].contiguous(), v[:, :, t:t + 1].contiguous(),
+                 torch.tensor([5 + t, 50 + t], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    R = layout.regions(a.cfg, a.buffer.numel())
+    # pages and ring of positions actually written must be identical; compare via the readers
+    for s, p0 in ((0, 5), (1, 50)):
+        for h in range(2):
+            ua = layout.read_unit(a.buffer, a.cfg, 0, s, h, p0 + 300)
+            ub = layout.read_unit(b.buffer, b.cfg, 0, s, h, p0 + 300)
+            for name in ua:
+                assert np.array_equal(ua[name][p0:].view(np.uint8), ub[name][p0:].view(np.uint8)), name
+            ka, va = layout.read_ring(a.buffer, a.cfg, 0, s, h)
+            kb, vb = layout.read_ring(b.buffer, b.cfg, 0, s, h)
+            assert np.array_equal(ka.view(np.uint32), kb.view(np.uint32))
+            assert np.array_equal(va.view(np.uint32), vb.view(np.uint32))
+    assert R["page_bytes"] == 10240
+
+
+@pytest.mark.parametrize("window", [128, 0, 64])
+def test_ragged_edge_lengths(gpu_lib, window):
+    lens = np.array([0, 1, 7, 63, 64, 65, 127, 128, 129, 191, 192, 200, 700, 1100], dtype=np.int32)
+    B = len(lens)
+    w = synth.WORKLOADS["dense27b-ragged-b32"]
+    gpu, ora, _ = harness.make_pair(1, 2, 4, B, 1152, window=window)
+    T = int(lens.max())
+    k, v = _inputs(w, 0, B, 2, 4, T)
+    gpu.append(0, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    ora.append(0, harness.to_np(k), harness.to_np(v), np.zeros(B, np.int64))
+    q = synth.queries(w, 0, B, 4, device="cuda")
+    got, want = _decode_both(gpu, ora, 0, q, lens)
+    for b in range(B):
+        if lens[b] == 0:
+            assert np.all(got[b] == 0)
+        else:
+            harness.assert_attention_close(got[b], want[b])
+
+
+def test_multilayer_gqa3_all_layers_call(gpu_lib):
+    """Llama-3.2-3B-shaped (GQA 3) at small size: one launch over all layers and per-layer calls."""
+    w = synth.WORKLOADS["llama3.2-3b-32k"]
+    Lyr, H, Hq, L = 3, 2, 6, 1500
+    gpu, ora, _ = harness.make_pair(Lyr, H, Hq, 1, 2048, window=128)
+    ks, vs = zip(*[_inputs(w, l, 1, H, Hq, L) for l in range(Lyr)])
+    k, v = torch.stack(ks), torch.stack(vs)
+    gpu.append(-1, k, v, torch.zeros(1, dtype=torch.int32, device="cuda"))
+    for l in range(Lyr):
+        ora.append(l, harness.to_np(ks[l]), harness.to_np(vs[l]), np.array([0]))
+        for h in range(H):
+            harness.compare_codes(gpu, ora, l, 0, h, L)
+            harness.compare_ring(gpu, ora, l, 0, h, L)
+    q = torch.stack([synth.queries(w, l, 1, Hq, device="cuda") for l in range(Lyr)])
+    sl = np.array([L], dtype=np.int32)
+    out = gpu.decode(-1, q, torch.as_tensor(sl, device="cuda"))
+    torch.cuda.synchronize()
+    for l in range(Lyr):
+        want = ora.decode(l, harness.to_np(q[l]), sl)
+        harness.assert_attention_close(harness.to_np(out[l]), want)
+        one = gpu.decode(l, q[l].contiguous(), torch.as_tensor(sl, device="cuda"))
+        torch.cuda.synchronize()
+        harness.assert_attention_close(harness.to_np(one), want)
+
+
+def test_decode_is_deterministic(gpu_lib):
+    w = synth.WORKLOADS["llama3.2-3b-32k"]
+    gpu, _, _ = harness.make_pair(2, 2, 6, 3, 3000, window=128)
+    for l in range(2):
+        k, v = _inputs(w, l, 3, 2, 6, 2900)
+        gpu.append(l, k, v, torch.zeros(3, dtype=torch.int32, device="cuda"))
+    q = torch.stack([synth.queries(w, l, 3, 6, device="cuda") for l in range(2)])
+    sl = torch.tensor([2900, 1234, 77], dtype=torch.int32, device="cuda")
+    a = gpu.decode(-1, q, sl).clone()
+    b = gpu.decode(-1, q, sl).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_sinkhorn_kvarn(gpu_lib):
+    """Qwen3-4B KVarN-shaped (GQA 4) at small size: calibrate, append, decode."""
+    w = synth.WORKLOADS["qwen3-4b-kvarn-128k"]
+    Lyr, H, Hq, L, n_cal = 2, 2, 8, 1300, 1024
+    gpu, ora, _ = harness.make_pair(Lyr, H, Hq, 1, 1408, window=128, sinkhorn=True)
+    for l in range(Lyr):
+        k, v = _inputs(w, l, 1, H, Hq, L)
+        kc, vc = k[0, :, :n_cal].contiguous(), v[0, :, :n_cal].contiguous()
+        gpu.calibrate(l, kc, vc)
+        ora.calibrate(l, harness.to_np(kc), harness.to_np(vc))
+        gpu.append(l, k, v, torch.zeros(1, dtype=torch.int32, device="cuda"))
+        ora.append(l, harness.to_np(k), harness.to_np(v), np.array([0]))
+    torch.cuda.synchronize()
+    sk, sv = layout.read_sigma(gpu.buffer, gpu.cfg)
+    assert np.array_equal(sk.view(np.uint16), ora.sigma_k.view(np.uint16))
+    assert np.array_equal(sv.view(np.uint16), ora.sigma_v.view(np.uint16))
+    for l in range(Lyr):
+        for h in range(H):
+            harness.compare_codes(gpu, ora, l, 0, h, L)
+        q = synth.queries(w, l, 1, Hq, device="cuda")
+        got, want = _decode_both(gpu, ora, l, q, np.array([L]))
+        harness.assert_attention_close(got, want)
+
+
+def test_turboquant_keys(gpu_lib):
+    """Llama-3.1-8B TurboQuant-shaped (GQA 4, B=2) at small size: TQ3+QJL keys, Q4 values."""
+    w = synth.WORKLOADS["llama3.1-8b-tq-b8-32k"]
+    Lyr, H, Hq, B, L = 2, 2, 8, 2, 900
+    gpu, ora, _ = harness.make_pair(Lyr, H, Hq, B, 1024, window=128, k_format="tq3_qjl")
+    for l in range(Lyr):
+        k, v = _inputs(w, l, B, H, Hq, L)
+        gpu.append(l, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+        ora.append(l, harness.to_np(k), harness.to_np(v), np.zeros(B, np.int64))
+    torch.cuda.synchronize()
+    for l in range(Lyr):
+        for b in range(B):
+            for h in range(H):
+                harness.compare_codes(gpu, ora, l, b, h, L)
+        q = synth.queries(w, l, B, Hq, device="cuda")
+        got, want = _decode_both(gpu, ora, l, q, np.array([L, L - 321]))
+        harness.assert_attention_close(got, want)
+
+
+def test_paged_ragged_batch(gpu_lib):
+    """dense-27B-shaped (GQA 2) paged cache: shuffled block table, chunked ragged prefill."""
+    w = synth.WORKLOADS["dense27b-ragged-b32"]
+    rng = np.random.default_rng(3)
+    B, H, Hq, cap, chunk = 5, 2, 4, 2048, 256
+    lens = rng.integers(100, 2000, B).astype(np.int32)
+    maxpps = cap // 64
+    need = [int(-(-L // 64)) for L in lens]
+    n_pages = sum(need) + 3
+    perm = rng.permutation(n_pages)
+    bt = np.full((B, maxpps), -1, np.int32)
+    o = 0
+    for b in range(B):
+        bt[b, :need[b]] = perm[o:o + need[b]]
+        o += need[b]
+    gpu, ora, _ = harness.make_pair(1, H, Hq, B, cap, window=128, n_pages=n_pages, block_table=bt)
+    T = int(lens.max())
+    k, v = _inputs(w, 0, B, H, Hq, T)
+
+    def app(t0, n, live):
+        pos = np.array([t0 if b in live else -1 for b in range(B)], np.int32)
+        kk, vv = k[:, :, t0:t0 + n].contiguous(), v[:, :, t0:t0 + n].contiguous()
+        gpu.append(0, kk, vv, torch.as_tensor(pos, device="cuda"))
+        ora.append(0, harness.to_np(kk), harness.to_np(vv), pos)
+
+    for t0 in range(0, T, chunk):                      # full chunks, all sequences that have them
+        live = {b for b in range(B) if lens[b] >= t0 + chunk}
+        if live:
+            app(t0, chunk, live)
+    for b in range(B):                                  # each sequence's remainder on its own
+        r0 = (int(lens[b]) // chunk) * chunk
+        if lens[b] > r0:
+            app(r0, int(lens[b]) - r0, {b})
+    torch.cuda.synchronize()
+    assert gpu.status() == 0
+    for b in range(B):
+        for h in range(H):
+            harness.compare_codes(gpu, ora, 0, b, h, int(lens[b]), bt)
+            harness.compare_ring(gpu, ora, 0, b, h, int(lens[b]))
+    q = synth.queries(w, 0, B, Hq, device="cuda")
+    got, want = _decode_both(gpu, ora, 0, q, lens)
+    harness.assert_attention_close(got, want)
+
+
+def test_out_of_range_append_is_flagged_and_skipped(gpu_lib):
+    gpu, _, _ = harness.make_pair(1, 1, 2, 2, 256, window=128)
+    before = gpu.buffer.clone()
+    k = torch.ones(2, 1, 10, 128, dtype=torch.bfloat16, device="cuda")
+    gpu.append(0, k, k, torch.tensor([250, -1], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert gpu.status() == 2                        # KVQ_DEV_POS_RANGE
+    assert torch.equal(before, gpu.buffer)
+    assert gpu.status() == 0                        # read-and-clear

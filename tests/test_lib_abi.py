@@ -1,0 +1,83 @@
+"""The C ABI library: builds, loads without a GPU, exports every declared symbol, sizes caches."""
+
+import os
+import re
+
+import pytest
+
+from kv_cache_quantization_append_gb300 import lib, synth
+from oracle import attention
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not os.path.exists(lib.LIB_PATH):
+        from kv_cache_quantization_append_gb300 import build
+
+        build.build()
+    return lib.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kv_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(kvq):
+    names = _declared()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(kvq, n), n
+    assert set(names) == set(lib.EXPORTS)
+
+
+def test_strerror(kvq):
+    assert lib.kv_strerror(0) == "ok"
+    assert "unknown" in lib.kv_strerror(99)
+
+
+def _cfg(w, layers=None):
+    return lib.make_config(layers or w.get("alloc_layers", w["n_layers"]), w["n_kv_heads"], w["n_q_heads"],
+                           w["batch"], w.get("ctx", w.get("ctx_range", (0, 0))[1]), window=w["window"],
+                           k_format=lib.KVQ_TQ3_QJL if w["k_format"] == "tq3_qjl" else lib.KVQ_Q4G32,
+                           sinkhorn=w["sinkhorn"])
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_cache_bytes_closed_form(kvq, name):
+    """Library size = oracle payload (records + window ring) + page rounding + a small header."""
+    w = synth.WORKLOADS[name]
+    cfg = _cfg(w)
+    got = lib.kv_cache_bytes(cfg)
+    ocfg = attention.OracleConfig(n_layers=cfg.n_layers, n_kv_heads=cfg.n_kv_heads, n_q_heads=cfg.n_q_heads,
+                                  max_batch=cfg.max_batch, max_seq_len=cfg.max_seq_len, window=cfg.window,
+                                  k_format=w["k_format"], v_format=w["v_format"])
+    pages = -(-cfg.max_seq_len // 64) * 64
+    payload = (cfg.n_layers * cfg.max_batch * cfg.n_kv_heads * pages *
+               attention.payload_bytes_per_token_head(ocfg) + attention.window_bytes(ocfg))
+    header = got - payload
+    assert 0 < header <= 64 * 1024 + 128 * 128 * 4 + 4 * cfg.max_batch * pages // 64 + \
+        4 * cfg.n_layers * cfg.n_kv_heads * 256 + 4096
+
+
+def test_invalid_configs_have_no_size(kvq):
+    good = lib.make_config(2, 8, 24, 1, 1024)
+    assert lib.kv_cache_bytes(good) > 0
+    for field, bad in (("head_dim", 64), ("n_q_heads", 23), ("n_q_heads", 48), ("window", 100),
+                       ("page_tokens", 32), ("k_format", 7), ("max_batch", 0)):
+        c = lib.make_config(2, 8, 24, 1, 1024)
+        setattr(c, field, bad)
+        assert lib.kv_cache_bytes(c) == 0, field
+    c = lib.make_config(2, 8, 24, 1, 1024, k_format=lib.KVQ_TQ3_QJL, sinkhorn=True)
+    assert lib.kv_cache_bytes(c) == 0
+
+
+def test_llama_3b_32k_quantised_store_is_6_4x_smaller_than_fp32(kvq):
+    """[QC]: 6.4x KV compression; FP32 KV of Llama-3.2-3B at 32K is 7.17 GB."""
+    flat = lib.make_config(28, 8, 24, 1, 32768, window=0)
+    b = lib.kv_cache_bytes(flat)
+    fp32 = attention.fp32_kv_bytes(28, 8, 32768)
+    assert abs(fp32 / b - 6.4) < 0.01
