@@ -316,16 +316,17 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_unit_time(w, lens, budget_s: float, which_units, bf16=True):
-    """Time the oracle's decode of sample units (encode excluded); returns (seconds per unit, n)."""
+def cpu_baseline(w, layers, lens, budget_s=12.0, max_units=3):
+    """Time the oracle's decode on a few (layer, kv-head) units of this workload (their encode is
+    not timed), repeating until ``budget_s`` of decode time, and scale to one full step."""
     from oracle import attention
 
     H, Hq = w["n_kv_heads"], w["n_q_heads"]
     g = Hq // H
-    times = []
-    spent = 0.0
     proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
-    for (layer, b) in which_units:
+    picks = [(l, int(b)) for l, b in zip(range(max_units), np.linspace(0, len(lens) - 1, max_units).astype(int))]
+    units = []
+    for layer, b in picks:
         L = int(lens[b])
         ocfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=g, max_batch=1, max_seq_len=L,
                                       window=w["window"], k_format=w["k_format"], sinkhorn=w["sinkhorn"],
@@ -334,27 +335,21 @@ def oracle_unit_time(w, lens, budget_s: float, which_units, bf16=True):
         k, v = synth.kv_tokens(w, layer, 1, 1, 0, L, device="cpu")
         ora.append(0, k.float().numpy(), v.float().numpy(), np.array([0]))
         q = synth.queries(w, layer, 1, g, device="cpu").float().numpy()
+        units.append((ora, q, L))
+    spent, tokens, n = 0.0, 0, 0
+    while spent < budget_s or n < len(units):
+        ora, q, L = units[n % len(units)]
         t = time.perf_counter()
         ora.decode(0, q, np.array([L]))
-        dt = time.perf_counter() - t
-        times.append(dt)
-        spent += dt
-        if spent >= budget_s:
-            break
-    return statistics.mean(times), len(times)
-
-
-def cpu_baseline(w, layers, lens, budget_s=12.0):
-    units = [(l % max(1, w["n_layers"]), int(b)) for l in range(64) for b in range(len(lens))][:64]
-    per_unit, n = oracle_unit_time(w, lens, budget_s, units)
-    n_units = layers * len(lens) * w["n_kv_heads"]
-    # unit times scale with length; normalise by the sampled lengths
-    sampled_tokens = sum(int(lens[b]) for (_, b) in units[:n]) / n
-    step_s = per_unit / sampled_tokens * (float(lens.sum()) / len(lens)) * n_units
-    value = float(lens.sum()) / step_s
-    return {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"numpy oracle decode of {n} (layer, kv-head) units of {int(sampled_tokens)} tokens, "
-                      f"scaled to the {n_units} units of one step; encode not timed"}
+        spent += time.perf_counter() - t
+        tokens += L
+        n += 1
+    per_token_head = spent / tokens                      # seconds per (token, kv-head) attended
+    step_s = per_token_head * float(lens.sum()) * H * layers
+    return {"value": float(lens.sum()) / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"numpy oracle decode of {len(units)} (layer, kv-head) units ({n} timed calls, "
+                      f"{spent:.1f} s), scaled by tokens to the {layers * len(lens) * H} units of one step; "
+                      f"their encode not timed; one thread"}
 
 
 def run_reference(args):
@@ -362,7 +357,7 @@ def run_reference(args):
     if rank != 0:
         return None
     w, layers, lens = workload_cfg(args.workload)
-    budget = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))
     vals = []
     for i in range(args.warmup + args.steps):
         cb = cpu_baseline(w, layers, lens, budget_s=budget)

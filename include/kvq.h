@@ -25,7 +25,7 @@
  *     device can see (a block-table entry out of range, a position past capacity, a pipeline wait
  *     that gave up) set bits in the cache's device status word, read with kv_status.
  *   - head_dim is 128; n_q_heads is a multiple of n_kv_heads with a GQA group of 1..4 query heads
- *     per kv-head; page_tokens is 64; window is 0 or a multiple of 8 up to 1024.
+ *     per kv-head; page_tokens is 64; window is 0 or a multiple of 4 up to 1024.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -103,11 +103,15 @@ typedef struct kvq_cache {
  *   ring_k     float [n_layers][max_batch][n_kv_heads][window][128]   slot = position % window
  *   ring_v     same
  *   pages      [n_layers][n_pages][n_kv_heads][page_bytes]; one page = 64 tokens of one
- *              (layer, kv-head), regions in order:
- *     K main   Q4G32: 64 B per token, TQ3_QJL: 48 B codes per token then 16 B sign bits per token
- *     V main   64 B per token
- *     K meta   Q4G32: per token fp16 {scale[4], zero[4]};  TQ3_QJL: fp16 norm[64], fp16 gamma[64]
- *     V meta   fp16 scale[4][64] then fp16 zero[4][64]   (group-major)
+ *              (layer, kv-head) stored as two 32-token halves (tokens 0-31, 32-63), each half
+ *              contiguous with regions in order (t = token index within the half):
+ *     K main   Q4G32: 64 B per token at 64t;  TQ3_QJL: 48 B codes at 48t, then 16 B sign bits at
+ *              1536 + 16t
+ *     V main   64 B per token at 2048 + 64t
+ *     K meta   at 4096: Q4G32 per token fp16 {scale[4], zero[4]} (512 B); TQ3_QJL fp16 norm[32],
+ *              gamma[32] (128 B)
+ *     V meta   after K meta: fp16 scale[4][32] then fp16 zero[4][32] (group-major, 512 B)
+ *   Half sizes: Q4G32 K + Q4G32 V = 5120 B, TQ3_QJL K + Q4G32 V = 4736 B.
  *   Q4G32 record (64 B): the 32 halfwords are indexed (r, G), r = 0..7, G = 0..3, halfword at byte
  *     8r + 2G holds channels 32G + 4r .. 32G + 4r + 3 of the rotated (and balanced) vector as
  *     nibbles, lowest channel in the lowest nibble.

@@ -36,10 +36,11 @@ bool compute_layout(const kvq_config& c, Layout* L) {
   if (contiguous > INT32_MAX) return false;
   l.n_pages = c.n_pages > 0 ? c.n_pages : (int)contiguous;
   l.kmeta_bytes = (c.k_format == KVQ_TQ3_QJL) ? 4 : 16;
-  l.off_vmain = 64 * PAGE;
-  l.off_kmeta = 128 * PAGE;
-  l.off_vmeta = l.off_kmeta + l.kmeta_bytes * PAGE;
-  l.page_bytes = l.off_vmeta + 16 * PAGE;
+  l.off_vmain = 64 * HALF;
+  l.off_kmeta = 128 * HALF;
+  l.off_vmeta = l.off_kmeta + l.kmeta_bytes * HALF;
+  l.half_bytes = l.off_vmeta + 16 * HALF;
+  l.page_bytes = 2 * l.half_bytes;
   size_t o = 0;
   l.off_status = o; o = align256(o + 16);
   l.off_signs = o;  o = align256(o + D * sizeof(float));

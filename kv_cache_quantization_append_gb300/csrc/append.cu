@@ -89,13 +89,15 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
     *reinterpret_cast<float4*>(dst) = xin;
   }
 
-  const int lp = p / PAGE, tin = p % PAGE;
+  const int lp = p / PAGE, tin = p % HALF;
   const int phys = a.block_table[(size_t)b * a.L.max_pages_per_seq + lp];
   if (phys < 0 || phys >= a.L.n_pages) {
     if (lane == 0) atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
     return;
   }
-  uint8_t* pg = a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + h) * (size_t)a.L.page_bytes;
+  // the half-page holding this token: K main | V main | K meta | V meta for 32 tokens
+  uint8_t* pg = a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + h) * (size_t)a.L.page_bytes +
+                (size_t)((p % PAGE) / HALF) * a.L.half_bytes;
 
   // rotation y = c * H (s . x): sign flip (exact), butterfly, one multiply by c
   const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
@@ -151,12 +153,12 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
     __syncwarp();
     uint8_t* rec = pg + (size_t)tin * 48;
     if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = sbits[wl][lane];
-    uint32_t* sgn = reinterpret_cast<uint32_t*>(pg + 48 * PAGE + (size_t)tin * 16);
+    uint32_t* sgn = reinterpret_cast<uint32_t*>(pg + 48 * HALF + (size_t)tin * 16);
     if ((lane & 7) == 0) sgn[lane >> 3] = word;
     if (lane == 0) {
       __half* meta = reinterpret_cast<__half*>(pg + a.L.off_kmeta);
       meta[tin] = __float2half_rn(n);
-      meta[PAGE + tin] = __float2half_rn(gamma);
+      meta[HALF + tin] = __float2half_rn(gamma);
     }
     return;
   }
@@ -180,11 +182,11 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
       *reinterpret_cast<uint4*>(pg + a.L.off_kmeta + (size_t)tin * 16) =
           make_uint4(s0 | (s1 << 16), s2 | (s3 << 16), z0 | (z1 << 16), z2 | (z3 << 16));
   } else if ((lane & 7) == 0) {
-    // V meta: group-major scale[4][64] then zero[4][64]
+    // V meta: group-major scale[4][32] then zero[4][32]
     __half* meta = reinterpret_cast<__half*>(pg + a.L.off_vmeta);
     const int G = lane >> 3;
-    meta[G * PAGE + tin] = s16;
-    meta[4 * PAGE + G * PAGE + tin] = z16;
+    meta[G * HALF + tin] = s16;
+    meta[4 * HALF + G * HALF + tin] = z16;
   }
 }
 

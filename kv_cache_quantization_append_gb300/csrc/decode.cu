@@ -6,12 +6,14 @@
 // where tokens t < L - window are read from the packed pages and scored in rotated space
 // (q~ = c H (s . q) [. sigma_k]), and the last `window` tokens come raw from the FP32 ring.
 //
-// Design for GB300 (one CTA per SM, 8 consumer warps + 1 producer warp):
-//  * The work of a call is a list of "steps" -- one 64-token page or one 8-slot window chunk of one
-//    (layer, sequence, kv-head) unit -- cut into equal contiguous ranges, one per CTA, so every SM
-//    streams the same number of bytes whatever the sequence lengths (ragged batches included).
-//  * The producer warp streams each step into a 16-stage shared-memory ring with
-//    cp.async.bulk (the 1D TMA path) completing on mbarriers; stage k goes to consumer warp k % 8.
+// Design for GB300 (one CTA per SM: 11 consumer warps + 1 producer warp):
+//  * The work of a call is a list of "steps" -- one 32-token half-page or one 4-slot window chunk
+//    of one (layer, sequence, kv-head) unit, window chunks first -- cut into equal contiguous
+//    ranges, one per CTA, so every SM streams the same bytes whatever the sequence lengths.
+//  * Consumer warp w takes the CTA's steps w, w + 11, ...; it owns two shared-memory stages
+//    (slots w and w + 11 of 22).  Lane w of the producer warp streams exactly that warp's steps
+//    with cp.async.bulk (the 1D TMA path) completing on mbarriers, so no consumer ever waits
+//    behind another one's progress.
 //  * Consumer warps dequantise nibbles to fp16 in registers (exponent-bias trick: OR a nibble into
 //    the mantissa of 1024.0, subtract exactly) and run the logits and P.V as tensor-core
 //    mma.sync m16n8k16 (fp32 accumulate): GQA query heads are the N axis (hi and lo halves of q
@@ -28,10 +30,10 @@ namespace kvq {
 
 namespace {
 
-constexpr int NCW = 8;                       // consumer warps
-constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int NSTAGE = 16;
-constexpr int STAGE_BYTES = 10240;           // max page (Q4/Q4) and window chunk (8 KB)
+constexpr int NCW = 11;                      // consumer warps
+constexpr int NTHREADS = (NCW + 1) * 32;     // 384: the 168-register budget of 12 warps
+constexpr int NSTAGE = 2 * NCW;              // two stages per consumer warp
+constexpr int STAGE_BYTES = 5120;            // max half-page (Q4/Q4) and window chunk (4 KB)
 constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
@@ -44,7 +46,10 @@ constexpr int SM_Q = SM_DESC + NSTAGE * 16;                       // [NCW][4][12
 constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;               // [NCW][4][128] float (TQ)
 constexpr int SM_QSUM = SM_SQ + NCW * MAX_GQA * D * 4;            // [NCW][4][4] float
 constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                    // [64][32] u32 (TQ)
-constexpr int SM_SEQ = SM_LUT + 64 * 32 * 4;                      // 3 int arrays of batch+1
+constexpr int SM_LG = SM_LUT + 64 * 32 * 4;                       // [NCW][4][32] float logits
+constexpr int SM_P = SM_LG + NCW * MAX_GQA * HALF * 4;            // [NCW][4][32] fp16 probabilities
+constexpr int SM_WML = SM_P + NCW * MAX_GQA * HALF * 2;           // [NCW][8] float window m, l
+constexpr int SM_SEQ = SM_WML + NCW * 8 * 4;                      // 3 int arrays of batch+1
 constexpr int SM_FIXED = SM_SEQ;
 
 // ------------------------------------------------------------------ PTX helpers
@@ -76,7 +81,7 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 // Bounded wait: false (and the status bit set) if the phase did not complete within ~1 s.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
   while (true) {
@@ -102,6 +107,12 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// 2^x in one MUFU op (max relative error 2^-22); 2^-inf = +0
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
@@ -154,6 +165,23 @@ __device__ __forceinline__ Pos locate(long long x, long long S_layer, int B, int
   return p;
 }
 
+// move a position forward by `by` steps (only called while the target step exists)
+__device__ __forceinline__ void advance(Pos& p, int by, int B, int H, const Seq& sq) {
+  p.local += by;
+  while (p.local >= sq.S[p.b]) {
+    p.local -= sq.S[p.b];
+    if (++p.h == H) {
+      p.h = 0;
+      do {
+        if (++p.b == B) {
+          p.b = 0;
+          p.ll++;
+        }
+      } while (sq.S[p.b] == 0);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ per-warp state
 struct QuantState {
   uint32_t qb[8][2];   // B fragments of q~ (K logits), hi/lo interleaved columns
@@ -164,10 +192,13 @@ struct QuantState {
   float m, l;          // running max / partial sum for head (lane & 3)
 };
 
+// Window-part state of a warp, kept in its shared-memory slices so that it is not live in
+// registers while the warp streams quantised pages: q [4][128] (the q staging slice, reused by the
+// quantised part only after the window partial is written), acc [4][128] (the S q~ slice), m, l.
 struct WinState {
-  float q[MAX_GQA][4];
-  float acc[MAX_GQA][4];
-  float m[MAX_GQA], l[MAX_GQA];
+  float* q;
+  float* acc;
+  float* ml;
 };
 
 template <int KF>
@@ -198,14 +229,12 @@ struct Kernel {
       for (int hh = 0; hh < MAX_GQA; ++hh) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (hh < g) x = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
-        ws.q[hh][0] = x.x * LOGIT_SCALE;
-        ws.q[hh][1] = x.y * LOGIT_SCALE;
-        ws.q[hh][2] = x.z * LOGIT_SCALE;
-        ws.q[hh][3] = x.w * LOGIT_SCALE;
-        ws.acc[hh][0] = ws.acc[hh][1] = ws.acc[hh][2] = ws.acc[hh][3] = 0.f;
-        ws.m[hh] = -INFINITY;
-        ws.l[hh] = 0.f;
+        *reinterpret_cast<float4*>(ws.q + hh * D + 4 * lane) =
+            make_float4(x.x * LOGIT_SCALE, x.y * LOGIT_SCALE, x.z * LOGIT_SCALE, x.w * LOGIT_SCALE);
+        *reinterpret_cast<float4*>(ws.acc + hh * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+      if (lane < 8) ws.ml[lane] = lane < 4 ? -INFINITY : 0.f;
+      __syncwarp();
       return;
     }
     float* qs = reinterpret_cast<float*>(smem + SM_Q) + warp * MAX_GQA * D;
@@ -309,17 +338,20 @@ struct Kernel {
   __device__ void window_step(const uint8_t* stage, int ntok, WinState& ws) {
     const float* Ks = reinterpret_cast<const float*>(stage);
     const float* Vs = Ks + WCHUNK * D;
-    float part[32];
+    float4 q4[MAX_GQA];
+#pragma unroll
+    for (int hh = 0; hh < MAX_GQA; ++hh) q4[hh] = *reinterpret_cast<const float4*>(ws.q + hh * D + 4 * lane);
+    float part[WCHUNK * MAX_GQA];
 #pragma unroll
     for (int t = 0; t < WCHUNK; ++t) {
       const float4 k4 = *reinterpret_cast<const float4*>(Ks + t * D + 4 * lane);
 #pragma unroll
       for (int hh = 0; hh < MAX_GQA; ++hh)
-        part[4 * t + hh] = ws.q[hh][0] * k4.x + ws.q[hh][1] * k4.y + ws.q[hh][2] * k4.z + ws.q[hh][3] * k4.w;
+        part[4 * t + hh] = q4[hh].x * k4.x + q4[hh].y * k4.y + q4[hh].z * k4.z + q4[hh].w * k4.w;
     }
-    // transpose-reduce 32 partial dots over 32 lanes: lane l ends with value index l = 4t + hh
+    // transpose-reduce 16 partial dots over 32 lanes: lanes 2v, 2v+1 end with value v = 4t + hh
 #pragma unroll
-    for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    for (int o = 16, n = 16; o >= 2; o >>= 1, n >>= 1) {
       const bool up = lane & o;
 #pragma unroll
       for (int k = 0; k < n / 2; ++k) {
@@ -328,197 +360,243 @@ struct Kernel {
         part[k] = keep + __shfl_xor_sync(FULL, send, o);
       }
     }
-    const int t = lane >> 2, hh = lane & 3;
+    part[0] += __shfl_xor_sync(FULL, part[0], 1);
+    const int t = lane >> 3, hh = (lane >> 1) & 3;
     const float lg = (t < ntok && hh < g) ? part[0] : -INFINITY;
     float mc = lg;
-    mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 4));
     mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 8));
     mc = fmaxf(mc, __shfl_xor_sync(FULL, mc, 16));
-    float alpha[MAX_GQA];
+    float alpha[MAX_GQA], mk[MAX_GQA];
     float mown = -INFINITY;
 #pragma unroll
     for (int k = 0; k < MAX_GQA; ++k) {
-      const float mk = __shfl_sync(FULL, mc, k);
-      const float mn = fmaxf(ws.m[k], mk);
-      alpha[k] = (mn == -INFINITY) ? 1.f : exp2f(ws.m[k] - mn);
-      ws.m[k] = mn;
+      const float mold = ws.ml[k];
+      const float mn = fmaxf(mold, __shfl_sync(FULL, mc, 2 * k));
+      alpha[k] = (mn == -INFINITY) ? 1.f : exp2f(mold - mn);
+      mk[k] = mn;
       if (hh == k) mown = mn;
     }
     const float p = (lg == -INFINITY) ? 0.f : exp2f(lg - mown);
     float ps = p;
-    ps += __shfl_xor_sync(FULL, ps, 4);
     ps += __shfl_xor_sync(FULL, ps, 8);
     ps += __shfl_xor_sync(FULL, ps, 16);
+    float lk[MAX_GQA];
+#pragma unroll
+    for (int k = 0; k < MAX_GQA; ++k) lk[k] = ws.ml[4 + k] * alpha[k] + __shfl_sync(FULL, ps, 2 * k);
 #pragma unroll
     for (int k = 0; k < MAX_GQA; ++k) {
-      ws.l[k] = ws.l[k] * alpha[k] + __shfl_sync(FULL, ps, k);
-      ws.acc[k][0] *= alpha[k];
-      ws.acc[k][1] *= alpha[k];
-      ws.acc[k][2] *= alpha[k];
-      ws.acc[k][3] *= alpha[k];
-    }
+      float4 acc = *reinterpret_cast<const float4*>(ws.acc + k * D + 4 * lane);
+      acc.x *= alpha[k];
+      acc.y *= alpha[k];
+      acc.z *= alpha[k];
+      acc.w *= alpha[k];
 #pragma unroll
-    for (int tt = 0; tt < WCHUNK; ++tt) {
-      if (tt < ntok) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Vs + tt * D + 4 * lane);
-#pragma unroll
-        for (int k = 0; k < MAX_GQA; ++k) {
-          const float pt = __shfl_sync(FULL, p, 4 * tt + k);
-          ws.acc[k][0] += pt * v4.x;
-          ws.acc[k][1] += pt * v4.y;
-          ws.acc[k][2] += pt * v4.z;
-          ws.acc[k][3] += pt * v4.w;
+      for (int tt = 0; tt < WCHUNK; ++tt) {
+        const float pt = __shfl_sync(FULL, p, 8 * tt + 2 * k);
+        if (tt < ntok) {
+          const float4 v4 = *reinterpret_cast<const float4*>(Vs + tt * D + 4 * lane);
+          acc.x += pt * v4.x;
+          acc.y += pt * v4.y;
+          acc.z += pt * v4.z;
+          acc.w += pt * v4.w;
         }
       }
+      *reinterpret_cast<float4*>(ws.acc + k * D + 4 * lane) = acc;
+    }
+    __syncwarp();
+    if (lane < MAX_GQA) {
+      ws.ml[lane] = mk[0];
+#pragma unroll
+      for (int k = 1; k < MAX_GQA; ++k)
+        if (lane == k) ws.ml[lane] = mk[k];
+    } else if (lane < 2 * MAX_GQA) {
+      ws.ml[lane] = lk[0];
+#pragma unroll
+      for (int k = 1; k < MAX_GQA; ++k)
+        if (lane - MAX_GQA == k) ws.ml[lane] = lk[k];
+    }
+    __syncwarp();
+  }
+
+  // ---------------------------------------------------------------- quantised half-page
+  // regions of a 32-token half-page (bytes): K main at 0, V main at 64*HALF, K meta at 128*HALF,
+  // V meta after K meta
+  static constexpr int OFF_VMAIN = 64 * HALF;
+  static constexpr int OFF_KMETA = 128 * HALF;
+  static constexpr int OFF_VMETA = OFF_KMETA + (KF == KVQ_TQ3_QJL ? 4 : 16) * HALF;
+
+  // logits of tokens ta = 16mt + r and tb = ta + 8 for head i (this thread's column pair)
+  __device__ __forceinline__ void tile_logits(const uint8_t* stage, int mt, const QuantState& st, float& la,
+                                              float& lb) {
+    const int r = lane >> 2, i = lane & 3;
+    const int ta = 16 * mt + r, tb = ta + 8;
+    const uint8_t* kmain = stage;
+    const uint8_t* kmeta = stage + OFF_KMETA;
+    if (KF == KVQ_TQ3_QJL) {
+      float cacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + SM_LUT) + lane;
+      const uint32_t* ca = reinterpret_cast<const uint32_t*>(kmain + ta * 48 + 12 * i);
+      const uint32_t* cbp = reinterpret_cast<const uint32_t*>(kmain + tb * 48 + 12 * i);
+      const uint32_t wa[4] = {ca[0], ca[1], ca[2], 0u};
+      const uint32_t wb[4] = {cbp[0], cbp[1], cbp[2], 0u};
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t pa[2], pb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int bit = 6 * (2 * kk + e), wi = bit >> 5, sh = bit & 31;
+          pa[e] = lut[(__funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u) * 32];
+          pb[e] = lut[(__funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u) * 32];
+        }
+        mma16816(cacc, pa[0], pb[0], pa[1], pb[1], st.qb[kk][0], st.qb[kk][1]);
+      }
+      const uint32_t sa = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * HALF + ta * 16 + 4 * i);
+      const uint32_t sbw = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * HALF + tb * 16 + 4 * i);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        // half2 index k' = 2kk + eps holds bits (k', k'+16) as +-1.0
+        const int k0 = 2 * kk, k1 = 2 * kk + 1;
+        const uint32_t a0 = ((sa << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
+        const uint32_t a1 = ((sbw << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
+        const uint32_t a2 = ((sa << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
+        const uint32_t a3 = ((sbw << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
+        mma16816(sacc, a0, a1, a2, a3, st.sb[kk][0], st.sb[kk][1]);
+      }
+      const __half* nrm = reinterpret_cast<const __half*>(kmeta);
+      const float na = __half2float(nrm[ta]), nb = __half2float(nrm[tb]);
+      const float ga = __half2float(nrm[HALF + ta]), gb = __half2float(nrm[HALF + tb]);
+      la = na * ((cacc[0] + cacc[1]) + QJL_CONST * ga * (sacc[0] + sacc[1]));
+      lb = nb * ((cacc[2] + cacc[3]) + QJL_CONST * gb * (sacc[2] + sacc[3]));
+    } else {
+      const uint4 ka = *reinterpret_cast<const uint4*>(kmain + ta * 64 + 16 * i);
+      const uint4 kb = *reinterpret_cast<const uint4*>(kmain + tb * 64 + 16 * i);
+      float acc[4][4];
+#pragma unroll
+      for (int G = 0; G < 4; ++G) {
+        acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+        // group G's 8 channels of this thread: halfwords (2i, G) and (2i+1, G)
+        const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
+        const uint32_t wa = __byte_perm((G < 2) ? ka.x : ka.y, (G < 2) ? ka.z : ka.w, sel);
+        const uint32_t wb = __byte_perm((G < 2) ? kb.x : kb.y, (G < 2) ? kb.z : kb.w, sel);
+        uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
+        nib8(wa, a04, a15, a26, a37);
+        nib8(wb, b04, b15, b26, b37);
+        mma16816(acc[G], a04, b04, a15, b15, st.qb[2 * G][0], st.qb[2 * G][1]);
+        mma16816(acc[G], a26, b26, a37, b37, st.qb[2 * G + 1][0], st.qb[2 * G + 1][1]);
+      }
+      const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
+      const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
+      const float2 sa01 = __half22float2(u2h(ma.x)), sa23 = __half22float2(u2h(ma.y));
+      const float2 za01 = __half22float2(u2h(ma.z)), za23 = __half22float2(u2h(ma.w));
+      const float2 sb01 = __half22float2(u2h(mb.x)), sb23 = __half22float2(u2h(mb.y));
+      const float2 zb01 = __half22float2(u2h(mb.z)), zb23 = __half22float2(u2h(mb.w));
+      la = za01.x * st.qsum[0] + za01.y * st.qsum[1] + za23.x * st.qsum[2] + za23.y * st.qsum[3];
+      lb = zb01.x * st.qsum[0] + zb01.y * st.qsum[1] + zb23.x * st.qsum[2] + zb23.y * st.qsum[3];
+      la += sa01.x * (acc[0][0] + acc[0][1]) + sa01.y * (acc[1][0] + acc[1][1]) +
+            sa23.x * (acc[2][0] + acc[2][1]) + sa23.y * (acc[3][0] + acc[3][1]);
+      lb += sb01.x * (acc[0][2] + acc[0][3]) + sb01.y * (acc[1][2] + acc[1][3]) +
+            sb23.x * (acc[2][2] + acc[2][3]) + sb23.y * (acc[3][2] + acc[3][3]);
     }
   }
 
-  // ---------------------------------------------------------------- quantised page
-  __device__ void quant_step(const uint8_t* stage, int ntok, QuantState& st) {
-    const int r = lane >> 2, i = lane & 3;
-    const uint8_t* kmain = stage;
-    const uint8_t* vmain = stage + a.L.off_vmain;
-    const uint8_t* kmeta = stage + a.L.off_kmeta;
-    const __half* vscale = reinterpret_cast<const __half*>(stage + a.L.off_vmeta);
-    const __half* vzero = vscale + 4 * PAGE;
-    const bool headok = i < g;
+  // Tail half-page (ntok < 32): zero the scales and zeros (and TQ norms) of the missing tokens in
+  // shared memory, so that their -inf logits and zero weights never meet stale values; the fence
+  // orders these generic-proxy writes before the next bulk copy into the stage.
+  __device__ void sanitize_tail(uint8_t* stage, int ntok) {
+    __half* vmeta = reinterpret_cast<__half*>(stage + OFF_VMETA);
+    for (int idx = lane; idx < 8 * HALF; idx += 32)
+      if ((idx % HALF) >= ntok) vmeta[idx] = __float2half_rn(0.f);
+    if (KF == KVQ_TQ3_QJL) {
+      __half* nrm = reinterpret_cast<__half*>(stage + OFF_KMETA);
+      for (int idx = lane; idx < 2 * HALF; idx += 32)
+        if ((idx % HALF) >= ntok) nrm[idx] = __float2half_rn(0.f);
+    } else {
+      for (int t = ntok + lane; t < HALF; t += 32)
+        *reinterpret_cast<uint4*>(stage + OFF_KMETA + t * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+  }
 
-    // ---- logits for the page: thread holds tokens 16mt + r and 16mt + r + 8, head i
-    float lg[4][2];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const int ta = 16 * mt + r, tb = ta + 8;
-      if (KF == KVQ_TQ3_QJL) {
-        float cacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + SM_LUT) + lane;
-        const uint32_t* ca = reinterpret_cast<const uint32_t*>(kmain + ta * 48 + 12 * i);
-        const uint32_t* cbp = reinterpret_cast<const uint32_t*>(kmain + tb * 48 + 12 * i);
-        const uint32_t wa[4] = {ca[0], ca[1], ca[2], 0u};
-        const uint32_t wb[4] = {cbp[0], cbp[1], cbp[2], 0u};
-        uint32_t pa[16], pb[16];
-#pragma unroll
-        for (int pp = 0; pp < 16; ++pp) {
-          const int bit = 6 * pp, wi = bit >> 5, sh = bit & 31;
-          const uint32_t ia = __funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u;
-          const uint32_t ib = __funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u;
-          pa[pp] = lut[ia * 32];
-          pb[pp] = lut[ib * 32];
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma16816(cacc, pa[2 * kk], pb[2 * kk], pa[2 * kk + 1], pb[2 * kk + 1], st.qb[kk][0], st.qb[kk][1]);
-        const uint32_t sa = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * PAGE + ta * 16 + 4 * i);
-        const uint32_t sbw = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * PAGE + tb * 16 + 4 * i);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          // half2 index k' = 2kk + eps holds bits (k', k'+16) as +-1.0
-          const int k0 = 2 * kk, k1 = 2 * kk + 1;
-          const uint32_t a0 = ((sa << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
-          const uint32_t a1 = ((sbw << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
-          const uint32_t a2 = ((sa << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
-          const uint32_t a3 = ((sbw << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
-          mma16816(sacc, a0, a1, a2, a3, st.sb[kk][0], st.sb[kk][1]);
-        }
-        const __half* nrm = reinterpret_cast<const __half*>(kmeta);
-        const float na = __half2float(nrm[ta]), nb = __half2float(nrm[tb]);
-        const float ga = __half2float(nrm[PAGE + ta]), gb = __half2float(nrm[PAGE + tb]);
-        const float la = na * ((cacc[0] + cacc[1]) + QJL_CONST * ga * (sacc[0] + sacc[1]));
-        const float lb = nb * ((cacc[2] + cacc[3]) + QJL_CONST * gb * (sacc[2] + sacc[3]));
-        lg[mt][0] = (headok && ta < ntok) ? la : -INFINITY;
-        lg[mt][1] = (headok && tb < ntok) ? lb : -INFINITY;
-      } else {
-        const uint4 ka = *reinterpret_cast<const uint4*>(kmain + ta * 64 + 16 * i);
-        const uint4 kb = *reinterpret_cast<const uint4*>(kmain + tb * 64 + 16 * i);
-        float acc[4][4];
-#pragma unroll
-        for (int G = 0; G < 4; ++G) {
-          acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
-          // group G's 8 channels of this thread: halfwords (2i, G) and (2i+1, G)
-          const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
-          const uint32_t wa = __byte_perm((G < 2) ? ka.x : ka.y, (G < 2) ? ka.z : ka.w, sel);
-          const uint32_t wb = __byte_perm((G < 2) ? kb.x : kb.y, (G < 2) ? kb.z : kb.w, sel);
-          uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-          nib8(wa, a04, a15, a26, a37);
-          nib8(wb, b04, b15, b26, b37);
-          mma16816(acc[G], a04, b04, a15, b15, st.qb[2 * G][0], st.qb[2 * G][1]);
-          mma16816(acc[G], a26, b26, a37, b37, st.qb[2 * G + 1][0], st.qb[2 * G + 1][1]);
-        }
-        const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
-        const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
-        const float2 sa01 = __half22float2(u2h(ma.x)), sa23 = __half22float2(u2h(ma.y));
-        const float2 za01 = __half22float2(u2h(ma.z)), za23 = __half22float2(u2h(ma.w));
-        const float2 sb01 = __half22float2(u2h(mb.x)), sb23 = __half22float2(u2h(mb.y));
-        const float2 zb01 = __half22float2(u2h(mb.z)), zb23 = __half22float2(u2h(mb.w));
-        float la = za01.x * st.qsum[0] + za01.y * st.qsum[1] + za23.x * st.qsum[2] + za23.y * st.qsum[3];
-        float lb = zb01.x * st.qsum[0] + zb01.y * st.qsum[1] + zb23.x * st.qsum[2] + zb23.y * st.qsum[3];
-        la += sa01.x * (acc[0][0] + acc[0][1]) + sa01.y * (acc[1][0] + acc[1][1]) +
-              sa23.x * (acc[2][0] + acc[2][1]) + sa23.y * (acc[3][0] + acc[3][1]);
-        lb += sb01.x * (acc[0][2] + acc[0][3]) + sb01.y * (acc[1][2] + acc[1][3]) +
-              sb23.x * (acc[2][2] + acc[2][3]) + sb23.y * (acc[3][2] + acc[3][3]);
-        lg[mt][0] = (headok && ta < ntok) ? la : -INFINITY;
-        lg[mt][1] = (headok && tb < ntok) ? lb : -INFINITY;
+  __device__ void quant_step(uint8_t* stage, int ntok, QuantState& st) {
+    const int r = lane >> 2, i = lane & 3;
+    const uint8_t* vmain = stage + OFF_VMAIN;
+    const __half* vscale = reinterpret_cast<const __half*>(stage + OFF_VMETA);
+    const __half* vzero = vscale + 4 * HALF;
+    float* lgs = reinterpret_cast<float*>(smem + SM_LG) + warp * MAX_GQA * HALF + i * HALF;
+    __half* pw = reinterpret_cast<__half*>(smem + SM_P) + warp * MAX_GQA * HALF;
+    const float lmask = (i < g) ? 0.f : -INFINITY;  // column pair of a missing head: never attended
+    const bool tail = ntok < HALF;
+    if (tail) sanitize_tail(stage, ntok);
+
+    // ---- logits of the 32 tokens (two 16-token m-tiles, rolled to keep the loop body small)
+    float mx = -INFINITY;
+#pragma unroll 1
+    for (int mt = 0; mt < 2; ++mt) {
+      float la, lb;
+      tile_logits(stage, mt, st, la, lb);
+      const int ta = 16 * mt + r;
+      float ma = lmask, mb = lmask;
+      if (tail) {
+        ma = ta < ntok ? lmask : -INFINITY;
+        mb = ta + 8 < ntok ? lmask : -INFINITY;
       }
+      la += ma;
+      lb += mb;
+      lgs[ta] = la;
+      lgs[ta + 8] = lb;
+      mx = fmaxf(mx, fmaxf(la, lb));
     }
 
-    // ---- online softmax update for head i (rows r = 0..7 share it)
-    float mx = -INFINITY;
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) mx = fmaxf(mx, fmaxf(lg[mt][0], lg[mt][1]));
+    // ---- online softmax update for head i (rows r = 0..7 share it); 2^(-inf - m) = 0 handles
+    // masked tokens, a finite reference max handles a head with nothing valid yet
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
     const float mnew = fmaxf(st.m, mx);
-    const float alpha = (mnew == -INFINITY) ? 1.f : exp2f(st.m - mnew);
+    const float mref = (mnew == -INFINITY) ? 0.f : mnew;
+    const float alpha = (mnew == -INFINITY) ? 1.f : ex2(st.m - mnew);
     st.m = mnew;
-    float pr[4][2];
     float psum = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        pr[mt][k] = (lg[mt][k] == -INFINITY) ? 0.f : exp2f(lg[mt][k] - mnew);
-        psum += pr[mt][k];
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int t = 8 * k + r;  // tokens r, r+8, r+16, r+24
+      const float pv = ex2(lgs[t] - mref);
+      psum += pv;
+      pw[i * HALF + t] = __float2half_rn(pv);
     }
     st.l = st.l * alpha + psum;
-    // accumulator columns 2i, 2i+1 are heads 2i, 2i+1: fetch their alpha from lanes (r, 2i), (r, 2i+1)
-    const float al0 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i) & 3));
-    const float al1 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i + 1) & 3));
+    if (__any_sync(FULL, alpha != 1.f)) {
+      // accumulator columns 2i, 2i+1 are heads 2i, 2i+1: their alpha lives in lanes (r, 2i), (r, 2i+1)
+      const float al0 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i) & 3));
+      const float al1 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i + 1) & 3));
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      st.acc[j][0] *= al0;
-      st.acc[j][1] *= al1;
-      st.acc[j][2] *= al0;
-      st.acc[j][3] *= al1;
+      for (int j = 0; j < 8; ++j) {
+        st.acc[j][0] *= al0;
+        st.acc[j][1] *= al1;
+        st.acc[j][2] *= al0;
+        st.acc[j][3] *= al1;
+      }
+      st.zacc[0] *= al0;
+      st.zacc[1] *= al1;
+      st.zacc[2] *= al0;
+      st.zacc[3] *= al1;
     }
-    st.zacc[0] *= al0;
-    st.zacc[1] *= al1;
-    st.zacc[2] *= al0;
-    st.zacc[3] *= al1;
+    __syncwarp();
 
-    // ---- P.V: k-step = 16 tokens; this thread's B column is head r (r < g), tokens 2i, 2i+1, +8, +9
+    // ---- P.V: k-step = 16 tokens; this thread's B column is head r (r < g), tokens t0, t0+1, +8, +9
     const bool colok = r < g;
-    const int src0 = 4 * (2 * i) + (r & 3), src1 = 4 * (2 * i + 1) + (r & 3);
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      const float pa0 = __shfl_sync(FULL, pr[mt][0], src0);  // token 16mt + 2i
-      const float pb0 = __shfl_sync(FULL, pr[mt][1], src0);  // token 16mt + 2i + 8
-      const float pa1 = __shfl_sync(FULL, pr[mt][0], src1);  // token 16mt + 2i + 1
-      const float pb1 = __shfl_sync(FULL, pr[mt][1], src1);  // token 16mt + 2i + 9
+    const __half* pcol = pw + (r & 3) * HALF;
+#pragma unroll 1
+    for (int mt = 0; mt < 2; ++mt) {
       const int t0 = 16 * mt + 2 * i;
-      const bool full = ntok >= 16 * (mt + 1);
-      const bool okA0 = t0 < ntok, okA1 = t0 + 1 < ntok, okB0 = t0 + 8 < ntok, okB1 = t0 + 9 < ntok;
-      const uint32_t pA = colok ? h2u(__floats2half2_rn(pa0, pa1)) : 0u;
-      const uint32_t pB = colok ? h2u(__floats2half2_rn(pb0, pb1)) : 0u;
-      // z-term: rows = groups r (< 4), k = tokens: A = z, B = unscaled p
+      const uint32_t pA = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
+      const uint32_t pB = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
+      // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = unscaled p
       uint32_t zA = 0u, zB = 0u;
       if (r < 4) {
-        zA = *reinterpret_cast<const uint32_t*>(vzero + r * PAGE + t0);
-        zB = *reinterpret_cast<const uint32_t*>(vzero + r * PAGE + t0 + 8);
-        if (!full) {
-          zA &= (okA0 ? 0x0000FFFFu : 0u) | (okA1 ? 0xFFFF0000u : 0u);
-          zB &= (okB0 ? 0x0000FFFFu : 0u) | (okB1 ? 0xFFFF0000u : 0u);
-        }
+        zA = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0);
+        zB = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0 + 8);
       }
       mma16816(st.zacc, zA, 0u, zB, 0u, pA, pB);
       // V codes of the four tokens for channel rows r: 8 bytes = halfwords (r, G = 0..3)
@@ -528,15 +606,11 @@ struct Kernel {
       const uint2 vd = *reinterpret_cast<const uint2*>(vmain + (t0 + 9) * 64 + 8 * r);
 #pragma unroll
       for (int G = 0; G < 4; ++G) {
-        // B operand for group G: p * scale (fp16), zero outside the valid tokens
-        uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * PAGE + t0);
-        uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * PAGE + t0 + 8);
-        uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
-        uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
-        if (!full) {
-          bA &= (okA0 ? 0x0000FFFFu : 0u) | (okA1 ? 0xFFFF0000u : 0u);
-          bB &= (okB0 ? 0x0000FFFFu : 0u) | (okB1 ? 0xFFFF0000u : 0u);
-        }
+        // B operand for group G: p * scale (fp16)
+        const uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0);
+        const uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0 + 8);
+        const uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
+        const uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
         const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
         const uint32_t wab = __byte_perm((G < 2) ? va.x : va.y, (G < 2) ? vb.x : vb.y, sel);
         const uint32_t wcd = __byte_perm((G < 2) ? vc.x : vc.y, (G < 2) ? vd.x : vd.y, sel);
@@ -547,6 +621,7 @@ struct Kernel {
         mma16816(st.acc[2 * G + 1], ab2, ab3, cd2, cd3, bA, bB);
       }
     }
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- records and merge
@@ -557,9 +632,9 @@ struct Kernel {
   __device__ void write_window(float* rec, const WinState& ws) {
 #pragma unroll
     for (int hh = 0; hh < MAX_GQA; ++hh)
-      if (hh < g && ws.l[hh] > 0.f)
+      if (hh < g && ws.ml[4 + hh] > 0.f)
         *reinterpret_cast<float4*>(rec + 16 + MAX_GQA * D + hh * D + 4 * lane) =
-            make_float4(ws.acc[hh][0], ws.acc[hh][1], ws.acc[hh][2], ws.acc[hh][3]);
+            *reinterpret_cast<const float4*>(ws.acc + hh * D + 4 * lane);
   }
 
   __device__ void write_quant(float* rec, QuantState& st) {
@@ -609,18 +684,11 @@ struct Kernel {
     const int k = lane & 3;
     const float qm = __shfl_sync(FULL, st.m, k);
     const float ql = __shfl_sync(FULL, st.l, k);
-    float wm = ws.m[0], wl = ws.l[0];
-#pragma unroll
-    for (int kk = 1; kk < MAX_GQA; ++kk)
-      if (k == kk) {
-        wm = ws.m[kk];
-        wl = ws.l[kk];
-      }
     float v;
     if (lane < 4) v = hasq ? qm : -INFINITY;
     else if (lane < 8) v = hasq ? ql : 0.f;
-    else if (lane < 12) v = hasw ? wm : -INFINITY;
-    else v = hasw ? wl : 0.f;
+    else if (lane < 12) v = hasw ? ws.ml[k] : -INFINITY;
+    else v = hasw ? ws.ml[4 + k] : 0.f;
     if (lane < 16) rec[lane] = v;
   }
 
@@ -712,6 +780,14 @@ struct Kernel {
     }
   }
 
+  __device__ void finish_unit(int u, int c, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
+    float* rec = record(u, c, warp);
+    if (kind == KIND_QUANT) write_quant(rec, st);
+    if (kind == KIND_WINDOW) write_window(rec, ws);
+    write_header(rec, hasq, st, hasw, ws);
+    arrive(u);
+  }
+
   __device__ void emit_empty(int u, int c) {
     float* rec = record(u, c, warp);
     if (lane < 16) rec[lane] = ((lane & 7) < 4) ? -INFINITY : 0.f;
@@ -720,7 +796,7 @@ struct Kernel {
 };
 
 template <int KF>
-__global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   Kernel<KF> K(a, smem);
   const int tid = threadIdx.x;
@@ -739,7 +815,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
   uint64_t* empty = full + NSTAGE;
   int4* desc = reinterpret_cast<int4*>(smem + SM_DESC);
 
-  // ---- per-sequence step counts: window chunks first, then quantised pages
+  // ---- per-sequence step counts: window chunks first, then quantised half-pages
   for (int b = tid; b < B; b += NTHREADS) {
     int L = a.seq_lens[b];
     if (L < 0 || L > a.max_seq_len) {
@@ -749,7 +825,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
     const int Lq = W > 0 ? max(0, L - W) : L;
     const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
     sL[b] = L;
-    sS[b] = nw + (Lq + PAGE - 1) / PAGE;
+    sS[b] = nw + (Lq + HALF - 1) / HALF;
   }
   __syncthreads();
   if (K.warp == 0) {
@@ -807,11 +883,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
   const int n = (int)(x1 - x0);
 
   if (K.warp == NCW) {
-    // ======================= producer
-    if (K.lane == 0) {
-      Pos ps = locate(x0, K.S_layer, B, H, K.sq);
-      int issued = 0;
-      for (int k = 0; k < n; ++k) {
+    // ======================= producer: lane w streams consumer warp w's steps w, w + NCW, ...
+    const int w = K.lane;
+    if (w < NCW && w < n) {
+      Pos ps = locate(x0 + w, K.S_layer, B, H, K.sq);
+      int issued = w;
+      for (int k = w; k < n; k += NCW) {
         const int slot = k % NSTAGE;
         if (k >= NSTAGE && !mbar_wait(empty + slot, ((k / NSTAGE) - 1) & 1, a.p.status)) break;
         const int u = (ps.ll * B + ps.b) * H + ps.h;
@@ -828,42 +905,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
           bulk_g2s(dst, a.p.ringk + ro, WCHUNK * D * 4, full + slot);
           bulk_g2s(dst + WCHUNK * D * 4, a.p.ringv + ro, WCHUNK * D * 4, full + slot);
         } else {
-          const int pi = ps.local - nw;
-          const int Lq = max(0, L - W);
-          const int Lqq = W > 0 ? Lq : L;
-          int ntok = min(PAGE, Lqq - pi * PAGE);
-          const int phys = a.block_table[(size_t)ps.b * a.max_pages_per_seq + pi];
+          const int hp = ps.local - nw;  // half-page index within the sequence
+          const int Lq = W > 0 ? max(0, L - W) : L;
+          const int ntok = min(HALF, Lq - hp * HALF);
+          const int phys = a.block_table[(size_t)ps.b * a.max_pages_per_seq + (hp >> 1)];
           if (phys < 0 || phys >= a.L.n_pages) {
             atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
             desc[slot] = make_int4(u, KIND_QUANT, 0, ps.local);
             mbar_arrive(full + slot);
           } else {
             desc[slot] = make_int4(u, KIND_QUANT, ntok, ps.local);
-            const uint8_t* src =
-                a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + ps.h) * (size_t)a.L.page_bytes;
-            mbar_arrive_tx(full + slot, a.L.page_bytes);
-            bulk_g2s(dst, src, a.L.page_bytes, full + slot);
+            const uint8_t* src = a.p.pages +
+                                 (((size_t)layer * a.L.n_pages + phys) * H + ps.h) * (size_t)a.L.page_bytes +
+                                 (size_t)(hp & 1) * a.L.half_bytes;
+            mbar_arrive_tx(full + slot, a.L.half_bytes);
+            bulk_g2s(dst, src, a.L.half_bytes, full + slot);
           }
         }
-        ++issued;
-        if (k + 1 < n) {
-          ps.local++;
-          if (ps.local == sS[ps.b]) {
-            ps.local = 0;
-            if (++ps.h == H) {
-              ps.h = 0;
-              do {
-                if (++ps.b == B) {
-                  ps.b = 0;
-                  ps.ll++;
-                }
-              } while (sS[ps.b] == 0);
-            }
-          }
-        }
+        issued = k;
+        if (k + NCW < n) advance(ps, NCW, B, H, K.sq);
       }
       // never leave the CTA with a copy still landing in shared memory
-      for (int k = max(0, issued - NSTAGE); k < issued; ++k)
+      for (int k = max(w, issued - NSTAGE + NCW); k <= issued; k += NCW)
         mbar_wait(full + (k % NSTAGE), (k / NSTAGE) & 1, a.p.status);
     }
     return;
@@ -877,27 +940,21 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
   const int c = blockIdx.x;
   QuantState st;
   WinState ws;
+  ws.q = reinterpret_cast<float*>(smem + SM_Q) + K.warp * MAX_GQA * D;
+  ws.acc = reinterpret_cast<float*>(smem + SM_SQ) + K.warp * MAX_GQA * D;
+  ws.ml = reinterpret_cast<float*>(smem + SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
-  int u_next = u_first;
-  auto unit_steps = [&](int u) { return sS[(u / H) % B]; };
-  auto finish = [&](int u) {
-    float* rec = K.record(u, c, K.warp);
-    if (kind == KIND_QUANT) K.write_quant(rec, st);
-    if (kind == KIND_WINDOW) K.write_window(rec, ws);
-    K.write_header(rec, hasq, st, hasw, ws);
-    K.arrive(u);
-  };
-  for (int k = K.warp; k < n; k += NCW) {
-    const int slot = k % NSTAGE;
-    if (!mbar_wait(full + slot, (k / NSTAGE) & 1, a.p.status)) break;
+  // step k = warp + NCW*m uses slot warp + NCW*(m & 1), phase (m >> 1) of that slot
+  for (int k = K.warp, m = 0; k < n; k += NCW, ++m) {
+    const int slot = K.warp + NCW * (m & 1);
+    if (!mbar_wait(full + slot, (m >> 1) & 1, a.p.status)) break;
     const int4 d = desc[slot];
     if (d.x != cur) {
-      if (cur >= 0) finish(cur);
-      for (int u = (cur >= 0 ? cur + 1 : u_next); u < d.x; ++u)
-        if (unit_steps(u) > 0) K.emit_empty(u, c);
+      if (cur >= 0) K.finish_unit(cur, c, kind, hasq, hasw, st, ws);
+      for (int u = (cur >= 0 ? cur + 1 : u_first); u < d.x; ++u)
+        if (sS[(u / H) % B] > 0) K.emit_empty(u, c);
       cur = d.x;
-      u_next = cur + 1;
       kind = -1;
       hasq = hasw = false;
     }
@@ -908,7 +965,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
       if (kind == KIND_WINDOW) hasw = true;
       else hasq = true;
     }
-    const uint8_t* stage = smem + SM_STAGES + slot * STAGE_BYTES;
+    uint8_t* stage = smem + SM_STAGES + slot * STAGE_BYTES;
     if (d.z > 0) {
       if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws);
       else K.quant_step(stage, d.z, st);
@@ -916,9 +973,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const DecodeArgs a)
     __syncwarp();
     if (K.lane == 0) mbar_arrive(empty + slot);
   }
-  if (cur >= 0) finish(cur);
-  for (int u = (cur >= 0 ? cur + 1 : u_next); u <= u_last; ++u)
-    if (unit_steps(u) > 0) K.emit_empty(u, c);
+  if (cur >= 0) K.finish_unit(cur, c, kind, hasq, hasw, st, ws);
+  for (int u = (cur >= 0 ? cur + 1 : u_first); u <= u_last; ++u)
+    if (sS[(u / H) % B] > 0) K.emit_empty(u, c);
 }
 
 }  // namespace

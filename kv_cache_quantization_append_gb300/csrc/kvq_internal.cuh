@@ -12,8 +12,9 @@
 namespace kvq {
 
 constexpr int D = 128;           // head_dim
-constexpr int PAGE = 64;         // tokens per page
-constexpr int WCHUNK = 8;        // window slots per pipeline stage
+constexpr int PAGE = 64;         // tokens per page (block-table granularity)
+constexpr int HALF = 32;         // tokens per half-page: one contiguous set of regions, one pipeline stage
+constexpr int WCHUNK = 4;        // window slots per pipeline stage
 constexpr int MAX_WINDOW = 1024;
 constexpr int MAX_GQA = 4;
 constexpr int MAX_BATCH = 1024;
@@ -33,7 +34,8 @@ struct Layout {
   size_t off_status, off_signs, off_cb, off_qjl, off_sigk, off_sigv, off_bt;
   size_t off_ringk, off_ringv, off_pages, total;
   int max_pages_per_seq, n_pages;
-  int page_bytes, off_vmain, off_kmeta, off_vmeta, kmeta_bytes;  // within a page
+  // A 64-token page is two 32-token halves, each laid out as K main | V main | K meta | V meta.
+  int page_bytes, half_bytes, off_vmain, off_kmeta, off_vmeta, kmeta_bytes;  // offsets within a half
 };
 
 // codebook block inside the header

@@ -10,7 +10,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-P = 64
+P = 64      # tokens per page (block-table granularity)
+H = 32      # tokens per half-page (one contiguous set of regions)
 
 
 def _a256(x: int) -> int:
@@ -20,7 +21,8 @@ def _a256(x: int) -> int:
 def regions(cfg, total: int) -> dict:
     tq = cfg.k_format == 3
     kmeta = 4 if tq else 16
-    page_bytes = 128 * P + kmeta * P + 16 * P
+    half_bytes = 128 * H + kmeta * H + 16 * H          # K main | V main | K meta | V meta (32 tokens)
+    page_bytes = 2 * half_bytes
     maxpps = -(-cfg.max_seq_len // P)
     n_pages = cfg.n_pages or cfg.max_batch * maxpps
     pages = cfg.n_layers * n_pages * cfg.n_kv_heads * page_bytes
@@ -33,9 +35,9 @@ def regions(cfg, total: int) -> dict:
     sig = _a256(cfg.n_layers * cfg.n_kv_heads * 128 * 2)
     off_sigv = off_bt - sig
     off_sigk = off_sigv - sig
-    return dict(page_bytes=page_bytes, n_pages=n_pages, maxpps=maxpps, off_pages=off_pages,
-                off_ringk=off_ringk, off_ringv=off_ringv, off_sigk=off_sigk, off_sigv=off_sigv,
-                kmeta=kmeta, off_bt=off_bt)
+    return dict(page_bytes=page_bytes, half_bytes=half_bytes, n_pages=n_pages, maxpps=maxpps,
+                off_pages=off_pages, off_ringk=off_ringk, off_ringv=off_ringv, off_sigk=off_sigk,
+                off_sigv=off_sigv, kmeta=kmeta, off_bt=off_bt)
 
 
 def _gather(buf: torch.Tensor, starts: np.ndarray, n: int) -> np.ndarray:
@@ -65,24 +67,25 @@ def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
         block_table = np.arange(cfg.max_batch * R["maxpps"]).reshape(cfg.max_batch, R["maxpps"])
     pos = np.arange(n_tokens)
     phys = block_table[b, pos // P].astype(np.int64)
-    pg = R["off_pages"] + ((layer * R["n_pages"] + phys) * cfg.n_kv_heads + h) * R["page_bytes"]
-    tin = pos % P
+    base = (R["off_pages"] + ((layer * R["n_pages"] + phys) * cfg.n_kv_heads + h) * R["page_bytes"] +
+            ((pos % P) // H) * R["half_bytes"])           # the half-page holding each position
+    t = pos % H
     out = {}
-    kmeta0 = pg + 128 * P
-    vmeta0 = kmeta0 + R["kmeta"] * P
+    kmeta0 = base + 128 * H
+    vmeta0 = kmeta0 + R["kmeta"] * H
     if cfg.k_format == 3:
-        out["k_code"] = _tq3_codes(_gather(buf, pg + tin * 48, 48))
-        sg = _gather(buf, pg + 48 * P + tin * 16, 16)
+        out["k_code"] = _tq3_codes(_gather(buf, base + t * 48, 48))
+        sg = _gather(buf, base + 48 * H + t * 16, 16)
         out["k_bits"] = np.unpackbits(sg, axis=1, bitorder="little").astype(bool)
-        out["k_norm"] = _gather(buf, kmeta0 + tin * 2, 2).view(np.float16)[:, 0]
-        out["k_gamma"] = _gather(buf, kmeta0 + 2 * P + tin * 2, 2).view(np.float16)[:, 0]
+        out["k_norm"] = _gather(buf, kmeta0 + t * 2, 2).view(np.float16)[:, 0]
+        out["k_gamma"] = _gather(buf, kmeta0 + 2 * H + t * 2, 2).view(np.float16)[:, 0]
     else:
-        out["k_code"] = _q4_codes(_gather(buf, pg + tin * 64, 64))
-        m = _gather(buf, kmeta0 + tin * 16, 16).view(np.float16)
+        out["k_code"] = _q4_codes(_gather(buf, base + t * 64, 64))
+        m = _gather(buf, kmeta0 + t * 16, 16).view(np.float16)
         out["k_scale"], out["k_zero"] = m[:, :4], m[:, 4:]
-    out["v_code"] = _q4_codes(_gather(buf, pg + 64 * P + tin * 64, 64))
-    sc = np.stack([_gather(buf, vmeta0 + (G * P + tin) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
-    zr = np.stack([_gather(buf, vmeta0 + 512 + (G * P + tin) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
+    out["v_code"] = _q4_codes(_gather(buf, base + 64 * H + t * 64, 64))
+    sc = np.stack([_gather(buf, vmeta0 + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
+    zr = np.stack([_gather(buf, vmeta0 + 8 * H + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
     out["v_scale"], out["v_zero"] = sc, zr
     return out
 

@@ -67,7 +67,7 @@ def test_bulk_append_equals_token_by_token(gpu_lib):
             kb, vb = layout.read_ring(b.buffer, b.cfg, 0, s, h)
             assert np.array_equal(ka.view(np.uint32), kb.view(np.uint32))
             assert np.array_equal(va.view(np.uint32), vb.view(np.uint32))
-    assert R["page_bytes"] == 10240
+    assert R["page_bytes"] == 10240 and R["half_bytes"] == 5120
 
 
 @pytest.mark.parametrize("window", [128, 0, 64])

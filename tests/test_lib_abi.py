@@ -66,7 +66,7 @@ def test_cache_bytes_closed_form(kvq, name):
 def test_invalid_configs_have_no_size(kvq):
     good = lib.make_config(2, 8, 24, 1, 1024)
     assert lib.kv_cache_bytes(good) > 0
-    for field, bad in (("head_dim", 64), ("n_q_heads", 23), ("n_q_heads", 48), ("window", 100),
+    for field, bad in (("head_dim", 64), ("n_q_heads", 23), ("n_q_heads", 48), ("window", 102),
                        ("page_tokens", 32), ("k_format", 7), ("max_batch", 0)):
         c = lib.make_config(2, 8, 24, 1, 1024)
         setattr(c, field, bad)
