@@ -112,9 +112,13 @@ typedef struct kvq_cache {
  *              gamma[32] (128 B)
  *     V meta   after K meta: fp16 scale[4][32] then fp16 zero[4][32] (group-major, 512 B)
  *   Half sizes: Q4G32 K + Q4G32 V = 5120 B, TQ3_QJL K + Q4G32 V = 4736 B.
- *   Q4G32 record (64 B): the 32 halfwords are indexed (r, G), r = 0..7, G = 0..3, halfword at byte
- *     8r + 2G holds channels 32G + 4r .. 32G + 4r + 3 of the rotated (and balanced) vector as
- *     nibbles, lowest channel in the lowest nibble.
+ *   Q4G32 K record (64 B per token): 32-bit word (i, G), i, G = 0..3, at byte 16i + 4G holds channels
+ *     32G + 8i .. 32G + 8i + 7 of the rotated (and balanced) vector; byte k of the word holds
+ *     channel 32G + 8i + 2k in its low nibble and the next channel in its high nibble.
+ *   Q4G32 V region (64 B per token): tokens 2p and 2p+1 of a half share bytes [128p, 128p + 128);
+ *     for r = 0..7, G = 0..3 the 4 bytes at 128p + 16*((r + 2*(p mod 4)) mod 8) + 4G are
+ *     [token 2p byte0, token 2p+1 byte0, token 2p byte1, token 2p+1 byte1], where byte0 holds
+ *     channels 32G + 4r (low nibble) and 32G + 4r + 1, byte1 channels 32G + 4r + 2 and + 3.
  *   TQ3 record: code of channel j at bits 3j .. 3j+2 of the 48-byte little-endian stream; sign
  *     bit i (= (S r)_i >= 0) at bit i of the 16-byte stream.
  */

@@ -291,7 +291,7 @@ size_t kv_decode_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t ba
   if (layers_of_call(cache, layer, &l0, &nl) != KVQ_OK) return 0;
   const int ctas = decode_ctas(cache->device);
   if (ctas <= 0) return 0;
-  return decode_scratch_bytes(nl * batch * cache->cfg.n_kv_heads, ctas);
+  return decode_scratch_bytes(nl * batch * cache->cfg.n_kv_heads, ctas, cache->cfg.k_format);
 }
 
 int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* out,
@@ -308,7 +308,7 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   const int ctas = decode_ctas(cache->device);
   if (ctas <= 0) return KVQ_ERR_CUDA;
   const int n_units = nl * batch * cache->cfg.n_kv_heads;
-  if (scratch_bytes < decode_scratch_bytes(n_units, ctas)) return KVQ_ERR_CAPACITY;
+  if (scratch_bytes < decode_scratch_bytes(n_units, ctas, cache->cfg.k_format)) return KVQ_ERR_CAPACITY;
   DecodeArgs a;
   a.p = dev_ptrs(*cache, L);
   a.L = L;

@@ -26,8 +26,8 @@ __device__ __forceinline__ uint32_t h16(__half h) { return (uint32_t)__half_as_u
 
 // Q4G32: per group of 32 channels exact min/max, fp16 scale (max-min)/15 and zero min, codes
 // clamp(rint((y - zero) / scale), 0, 15); 0 when the scale is 0.
-__device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, uint8_t* rec, __half& s16,
-                                          __half& z16) {
+__device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, int kv, int tin, uint8_t* main,
+                                          __half& s16, __half& z16) {
   float mn = fminf(fminf(y[0], y[1]), fminf(y[2], y[3]));
   float mx = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
 #pragma unroll
@@ -45,13 +45,22 @@ __device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, uint8_t
     if (s > 0.0f) c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(y[e], z), s)), 0), 15);
     hw |= (uint32_t)c << (4 * e);
   }
-  // halfword (r, G) = channels 32G + 4r .. +3 is stored at byte 8r + 2G; lane r gathers G = 0..3
-  const int r = lane & 7;
-  const uint32_t h0 = __shfl_sync(FULL, hw, r);
-  const uint32_t h1 = __shfl_sync(FULL, hw, r + 8);
-  const uint32_t h2 = __shfl_sync(FULL, hw, r + 16);
-  const uint32_t h3 = __shfl_sync(FULL, hw, r + 24);
-  if (lane < 8) *reinterpret_cast<uint2*>(rec + 8 * lane) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+  // lane 8G + r holds channels 32G + 4r .. +3 as the halfword hw (byte 0: channels +0,+1; byte 1: +2,+3)
+  if (kv == 0) {
+    // K record (64 B per token at 64 * tin): 32-bit word (i, G) at byte 16i + 4G holds channels
+    // 32G + 8i .. +7, i.e. the halfwords of lanes 8G + 2i (low) and 8G + 2i + 1 (high)
+    const int j = lane & 15, i = j >> 2, G = j & 3;
+    const uint32_t lo = __shfl_sync(FULL, hw, 8 * G + 2 * i);
+    const uint32_t hi = __shfl_sync(FULL, hw, 8 * G + 2 * i + 1);
+    if (lane < 16) reinterpret_cast<uint32_t*>(main + (size_t)tin * 64)[j] = lo | (hi << 16);
+  } else {
+    // V region: tokens 2p, 2p+1 share a 128-byte block; row r (= lane & 7) of group G sits at
+    // 16 * ((r + 2 * (p & 3)) & 7) + 4G as bytes [t0 byte0, t1 byte0, t0 byte1, t1 byte1]
+    const int r = lane & 7, G = lane >> 3, pp = tin >> 1, slot = tin & 1;
+    uint8_t* dst = main + (size_t)pp * 128 + 16 * ((r + 2 * (pp & 3)) & 7) + 4 * G + slot;
+    dst[0] = (uint8_t)(hw & 0xffu);
+    dst[2] = (uint8_t)(hw >> 8);
+  }
 }
 
 __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
@@ -170,8 +179,7 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
     for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(y[e], __half2float(sig[e]));
   }
   __half s16, z16;
-  uint8_t* rec = pg + (kv ? a.L.off_vmain : 0) + (size_t)tin * 64;
-  q4_encode(y, lane, rec, s16, z16);
+  q4_encode(y, lane, kv, tin, pg + (kv ? a.L.off_vmain : 0), s16, z16);
   if (kv == 0) {
     // K meta: per token {scale[4], zero[4]} fp16
     const uint32_t s0 = __shfl_sync(FULL, h16(s16), 0), s1 = __shfl_sync(FULL, h16(s16), 8);

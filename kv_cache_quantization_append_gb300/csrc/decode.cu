@@ -30,27 +30,36 @@ namespace kvq {
 
 namespace {
 
-constexpr int NCW = 11;                      // consumer warps
-constexpr int NTHREADS = (NCW + 1) * 32;     // 384: the 168-register budget of 12 warps
-constexpr int NSTAGE = 2 * NCW;              // two stages per consumer warp
 constexpr int STAGE_BYTES = 5120;            // max half-page (Q4/Q4) and window chunk (4 KB)
 constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
 
-// shared-memory carve-up (bytes)
-constexpr int SM_STAGES = 0;
-constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
-constexpr int SM_DESC = SM_BARS + 2 * NSTAGE * 8;
-constexpr int SM_Q = SM_DESC + NSTAGE * 16;                       // [NCW][4][128] float
-constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;               // [NCW][4][128] float (TQ)
-constexpr int SM_QSUM = SM_SQ + NCW * MAX_GQA * D * 4;            // [NCW][4][4] float
-constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                    // [64][32] u32 (TQ)
-constexpr int SM_LG = SM_LUT + 64 * 32 * 4;                       // [NCW][4][32] float logits
-constexpr int SM_P = SM_LG + NCW * MAX_GQA * HALF * 4;            // [NCW][4][32] fp16 probabilities
-constexpr int SM_WML = SM_P + NCW * MAX_GQA * HALF * 2;           // [NCW][8] float window m, l
-constexpr int SM_SEQ = SM_WML + NCW * 8 * 4;                      // 3 int arrays of batch+1
-constexpr int SM_FIXED = SM_SEQ;
+// Per-format CTA geometry and shared-memory carve-up (bytes): 11 consumer warps + 1 producer warp
+// (12 warps keep the 168-register budget per thread); measured faster than 15 consumer warps at 128
+// registers for Q4G32 keys (the build flag KVQ_Q4_CONSUMER_WARPS selects the latter).
+template <int KF>
+struct Geo {
+  static constexpr bool TQ = KF == KVQ_TQ3_QJL;
+#ifndef KVQ_Q4_CONSUMER_WARPS
+#define KVQ_Q4_CONSUMER_WARPS 11
+#endif
+  static constexpr int NCW = TQ ? 11 : KVQ_Q4_CONSUMER_WARPS;  // consumer warps
+  static constexpr int NTHREADS = (NCW + 1) * 32;      // + 1 producer warp
+  static constexpr int NSTAGE = 2 * NCW;               // two stages per consumer warp
+  static constexpr bool UNROLL_TILES = NCW <= 11;      // unrolled m-tiles need the larger budget
+  static constexpr int SM_STAGES = 0;
+  static constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
+  static constexpr int SM_DESC = SM_BARS + 2 * NSTAGE * 8;
+  static constexpr int SM_Q = SM_DESC + NSTAGE * 16;                         // [NCW][4][128] float
+  static constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;                 // [NCW][4][128] (TQ)
+  static constexpr int SM_QSUM = SM_SQ + (TQ ? NCW * MAX_GQA * D * 4 : 0);   // [NCW][4][4] float
+  static constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                      // [64][32] u32 (TQ)
+  static constexpr int SM_LG = SM_LUT + (TQ ? 64 * 32 * 4 : 0);              // [NCW][4][32] float
+  static constexpr int SM_P = SM_LG + NCW * MAX_GQA * HALF * 4;              // [NCW][4][32] fp16
+  static constexpr int SM_WML = SM_P + NCW * MAX_GQA * HALF * 2;             // [NCW][8] float
+  static constexpr int SM_SEQ = SM_WML + NCW * 8 * 4;                        // 3 int[batch+1]
+};
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -117,21 +126,20 @@ __device__ __forceinline__ float ex2(float x) {
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// Eight nibbles of w (bytes B0..B3, each = channel 2k low nibble, 2k+1 high nibble) -> four exact
-// fp16 pairs: (n0, n4), (n1, n5), (n2, n6), (n3, n7) where n_m is the m-th nibble.  A nibble ORed
-// into the mantissa of 1024.0 gives 1024 + c (or 1024 + 16c for a high nibble) exactly; the
-// subtraction / scaled fma back to c is exact in fp16.
-__device__ __forceinline__ void nib8(uint32_t w, uint32_t& p04, uint32_t& p15, uint32_t& p26, uint32_t& p37) {
-  const uint32_t M = 0x64006400u;
-  const __half2 k1024 = __float2half2_rn(1024.0f);
-  const __half2 k16 = __float2half2_rn(0.0625f);
-  const __half2 k64 = __float2half2_rn(-64.0f);
-  const uint32_t w8 = w >> 8;
-  p04 = h2u(__hsub2(u2h((w & 0x000F000Fu) | M), k1024));
-  p15 = h2u(__hfma2(u2h((w & 0x00F000F0u) | M), k16, k64));
-  p26 = h2u(__hsub2(u2h((w8 & 0x000F000Fu) | M), k1024));
-  p37 = h2u(__hfma2(u2h((w8 & 0x00F000F0u) | M), k16, k64));
+// Eight nibbles of w -> four exact fp16 pairs scaled by 2^-9: each nibble is moved into its own
+// byte and converted as an FP8 E4M3 value, which for bit patterns 0..15 (exponent field 0 or 1)
+// is exactly c * 2^-9.  lo0 = (n0, n2), lo1 = (n4, n6), hi0 = (n1, n3), hi1 = (n5, n7) where n_m is
+// the m-th nibble (low nibble of byte k is n_2k).
+__device__ __forceinline__ void cvt8(uint32_t w, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
+  const uint32_t lo = w & 0x0F0F0F0Fu;
+  const uint32_t hi = __umulhi(w, 1u << 28) & 0x0F0F0F0Fu;  // w >> 4 on the multiply pipe
+  asm("{\n .reg .b16 a, b, c, d;\n mov.b32 {a, b}, %4;\n mov.b32 {c, d}, %5;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
+      " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n}"
+      : "=r"(lo0), "=r"(lo1), "=r"(hi0), "=r"(hi1)
+      : "r"(lo), "r"(hi));
 }
+constexpr float CODE_UNSCALE = 512.0f;  // undoes the 2^-9 of cvt8
 
 __device__ __forceinline__ uint32_t split_pick(float v, bool lo) {
   const __half hi = __float2half_rn(v);
@@ -192,9 +200,10 @@ struct QuantState {
   float m, l;          // running max / partial sum for head (lane & 3)
 };
 
-// Window-part state of a warp, kept in its shared-memory slices so that it is not live in
-// registers while the warp streams quantised pages: q [4][128] (the q staging slice, reused by the
-// quantised part only after the window partial is written), acc [4][128] (the S q~ slice), m, l.
+// Window-part state of a warp, kept out of registers while the warp streams quantised pages:
+// q [4][128] in its shared-memory q slice (reused by the quantised part only after the window
+// steps of the unit), acc [4][128] directly in the warp's own partial record (global scratch,
+// written and read back only by this warp's lanes), m and l in a small shared slice.
 struct WinState {
   float* q;
   float* acc;
@@ -203,6 +212,10 @@ struct WinState {
 
 template <int KF>
 struct Kernel {
+  using GE = Geo<KF>;
+  static constexpr int NCW = GE::NCW;
+  static constexpr int SM_Q = GE::SM_Q, SM_SQ = GE::SM_SQ, SM_QSUM = GE::SM_QSUM, SM_LUT = GE::SM_LUT;
+  static constexpr int SM_LG = GE::SM_LG, SM_P = GE::SM_P;
   const DecodeArgs& a;
   uint8_t* smem;
   int lane, warp;
@@ -304,15 +317,17 @@ struct Kernel {
         d2 = d0 + 2;
         d3 = d0 + 3;
       } else {
-        // Q4: k-step (G, e) = (kk >> 1, kk & 1) holds channels 32G + 8i + {0,4 | 1,5} + 2e
+        // Q4: k-step (G, e) = (kk >> 1, kk & 1) holds channels 32G + 8i + 4e + {0,2 | 1,3}; the codes
+        // arrive scaled by 2^-9, so q~ is scaled by 2^9 (exact)
         const int G = kk >> 1, e = kk & 1;
-        d0 = 32 * G + 8 * i + 2 * e;
-        d1 = d0 + 4;
+        d0 = 32 * G + 8 * i + 4 * e;
+        d1 = d0 + 2;
         d2 = d0 + 1;
-        d3 = d0 + 5;
+        d3 = d0 + 3;
       }
-      const uint32_t v0 = hv ? split_pick(qh[d0], lo) : 0u, v1 = hv ? split_pick(qh[d1], lo) : 0u;
-      const uint32_t v2 = hv ? split_pick(qh[d2], lo) : 0u, v3 = hv ? split_pick(qh[d3], lo) : 0u;
+      const float us = (KF == KVQ_TQ3_QJL) ? 1.f : CODE_UNSCALE;
+      const uint32_t v0 = hv ? split_pick(qh[d0] * us, lo) : 0u, v1 = hv ? split_pick(qh[d1] * us, lo) : 0u;
+      const uint32_t v2 = hv ? split_pick(qh[d2] * us, lo) : 0u, v3 = hv ? split_pick(qh[d3] * us, lo) : 0u;
       st.qb[kk][0] = v0 | (v1 << 16);
       st.qb[kk][1] = v2 | (v3 << 16);
       if (KF == KVQ_TQ3_QJL) {
@@ -474,15 +489,14 @@ struct Kernel {
 #pragma unroll
       for (int G = 0; G < 4; ++G) {
         acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
-        // group G's 8 channels of this thread: halfwords (2i, G) and (2i+1, G)
-        const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
-        const uint32_t wa = __byte_perm((G < 2) ? ka.x : ka.y, (G < 2) ? ka.z : ka.w, sel);
-        const uint32_t wb = __byte_perm((G < 2) ? kb.x : kb.y, (G < 2) ? kb.z : kb.w, sel);
-        uint32_t a04, a15, a26, a37, b04, b15, b26, b37;
-        nib8(wa, a04, a15, a26, a37);
-        nib8(wb, b04, b15, b26, b37);
-        mma16816(acc[G], a04, b04, a15, b15, st.qb[2 * G][0], st.qb[2 * G][1]);
-        mma16816(acc[G], a26, b26, a37, b37, st.qb[2 * G + 1][0], st.qb[2 * G + 1][1]);
+        // word G of this thread's 16 bytes = channels 32G + 8i .. +7 of the token
+        const uint32_t wa = G == 0 ? ka.x : G == 1 ? ka.y : G == 2 ? ka.z : ka.w;
+        const uint32_t wb = G == 0 ? kb.x : G == 1 ? kb.y : G == 2 ? kb.z : kb.w;
+        uint32_t al0, al1, ah0, ah1, bl0, bl1, bh0, bh1;
+        cvt8(wa, al0, al1, ah0, ah1);
+        cvt8(wb, bl0, bl1, bh0, bh1);
+        mma16816(acc[G], al0, bl0, ah0, bh0, st.qb[2 * G][0], st.qb[2 * G][1]);
+        mma16816(acc[G], al1, bl1, ah1, bh1, st.qb[2 * G + 1][0], st.qb[2 * G + 1][1]);
       }
       const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
       const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
@@ -518,6 +532,64 @@ struct Kernel {
     __syncwarp();
   }
 
+  __device__ __forceinline__ void logits_tile(const uint8_t* stage, int mt, int ntok, bool tail, float lmask,
+                                              float* lgs, const QuantState& st, float& mx) {
+    const int r = lane >> 2;
+    float la, lb;
+    tile_logits(stage, mt, st, la, lb);
+    const int ta = 16 * mt + r;
+    float ma = lmask, mb = lmask;
+    if (tail) {
+      ma = ta < ntok ? lmask : -INFINITY;
+      mb = ta + 8 < ntok ? lmask : -INFINITY;
+    }
+    la += ma;
+    lb += mb;
+    lgs[ta] = la;
+    lgs[ta + 8] = lb;
+    mx = fmaxf(mx, fmaxf(la, lb));
+  }
+
+  __device__ __forceinline__ void pv_tile(const uint8_t* stage, int mt, bool colok, const __half* pcol,
+                                          QuantState& st) {
+    const int r = lane >> 2, i = lane & 3;
+    const uint8_t* vmain = stage + OFF_VMAIN;
+    const __half* vscale = reinterpret_cast<const __half*>(stage + OFF_VMETA);
+    const __half* vzero = vscale + 4 * HALF;
+
+    const int t0 = 16 * mt + 2 * i;
+    const uint32_t pA = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
+    const uint32_t pB = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
+    // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = unscaled p
+    uint32_t zA = 0u, zB = 0u;
+    if (r < 4) {
+      zA = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0);
+      zB = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0 + 8);
+    }
+    mma16816(st.zacc, zA, 0u, zB, 0u, pA, pB);
+    // V codes of tokens (t0, t0+1) and (t0+8, t0+9) for channel row r: one 16-byte block per token
+    // pair, word G = [t0 byte0, t1 byte0, t0 byte1, t1 byte1] of group G's channels 32G+4r..+3
+    const int p0 = 8 * mt + i;
+    const int blk = 16 * ((r + 2 * (p0 & 3)) & 7);
+    const uint4 vab = *reinterpret_cast<const uint4*>(vmain + p0 * 128 + blk);
+    const uint4 vcd = *reinterpret_cast<const uint4*>(vmain + (p0 + 4) * 128 + blk);
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+      // B operand for group G: p * scale (fp16)
+      const uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0);
+      const uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0 + 8);
+      const uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
+      const uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
+      const uint32_t wab = G == 0 ? vab.x : G == 1 ? vab.y : G == 2 ? vab.z : vab.w;
+      const uint32_t wcd = G == 0 ? vcd.x : G == 1 ? vcd.y : G == 2 ? vcd.z : vcd.w;
+      uint32_t x0, x2, x1, x3, y0, y2, y1, y3;
+      cvt8(wab, x0, x2, x1, x3);  // channel 32G + 4r + {0, 2, 1, 3}, tokens (t0, t0 + 1)
+      cvt8(wcd, y0, y2, y1, y3);  // same channels, tokens (t0 + 8, t0 + 9)
+      mma16816(st.acc[2 * G], x0, x1, y0, y1, bA, bB);
+      mma16816(st.acc[2 * G + 1], x2, x3, y2, y3, bA, bB);
+    }
+  }
+
   __device__ void quant_step(uint8_t* stage, int ntok, QuantState& st) {
     const int r = lane >> 2, i = lane & 3;
     const uint8_t* vmain = stage + OFF_VMAIN;
@@ -529,23 +601,14 @@ struct Kernel {
     const bool tail = ntok < HALF;
     if (tail) sanitize_tail(stage, ntok);
 
-    // ---- logits of the 32 tokens (two 16-token m-tiles, rolled to keep the loop body small)
+    // ---- logits of the 32 tokens (two 16-token m-tiles)
     float mx = -INFINITY;
+    if (GE::UNROLL_TILES) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) logits_tile(stage, mt, ntok, tail, lmask, lgs, st, mx);
+    } else {
 #pragma unroll 1
-    for (int mt = 0; mt < 2; ++mt) {
-      float la, lb;
-      tile_logits(stage, mt, st, la, lb);
-      const int ta = 16 * mt + r;
-      float ma = lmask, mb = lmask;
-      if (tail) {
-        ma = ta < ntok ? lmask : -INFINITY;
-        mb = ta + 8 < ntok ? lmask : -INFINITY;
-      }
-      la += ma;
-      lb += mb;
-      lgs[ta] = la;
-      lgs[ta + 8] = lb;
-      mx = fmaxf(mx, fmaxf(la, lb));
+      for (int mt = 0; mt < 2; ++mt) logits_tile(stage, mt, ntok, tail, lmask, lgs, st, mx);
     }
 
     // ---- online softmax update for head i (rows r = 0..7 share it); 2^(-inf - m) = 0 handles
@@ -587,39 +650,12 @@ struct Kernel {
     // ---- P.V: k-step = 16 tokens; this thread's B column is head r (r < g), tokens t0, t0+1, +8, +9
     const bool colok = r < g;
     const __half* pcol = pw + (r & 3) * HALF;
-#pragma unroll 1
-    for (int mt = 0; mt < 2; ++mt) {
-      const int t0 = 16 * mt + 2 * i;
-      const uint32_t pA = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
-      const uint32_t pB = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
-      // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = unscaled p
-      uint32_t zA = 0u, zB = 0u;
-      if (r < 4) {
-        zA = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0);
-        zB = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0 + 8);
-      }
-      mma16816(st.zacc, zA, 0u, zB, 0u, pA, pB);
-      // V codes of the four tokens for channel rows r: 8 bytes = halfwords (r, G = 0..3)
-      const uint2 va = *reinterpret_cast<const uint2*>(vmain + t0 * 64 + 8 * r);
-      const uint2 vb = *reinterpret_cast<const uint2*>(vmain + (t0 + 1) * 64 + 8 * r);
-      const uint2 vc = *reinterpret_cast<const uint2*>(vmain + (t0 + 8) * 64 + 8 * r);
-      const uint2 vd = *reinterpret_cast<const uint2*>(vmain + (t0 + 9) * 64 + 8 * r);
+    if (GE::UNROLL_TILES) {
 #pragma unroll
-      for (int G = 0; G < 4; ++G) {
-        // B operand for group G: p * scale (fp16)
-        const uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0);
-        const uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0 + 8);
-        const uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
-        const uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
-        const uint32_t sel = (G & 1) ? 0x7632u : 0x5410u;
-        const uint32_t wab = __byte_perm((G < 2) ? va.x : va.y, (G < 2) ? vb.x : vb.y, sel);
-        const uint32_t wcd = __byte_perm((G < 2) ? vc.x : vc.y, (G < 2) ? vd.x : vd.y, sel);
-        uint32_t ab0, ab1, ab2, ab3, cd0, cd1, cd2, cd3;
-        nib8(wab, ab0, ab1, ab2, ab3);  // channel 32G + 4r + {0, 1, 2, 3}, tokens (t0, t0 + 1)
-        nib8(wcd, cd0, cd1, cd2, cd3);  // same channels, tokens (t0 + 8, t0 + 9)
-        mma16816(st.acc[2 * G], ab0, ab1, cd0, cd1, bA, bB);
-        mma16816(st.acc[2 * G + 1], ab2, ab3, cd2, cd3, bA, bB);
-      }
+      for (int mt = 0; mt < 2; ++mt) pv_tile(stage, mt, colok, pcol, st);
+    } else {
+#pragma unroll 1
+      for (int mt = 0; mt < 2; ++mt) pv_tile(stage, mt, colok, pcol, st);
     }
     __syncwarp();
   }
@@ -629,27 +665,20 @@ struct Kernel {
     return a.records + ((size_t)(u + c) * NCW + w) * REC_FLOATS;
   }
 
-  __device__ void write_window(float* rec, const WinState& ws) {
-#pragma unroll
-    for (int hh = 0; hh < MAX_GQA; ++hh)
-      if (hh < g && ws.ml[4 + hh] > 0.f)
-        *reinterpret_cast<float4*>(rec + 16 + MAX_GQA * D + hh * D + 4 * lane) =
-            *reinterpret_cast<const float4*>(ws.acc + hh * D + 4 * lane);
-  }
-
   __device__ void write_quant(float* rec, QuantState& st) {
     const int r = lane >> 2, i = lane & 3;
-    // fold the zero-point term into the accumulators: acc[h][c] += zterm[G(c)][h]
+    // undo the 2^-9 of the converted codes and fold in the zero-point term:
+    // acc[h][c] = 512 * acc[h][c] + zterm[G(c)][h]
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
       const float z0 = __shfl_sync(FULL, st.zacc[0], 4 * G + i);
       const float z1 = __shfl_sync(FULL, st.zacc[1], 4 * G + i);
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        st.acc[2 * G + e][0] += z0;
-        st.acc[2 * G + e][1] += z1;
-        st.acc[2 * G + e][2] += z0;
-        st.acc[2 * G + e][3] += z1;
+        st.acc[2 * G + e][0] = st.acc[2 * G + e][0] * CODE_UNSCALE + z0;
+        st.acc[2 * G + e][1] = st.acc[2 * G + e][1] * CODE_UNSCALE + z1;
+        st.acc[2 * G + e][2] = st.acc[2 * G + e][2] * CODE_UNSCALE + z0;
+        st.acc[2 * G + e][3] = st.acc[2 * G + e][3] * CODE_UNSCALE + z1;
       }
     }
     float l = st.l;
@@ -783,7 +812,6 @@ struct Kernel {
   __device__ void finish_unit(int u, int c, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
     float* rec = record(u, c, warp);
     if (kind == KIND_QUANT) write_quant(rec, st);
-    if (kind == KIND_WINDOW) write_window(rec, ws);
     write_header(rec, hasq, st, hasw, ws);
     arrive(u);
   }
@@ -796,7 +824,9 @@ struct Kernel {
 };
 
 template <int KF>
-__global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
+  using GE = Geo<KF>;
+  constexpr int NCW = GE::NCW, NSTAGE = GE::NSTAGE, NTHREADS = GE::NTHREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
   Kernel<KF> K(a, smem);
   const int tid = threadIdx.x;
@@ -808,12 +838,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   K.g = a.g;
   K.Hq = a.Hkv * a.g;
   const int B = a.batch, H = a.Hkv, W = a.W;
-  int* sS = reinterpret_cast<int*>(smem + SM_SEQ);
+  int* sS = reinterpret_cast<int*>(smem + GE::SM_SEQ);
   int* sPre = sS + (B + 1);
   int* sL = sPre + (B + 1);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM_BARS);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + GE::SM_BARS);
   uint64_t* empty = full + NSTAGE;
-  int4* desc = reinterpret_cast<int4*>(smem + SM_DESC);
+  int4* desc = reinterpret_cast<int4*>(smem + GE::SM_DESC);
 
   // ---- per-sequence step counts: window chunks first, then quantised half-pages
   for (int b = tid; b < B; b += NTHREADS) {
@@ -855,7 +885,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (KF == KVQ_TQ3_QJL) {
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + SM_LUT);
+    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + GE::SM_LUT);
     for (int idx = tid; idx < 64 * 32; idx += NTHREADS) lut[idx] = a.p.cb->lut[idx >> 5];
   }
   __syncthreads();
@@ -895,7 +925,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
         const int layer = a.layer0 + ps.ll;
         const int L = sL[ps.b];
         const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
-        uint8_t* dst = smem + SM_STAGES + slot * STAGE_BYTES;
+        uint8_t* dst = smem + GE::SM_STAGES + slot * STAGE_BYTES;
         if (ps.local < nw) {
           const int s0 = ps.local * WCHUNK;
           const int ntok = min(WCHUNK, min(L, W) - s0);
@@ -940,9 +970,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
   const int c = blockIdx.x;
   QuantState st;
   WinState ws;
-  ws.q = reinterpret_cast<float*>(smem + SM_Q) + K.warp * MAX_GQA * D;
-  ws.acc = reinterpret_cast<float*>(smem + SM_SQ) + K.warp * MAX_GQA * D;
-  ws.ml = reinterpret_cast<float*>(smem + SM_WML) + K.warp * 8;
+  ws.q = reinterpret_cast<float*>(smem + GE::SM_Q) + K.warp * MAX_GQA * D;
+  ws.acc = nullptr;  // set to the unit's record when its window steps start
+  ws.ml = reinterpret_cast<float*>(smem + GE::SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
   // step k = warp + NCW*m uses slot warp + NCW*(m & 1), phase (m >> 1) of that slot
@@ -959,13 +989,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
       hasq = hasw = false;
     }
     if (d.y != kind) {
-      if (kind == KIND_WINDOW) K.write_window(K.record(cur, c, K.warp), ws);
+      if (d.y == KIND_WINDOW) ws.acc = K.record(cur, c, K.warp) + 16 + MAX_GQA * D;
       K.load_q(cur, st, ws, d.y);
       kind = d.y;
       if (kind == KIND_WINDOW) hasw = true;
       else hasq = true;
     }
-    uint8_t* stage = smem + SM_STAGES + slot * STAGE_BYTES;
+    uint8_t* stage = smem + GE::SM_STAGES + slot * STAGE_BYTES;
     if (d.z > 0) {
       if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws);
       else K.quant_step(stage, d.z, st);
@@ -980,23 +1010,22 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_kernel(const __grid_consta
 
 }  // namespace
 
-size_t decode_scratch_bytes(int n_units, int n_ctas) {
-  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + n_ctas) * NCW * REC_FLOATS * sizeof(float);
+size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
+  const int ncw = k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
+  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + n_ctas) * ncw * REC_FLOATS * sizeof(float);
+}
+
+template <int KF>
+static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
+  const size_t smem = Geo<KF>::SM_SEQ + 3 * (size_t)(a.batch + 1) * sizeof(int);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<KF><<<a.n_ctas, Geo<KF>::NTHREADS, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  const size_t smem = SM_FIXED + 3 * (size_t)(a.batch + 1) * sizeof(int);
-  cudaError_t e;
-  if (a.k_format == KVQ_TQ3_QJL) {
-    e = cudaFuncSetAttribute(decode_kernel<KVQ_TQ3_QJL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<KVQ_TQ3_QJL><<<a.n_ctas, NTHREADS, smem, s>>>(a);
-  } else {
-    e = cudaFuncSetAttribute(decode_kernel<KVQ_Q4G32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    decode_kernel<KVQ_Q4G32><<<a.n_ctas, NTHREADS, smem, s>>>(a);
-  }
-  return cudaGetLastError();
+  return a.k_format == KVQ_TQ3_QJL ? launch_kf<KVQ_TQ3_QJL>(a, s) : launch_kf<KVQ_Q4G32>(a, s);
 }
 
 }  // namespace kvq

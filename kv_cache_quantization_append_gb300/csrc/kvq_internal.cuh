@@ -95,7 +95,7 @@ struct DecodeArgs {
   int max_pages_per_seq, n_units, n_ctas;
 };
 int decode_ctas(int device);
-size_t decode_scratch_bytes(int n_units, int n_ctas);
+size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- device helpers

@@ -46,12 +46,31 @@ def _gather(buf: torch.Tensor, starts: np.ndarray, n: int) -> np.ndarray:
     return buf[idx.reshape(-1)].reshape(len(starts), n).cpu().numpy()
 
 
-def _q4_codes(rec: np.ndarray) -> np.ndarray:
-    """rec [T][64] bytes -> codes [T][128]: halfword (r, G) at byte 8r + 2G = channels 32G+4r..+3."""
-    hw = rec.reshape(-1, 8, 4, 2).astype(np.uint16)
-    hw = hw[..., 0] | (hw[..., 1] << 8)                        # [T][r][G]
-    nib = (hw[..., None] >> (4 * np.arange(4, dtype=np.uint16))) & 15   # [T][r][G][e]
-    return nib.transpose(0, 2, 1, 3).reshape(-1, 128).astype(np.uint8)   # channel 32G + 4r + e
+def _q4k_codes(rec: np.ndarray) -> np.ndarray:
+    """K record [T][64]: word (i, G) at byte 16i + 4G holds channels 32G + 8i .. +7, byte k = channels
+    32G + 8i + 2k (low nibble) and + 1 (high nibble)."""
+    b = rec.reshape(-1, 4, 4, 4)                                # [T][i][G][k]
+    nib = np.stack([b & 15, b >> 4], axis=-1)                   # [T][i][G][k][lo/hi]
+    return nib.transpose(0, 2, 1, 3, 4).reshape(-1, 128).astype(np.uint8)   # channel 32G + 8i + 2k + e
+
+
+def _q4v_codes(half_v: np.ndarray, t: np.ndarray) -> np.ndarray:
+    """V codes of tokens t from the V region of their half-pages (half_v [T][2048] bytes): tokens 2p and
+    2p+1 share 128 bytes; row r of group G is at 16*((r + 2*(p & 3)) & 7) + 4G with bytes
+    [t0 byte0, t1 byte0, t0 byte1, t1 byte1]; byte0 = channels 32G+4r (low), +1; byte1 = +2, +3."""
+    p = t // 2
+    slot = t % 2
+    out = np.zeros((len(t), 128), np.uint8)
+    for r in range(8):
+        blk = 16 * ((r + 2 * (p & 3)) & 7)
+        for G in range(4):
+            base = p * 128 + blk + 4 * G + slot
+            b0 = half_v[np.arange(len(t)), base]
+            b1 = half_v[np.arange(len(t)), base + 2]
+            c = 32 * G + 4 * r
+            out[:, c], out[:, c + 1] = b0 & 15, b0 >> 4
+            out[:, c + 2], out[:, c + 3] = b1 & 15, b1 >> 4
+    return out
 
 
 def _tq3_codes(rec: np.ndarray) -> np.ndarray:
@@ -80,10 +99,10 @@ def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
         out["k_norm"] = _gather(buf, kmeta0 + t * 2, 2).view(np.float16)[:, 0]
         out["k_gamma"] = _gather(buf, kmeta0 + 2 * H + t * 2, 2).view(np.float16)[:, 0]
     else:
-        out["k_code"] = _q4_codes(_gather(buf, base + t * 64, 64))
+        out["k_code"] = _q4k_codes(_gather(buf, base + t * 64, 64))
         m = _gather(buf, kmeta0 + t * 16, 16).view(np.float16)
         out["k_scale"], out["k_zero"] = m[:, :4], m[:, 4:]
-    out["v_code"] = _q4_codes(_gather(buf, base + 64 * H + t * 64, 64))
+    out["v_code"] = _q4v_codes(_gather(buf, base + 64 * H, 64 * H), t)
     sc = np.stack([_gather(buf, vmeta0 + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
     zr = np.stack([_gather(buf, vmeta0 + 8 * H + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
     out["v_scale"], out["v_zero"] = sc, zr
