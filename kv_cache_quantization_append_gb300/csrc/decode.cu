@@ -8,12 +8,12 @@
 //
 // Design for GB300 (one CTA per SM: 11 consumer warps + 1 producer warp):
 //  * The work of a call is a list of "steps" -- one 32-token half-page or one 4-slot window chunk
-//    of one (layer, sequence, kv-head) unit, window chunks first -- cut into equal contiguous
-//    ranges, one per CTA, so every SM streams the same bytes whatever the sequence lengths.
-//  * Consumer warp w takes the CTA's steps w, w + 11, ...; it owns two shared-memory stages
-//    (slots w and w + 11 of 22).  Lane w of the producer warp streams exactly that warp's steps
-//    with cp.async.bulk (the 1D TMA path) completing on mbarriers, so no consumer ever waits
-//    behind another one's progress.
+//    of one (layer, sequence, kv-head) unit, window chunks first.
+//  * The list is cut into equal contiguous ranges, one per consumer warp of every CTA (stream-K
+//    at warp granularity), so every warp streams the same bytes whatever the sequence lengths and
+//    touches only one to a few units.  Consumer warp w owns two shared-memory stages (slots w and
+//    w + 11 of 22); lane w of the producer warp streams exactly that warp's range with
+//    cp.async.bulk (the 1D TMA path) completing on mbarriers.
 //  * Consumer warps dequantise nibbles to fp16 in registers (exponent-bias trick: OR a nibble into
 //    the mantissa of 1024.0, subtract exactly) and run the logits and P.V as tensor-core
 //    mma.sync m16n8k16 (fp32 accumulate): GQA query heads are the N axis (hi and lo halves of q
@@ -221,7 +221,7 @@ struct Kernel {
   int lane, warp;
   int B, H, W, g, Hq;
   long long S_layer, S;
-  long long nct;  // CTAs that own steps: min(gridDim.x, S), each owns at least one
+  long long nw;  // warps that own steps: min(gridDim.x * NCW, S), each owns at least one
   Seq sq;
 
   __device__ Kernel(const DecodeArgs& args, uint8_t* s) : a(args), smem(s) {}
@@ -229,8 +229,9 @@ struct Kernel {
   __device__ __forceinline__ long long steps_before(int ll, int b, int h) const {
     return (long long)ll * S_layer + (long long)H * sq.pre[b] + (long long)h * sq.S[b];
   }
-  // CTA whose contiguous step range holds step x; the ranges split S steps over nct CTAs
-  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * nct - 1) / S); }
+  // global consumer warp whose contiguous step range holds step x; the ranges split the S steps
+  // over nw warps (warp gw = CTA * NCW + warp owns [gw*S/nw, (gw+1)*S/nw))
+  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * nw - 1) / S); }
 
   // ---------------------------------------------------------------- unit set-up
   __device__ void load_q(int u, QuantState& st, WinState& ws, int kind) {
@@ -661,8 +662,10 @@ struct Kernel {
   }
 
   // ---------------------------------------------------------------- records and merge
-  __device__ __forceinline__ float* record(int u, int c, int w) const {
-    return a.records + ((size_t)(u + c) * NCW + w) * REC_FLOATS;
+  // partial record of (unit u, global warp gw): the index u + gw is unique because both the units
+  // and the warps' step ranges are ordered along the step list
+  __device__ __forceinline__ float* record(int u, int gw) const {
+    return a.records + (size_t)(u + gw) * REC_FLOATS;
   }
 
   __device__ void write_quant(float* rec, QuantState& st) {
@@ -734,16 +737,14 @@ struct Kernel {
         const int mo = kind ? 8 : 0, lo = kind ? 12 : 4;
         const int ao = 16 + (kind ? MAX_GQA * D : 0) + hh * D + 4 * lane;
         float M = -INFINITY;
-        for (int c = cf; c <= cl; ++c)
-          for (int w = 0; w < NCW; ++w) {
-            const float* rec = record(u, c, w);
-            if (__ldcg(rec + lo + hh) > 0.f) M = fmaxf(M, __ldcg(rec + mo + hh));
-          }
+        for (int gw = cf; gw <= cl; ++gw) {
+          const float* rec = record(u, gw);
+          if (__ldcg(rec + lo + hh) > 0.f) M = fmaxf(M, __ldcg(rec + mo + hh));
+        }
         float L = 0.f;
         float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = cf; c <= cl; ++c)
-          for (int w = 0; w < NCW; ++w) {
-            const float* rec = record(u, c, w);
+        for (int gw = cf; gw <= cl; ++gw) {
+            const float* rec = record(u, gw);
             const float l = __ldcg(rec + lo + hh);
             if (l > 0.f) {
               const float f = exp2f(__ldcg(rec + mo + hh) - M);
@@ -794,7 +795,7 @@ struct Kernel {
   __device__ void arrive(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const long long sb = steps_before(ll, b, h);
-    const int ncta = owner(sb + sq.S[b] - 1) - owner(sb) + 1;
+    const int nwu = owner(sb + sq.S[b] - 1) - owner(sb) + 1;
     __syncwarp();
     int old = 0;
     if (lane == 0) {
@@ -802,25 +803,20 @@ struct Kernel {
       old = atomicAdd(a.counters + u, 1);
     }
     old = __shfl_sync(FULL, old, 0);
-    if (old == NCW * ncta - 1) {
+    if (old == nwu - 1) {
       __threadfence();
       merge(u);
       if (lane == 0) a.counters[u] = 0;
     }
   }
 
-  __device__ void finish_unit(int u, int c, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
-    float* rec = record(u, c, warp);
+  __device__ void finish_unit(int u, int gw, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
+    float* rec = record(u, gw);
     if (kind == KIND_QUANT) write_quant(rec, st);
     write_header(rec, hasq, st, hasw, ws);
     arrive(u);
   }
 
-  __device__ void emit_empty(int u, int c) {
-    float* rec = record(u, c, warp);
-    if (lane < 16) rec[lane] = ((lane & 7) < 4) ? -INFINITY : 0.f;
-    arrive(u);
-  }
 };
 
 template <int KF>
@@ -906,27 +902,27 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   K.S_layer = (long long)H * sPre[B];
   K.S = K.S_layer * a.n_layers_call;
   if (K.S == 0) return;
-  K.nct = min((long long)gridDim.x, K.S);
-  if (blockIdx.x >= K.nct) return;
-  const long long x0 = (long long)blockIdx.x * K.S / K.nct;
-  const long long x1 = (long long)(blockIdx.x + 1) * K.S / K.nct;
-  const int n = (int)(x1 - x0);
+  K.nw = min((long long)gridDim.x * NCW, K.S);
+  if ((long long)blockIdx.x * NCW >= K.nw) return;
 
   if (K.warp == NCW) {
-    // ======================= producer: lane w streams consumer warp w's steps w, w + NCW, ...
+    // ======================= producer: lane w streams consumer warp w's contiguous step range
     const int w = K.lane;
-    if (w < NCW && w < n) {
-      Pos ps = locate(x0 + w, K.S_layer, B, H, K.sq);
-      int issued = w;
-      for (int k = w; k < n; k += NCW) {
-        const int slot = k % NSTAGE;
-        if (k >= NSTAGE && !mbar_wait(empty + slot, ((k / NSTAGE) - 1) & 1, a.p.status)) break;
+    const long long gw = (long long)blockIdx.x * NCW + w;
+    if (w < NCW && gw < K.nw) {
+      const long long xs = gw * K.S / K.nw, xe = (gw + 1) * K.S / K.nw;
+      const int n = (int)(xe - xs);
+      Pos ps = locate(xs, K.S_layer, B, H, K.sq);
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int slot = w + NCW * (k & 1);
+        if (k >= 2 && !mbar_wait(empty + slot, ((k >> 1) - 1) & 1, a.p.status)) break;
         const int u = (ps.ll * B + ps.b) * H + ps.h;
         const int layer = a.layer0 + ps.ll;
         const int L = sL[ps.b];
-        const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
+        const int nwin = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
         uint8_t* dst = smem + GE::SM_STAGES + slot * STAGE_BYTES;
-        if (ps.local < nw) {
+        if (ps.local < nwin) {
           const int s0 = ps.local * WCHUNK;
           const int ntok = min(WCHUNK, min(L, W) - s0);
           desc[slot] = make_int4(u, KIND_WINDOW, ntok, ps.local);
@@ -935,7 +931,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
           bulk_g2s(dst, a.p.ringk + ro, WCHUNK * D * 4, full + slot);
           bulk_g2s(dst + WCHUNK * D * 4, a.p.ringv + ro, WCHUNK * D * 4, full + slot);
         } else {
-          const int hp = ps.local - nw;  // half-page index within the sequence
+          const int hp = ps.local - nwin;  // half-page index within the sequence
           const int Lq = W > 0 ? max(0, L - W) : L;
           const int ntok = min(HALF, Lq - hp * HALF);
           const int phys = a.block_table[(size_t)ps.b * a.max_pages_per_seq + (hp >> 1)];
@@ -952,22 +948,20 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
             bulk_g2s(dst, src, a.L.half_bytes, full + slot);
           }
         }
-        issued = k;
-        if (k + NCW < n) advance(ps, NCW, B, H, K.sq);
+        issued = k + 1;
+        if (k + 1 < n) advance(ps, 1, B, H, K.sq);
       }
       // never leave the CTA with a copy still landing in shared memory
-      for (int k = max(w, issued - NSTAGE + NCW); k <= issued; k += NCW)
-        mbar_wait(full + (k % NSTAGE), (k / NSTAGE) & 1, a.p.status);
+      for (int k = max(0, issued - 2); k < issued; ++k)
+        mbar_wait(full + w + NCW * (k & 1), (k >> 1) & 1, a.p.status);
     }
     return;
   }
 
-  // ======================= consumers
-  const Pos pf = locate(x0, K.S_layer, B, H, K.sq);
-  const Pos pl = locate(x1 - 1, K.S_layer, B, H, K.sq);
-  const int u_first = (pf.ll * B + pf.b) * H + pf.h;
-  const int u_last = (pl.ll * B + pl.b) * H + pl.h;
-  const int c = blockIdx.x;
+  // ======================= consumers: warp gw processes steps [gw*S/nw, (gw+1)*S/nw) in order
+  const long long gw = (long long)blockIdx.x * NCW + K.warp;
+  if (gw >= K.nw) return;
+  const int n = (int)((gw + 1) * K.S / K.nw - gw * K.S / K.nw);
   QuantState st;
   WinState ws;
   ws.q = reinterpret_cast<float*>(smem + GE::SM_Q) + K.warp * MAX_GQA * D;
@@ -975,21 +969,19 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   ws.ml = reinterpret_cast<float*>(smem + GE::SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
-  // step k = warp + NCW*m uses slot warp + NCW*(m & 1), phase (m >> 1) of that slot
-  for (int k = K.warp, m = 0; k < n; k += NCW, ++m) {
-    const int slot = K.warp + NCW * (m & 1);
-    if (!mbar_wait(full + slot, (m >> 1) & 1, a.p.status)) break;
+  // step k uses slot warp + NCW*(k & 1), phase (k >> 1) of that slot
+  for (int k = 0; k < n; ++k) {
+    const int slot = K.warp + NCW * (k & 1);
+    if (!mbar_wait(full + slot, (k >> 1) & 1, a.p.status)) break;
     const int4 d = desc[slot];
     if (d.x != cur) {
-      if (cur >= 0) K.finish_unit(cur, c, kind, hasq, hasw, st, ws);
-      for (int u = (cur >= 0 ? cur + 1 : u_first); u < d.x; ++u)
-        if (sS[(u / H) % B] > 0) K.emit_empty(u, c);
+      if (cur >= 0) K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
       cur = d.x;
       kind = -1;
       hasq = hasw = false;
     }
     if (d.y != kind) {
-      if (d.y == KIND_WINDOW) ws.acc = K.record(cur, c, K.warp) + 16 + MAX_GQA * D;
+      if (d.y == KIND_WINDOW) ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
       K.load_q(cur, st, ws, d.y);
       kind = d.y;
       if (kind == KIND_WINDOW) hasw = true;
@@ -1003,16 +995,14 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     __syncwarp();
     if (K.lane == 0) mbar_arrive(empty + slot);
   }
-  if (cur >= 0) K.finish_unit(cur, c, kind, hasq, hasw, st, ws);
-  for (int u = (cur >= 0 ? cur + 1 : u_first); u <= u_last; ++u)
-    if (sS[(u / H) % B] > 0) K.emit_empty(u, c);
+  if (cur >= 0) K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
 }
 
 }  // namespace
 
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
   const int ncw = k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
-  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + n_ctas) * ncw * REC_FLOATS * sizeof(float);
+  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + (size_t)n_ctas * ncw) * REC_FLOATS * sizeof(float);
 }
 
 template <int KF>
