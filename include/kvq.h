@@ -187,6 +187,26 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
                         const int32_t* seq_lens, int32_t batch, void* scratch,
                         size_t scratch_bytes, void* stream);
 
+/*
+ * Allocation-free variant of kv_decode_attention (no counterpart on the pages: it exists for
+ * callers that cannot allocate device memory -- hosts that own every device allocation
+ * themselves, such as a serving engine that hands a plugin only pre-planned buffers, or a C caller
+ * without an allocator of its own).  Same arguments and results as kv_decode_attention minus the
+ * scratch buffer: the scratch comes from a fixed array of KVQ_NOALLOC_SCRATCH_MAX bytes inside the
+ * library's device memory, held on every device that uses it until the process exits.
+ *   - Calls needing more scratch than that (kv_decode_scratch_bytes > KVQ_NOALLOC_SCRATCH_MAX)
+ *     return KVQ_ERR_CAPACITY and launch nothing.
+ *   - The first call on a device looks up the array's device address (once per device, with that
+ *     device current); make that first call before any stream capture.
+ *   - Every call shares the one array: the call clears the arrival counters it needs on ``stream``
+ *     before its kernel, but calls that overlap on the GPU (other streams, other host threads)
+ *     race on the array and must be serialised by the caller.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+#define KVQ_NOALLOC_SCRATCH_MAX (32u * 1024u * 1024u)
+int kv_decode_attention_noalloc(kvq_cache* cache, int32_t layer, const void* q, float* out,
+                                const int32_t* seq_lens, int32_t batch, void* stream);
+
 /* Read and clear the device status word (synchronises ``stream``); *flags gets KVQ_DEV_* bits. */
 int kv_status(kvq_cache* cache, uint32_t* flags, void* stream);
 

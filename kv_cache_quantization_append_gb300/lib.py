@@ -27,8 +27,9 @@ DEV_SEQLEN_RANGE = 4
 DEV_TIMEOUT = 8
 
 EXPORTS = ("kv_cache_bytes", "kv_cache_init", "kv_calibrate_scratch_bytes", "kv_calibrate",
-           "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention", "kv_status",
-           "kv_strerror")
+           "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention",
+           "kv_decode_attention_noalloc", "kv_status", "kv_strerror")
+NOALLOC_SCRATCH_MAX = 32 * 1024 * 1024
 
 
 class kvq_config(ctypes.Structure):
@@ -73,6 +74,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_quant_append": (ctypes.c_int, [cachep, I32, P, P, P, I32, I32, P]),
         "kv_decode_scratch_bytes": (SZ, [cachep, I32, I32]),
         "kv_decode_attention": (ctypes.c_int, [cachep, I32, P, P, P, I32, P, SZ, P]),
+        "kv_decode_attention_noalloc": (ctypes.c_int, [cachep, I32, P, P, P, I32, P]),
         "kv_status": (ctypes.c_int, [cachep, U32P, P]),
         "kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -163,6 +165,17 @@ def kv_decode_attention(cache: kvq_cache, layer: int, q: torch.Tensor, out: torc
     _check(load().kv_decode_attention(ctypes.byref(cache), layer, _ptr(q), _ptr(out), _ptr(seq_lens),
                                       B, _ptr(scratch), scratch.numel() * scratch.element_size(),
                                       _stream(stream)))
+
+
+def kv_decode_attention_noalloc(cache: kvq_cache, layer: int, q: torch.Tensor, out: torch.Tensor,
+                                seq_lens: torch.Tensor, stream=None):
+    """Decode without a caller scratch buffer: the library's own fixed device array is used (for
+    callers that cannot allocate).  Same shapes as kv_decode_attention."""
+    if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
+        raise KVQError("seq_lens must be int32 and out float32")
+    B = q.shape[-3]
+    _check(load().kv_decode_attention_noalloc(ctypes.byref(cache), layer, _ptr(q), _ptr(out),
+                                              _ptr(seq_lens), B, _stream(stream)))
 
 
 def kv_status(cache: kvq_cache, stream=None) -> int:
