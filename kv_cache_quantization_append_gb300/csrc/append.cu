@@ -38,11 +38,21 @@ __device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, int kv,
   s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 15.0f));
   z16 = __float2half_rn(mn);
   const float s = __half2float(s16), z = __half2float(z16);
+  // code = clamp(rint(RN((y - z) / s)), 0, 15).  The quotient is first formed as (y - z) * RN(1/s),
+  // within a few ulp of the IEEE quotient (|q| < 2^5, so well under 2^-17 away); its rounding to an
+  // integer can differ from the IEEE quotient's only within that distance of a half-integer, and
+  // there the IEEE division is done instead, so the code equals the exact definition.
+  const float inv = __frcp_rn(s);
   uint32_t hw = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     int c = 0;
-    if (s > 0.0f) c = min(max(__float2int_rn(__fdiv_rn(__fsub_rn(y[e], z), s)), 0), 15);
+    if (s > 0.0f) {
+      const float num = __fsub_rn(y[e], z);
+      float qt = __fmul_rn(num, inv);
+      if (fabsf(qt - rintf(qt)) > 0.499f) qt = __fdiv_rn(num, s);
+      c = min(max(__float2int_rn(qt), 0), 15);
+    }
     hw |= (uint32_t)c << (4 * e);
   }
   // lane 8G + r holds channels 32G + 4r .. +3 as the halfword hw (byte 0: channels +0,+1; byte 1: +2,+3)
@@ -63,33 +73,12 @@ __device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, int kv,
   }
 }
 
-__global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
-  __shared__ uint32_t sbits[WARPS][12];
-  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  const long long total = (long long)a.n_layers_call * a.batch * a.Hkv * a.T * 2;
-  const long long wid = (long long)blockIdx.x * WARPS + wl;
-  if (wid >= total) return;
-  const int kv = (int)(wid & 1);
-  long long rest = wid >> 1;
-  const int t = (int)(rest % a.T);
-  rest /= a.T;
-  const int h = (int)(rest % a.Hkv);
-  rest /= a.Hkv;
-  const int b = (int)(rest % a.batch);
-  const int ll = (int)(rest / a.batch);
-  const int layer = a.layer0 + ll;
+constexpr int VPW = 4;  // vectors (consecutive tokens) per warp: their loads are issued together
+
+// encode one vector (lane holds channels 4*lane..+3 of the raw input) into its page and ring slot
+__device__ __forceinline__ void encode_vector(const AppendArgs& a, uint32_t (&sbits)[12], int lane, int kv,
+                                              int layer, int b, int h, int t, int p, float4 xin) {
   const int H = a.Hkv;
-
-  const int p0 = a.pos[b];
-  if (p0 < 0) return;  // sequence not part of this append
-  if ((long long)p0 + a.T > a.max_seq_len) {
-    if (lane == 0 && t == 0 && kv == 0 && h == 0) atomicOr(a.p.status, KVQ_DEV_POS_RANGE);
-    return;
-  }
-  const int p = p0 + t;
-  const size_t vec = (((size_t)ll * a.batch + b) * H + h) * a.T + t;
-  const float4 xin = load4_in(kv ? a.v : a.k, vec * D + 4 * lane, a.in_bf16);
-
   // raw copy into the window ring for the last `window` tokens of this call
   if (a.W > 0 && t >= a.T - a.W) {
     float* ring = kv ? a.p.ringv : a.p.ringk;
@@ -154,14 +143,14 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
 #pragma unroll
     for (int m = 1; m < 8; m <<= 1) word |= __shfl_xor_sync(FULL, word, m);
     // 3-bit codes: channel j at bits 3j..3j+2 of a 384-bit stream; lane holds bits 12*lane..+11
-    if (lane < 12) sbits[wl][lane] = 0u;
+    if (lane < 12) sbits[lane] = 0u;
     __syncwarp();
     const int bit = 12 * lane, w0 = bit >> 5, sh = bit & 31;
-    atomicOr(&sbits[wl][w0], c12 << sh);
-    if (sh > 20) atomicOr(&sbits[wl][w0 + 1], c12 >> (32 - sh));
+    atomicOr(&sbits[w0], c12 << sh);
+    if (sh > 20) atomicOr(&sbits[w0 + 1], c12 >> (32 - sh));
     __syncwarp();
     uint8_t* rec = pg + (size_t)tin * 48;
-    if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = sbits[wl][lane];
+    if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = sbits[lane];
     uint32_t* sgn = reinterpret_cast<uint32_t*>(pg + 48 * HALF + (size_t)tin * 16);
     if ((lane & 7) == 0) sgn[lane >> 3] = word;
     if (lane == 0) {
@@ -182,13 +171,13 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
   q4_encode(y, lane, kv, tin, pg + (kv ? a.L.off_vmain : 0), s16, z16);
   if (kv == 0) {
     // K meta: per token {scale[4], zero[4]} fp16
-    const uint32_t s0 = __shfl_sync(FULL, h16(s16), 0), s1 = __shfl_sync(FULL, h16(s16), 8);
-    const uint32_t s2 = __shfl_sync(FULL, h16(s16), 16), s3 = __shfl_sync(FULL, h16(s16), 24);
-    const uint32_t z0 = __shfl_sync(FULL, h16(z16), 0), z1 = __shfl_sync(FULL, h16(z16), 8);
-    const uint32_t z2 = __shfl_sync(FULL, h16(z16), 16), z3 = __shfl_sync(FULL, h16(z16), 24);
+    const uint32_t sz = h16(s16) | (h16(z16) << 16);
+    const uint32_t g0 = __shfl_sync(FULL, sz, 0), g1 = __shfl_sync(FULL, sz, 8);
+    const uint32_t g2 = __shfl_sync(FULL, sz, 16), g3 = __shfl_sync(FULL, sz, 24);
     if (lane == 0)
       *reinterpret_cast<uint4*>(pg + a.L.off_kmeta + (size_t)tin * 16) =
-          make_uint4(s0 | (s1 << 16), s2 | (s3 << 16), z0 | (z1 << 16), z2 | (z3 << 16));
+          make_uint4((g0 & 0xffffu) | (g1 << 16), (g2 & 0xffffu) | (g3 << 16), (g0 >> 16) | (g1 & 0xffff0000u),
+                     (g2 >> 16) | (g3 & 0xffff0000u));
   } else if ((lane & 7) == 0) {
     // V meta: group-major scale[4][32] then zero[4][32]
     __half* meta = reinterpret_cast<__half*>(pg + a.L.off_vmeta);
@@ -198,10 +187,45 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
   }
 }
 
+__global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
+  __shared__ uint32_t sbits[WARPS][12];
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  const int nq = (a.T + VPW - 1) / VPW;
+  const long long total = (long long)a.n_layers_call * a.batch * a.Hkv * nq * 2;
+  const long long wid = (long long)blockIdx.x * WARPS + wl;
+  if (wid >= total) return;
+  const int kv = (int)(wid & 1);
+  long long rest = wid >> 1;
+  const int tq = (int)(rest % nq);
+  rest /= nq;
+  const int h = (int)(rest % a.Hkv);
+  rest /= a.Hkv;
+  const int b = (int)(rest % a.batch);
+  const int ll = (int)(rest / a.batch);
+  const int layer = a.layer0 + ll;
+
+  const int p0 = a.pos[b];
+  if (p0 < 0) return;  // sequence not part of this append
+  if ((long long)p0 + a.T > a.max_seq_len) {
+    if (lane == 0 && tq == 0 && kv == 0 && h == 0) atomicOr(a.p.status, KVQ_DEV_POS_RANGE);
+    return;
+  }
+  const int t0 = tq * VPW;
+  const int nv = min(VPW, a.T - t0);
+  const size_t vec0 = (((size_t)ll * a.batch + b) * a.Hkv + h) * a.T + t0;
+  float4 x[VPW];
+#pragma unroll
+  for (int j = 0; j < VPW; ++j)
+    if (j < nv) x[j] = load4_in(kv ? a.v : a.k, (vec0 + j) * D + 4 * lane, a.in_bf16);
+#pragma unroll
+  for (int j = 0; j < VPW; ++j)
+    if (j < nv) encode_vector(a, sbits[wl], lane, kv, layer, b, h, t0 + j, p0 + t0 + j, x[j]);
+}
+
 }  // namespace
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s) {
-  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * a.T * 2;
+  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + VPW - 1) / VPW) * 2;
   const long long blocks = (warps + WARPS - 1) / WARPS;
   if (blocks <= 0) return cudaSuccess;
   if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;

@@ -19,7 +19,7 @@ namespace {
 constexpr int THREADS = 1024;
 constexpr int ITERS = 8;
 
-__global__ void __launch_bounds__(THREADS) calibrate_kernel(const CalibArgs a) {
+__global__ void __launch_bounds__(THREADS, 1) calibrate_kernel(const CalibArgs a) {
   __shared__ float sigma[D];
   __shared__ float kappa[D];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -46,7 +46,11 @@ struct Geo {
 #endif
   static constexpr int NCW = TQ ? 11 : KVQ_Q4_CONSUMER_WARPS;  // consumer warps
   static constexpr int NTHREADS = (NCW + 1) * 32;      // + 1 producer warp
-  static constexpr int NSTAGE = 2 * NCW;               // two stages per consumer warp
+#ifndef KVQ_Q4_SLOTS
+#define KVQ_Q4_SLOTS 3
+#endif
+  static constexpr int NSLOT = TQ ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
+  static constexpr int NSTAGE = NSLOT * NCW;
   static constexpr bool UNROLL_TILES = NCW <= 11;      // unrolled m-tiles need the larger budget
   static constexpr int SM_STAGES = 0;
   static constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
@@ -914,9 +918,10 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       const int n = (int)(xe - xs);
       Pos ps = locate(xs, K.S_layer, B, H, K.sq);
       int issued = 0;
+      constexpr int NS = GE::NSLOT;
       for (int k = 0; k < n; ++k) {
-        const int slot = w + NCW * (k & 1);
-        if (k >= 2 && !mbar_wait(empty + slot, ((k >> 1) - 1) & 1, a.p.status)) break;
+        const int slot = w + NCW * (k % NS);
+        if (k >= NS && !mbar_wait(empty + slot, ((k / NS) - 1) & 1, a.p.status)) break;
         const int u = (ps.ll * B + ps.b) * H + ps.h;
         const int layer = a.layer0 + ps.ll;
         const int L = sL[ps.b];
@@ -952,8 +957,8 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
         if (k + 1 < n) advance(ps, 1, B, H, K.sq);
       }
       // never leave the CTA with a copy still landing in shared memory
-      for (int k = max(0, issued - 2); k < issued; ++k)
-        mbar_wait(full + w + NCW * (k & 1), (k >> 1) & 1, a.p.status);
+      for (int k = max(0, issued - NS); k < issued; ++k)
+        mbar_wait(full + w + NCW * (k % NS), (k / NS) & 1, a.p.status);
     }
     return;
   }
@@ -969,10 +974,14 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   ws.ml = reinterpret_cast<float*>(smem + GE::SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
-  // step k uses slot warp + NCW*(k & 1), phase (k >> 1) of that slot
-  for (int k = 0; k < n; ++k) {
-    const int slot = K.warp + NCW * (k & 1);
-    if (!mbar_wait(full + slot, (k >> 1) & 1, a.p.status)) break;
+  // step k uses slot warp + NCW*(k mod NSLOT), phase k / NSLOT of that slot
+  for (int k = 0, j = 0, ph = 0; k < n; ++k) {
+    const int slot = K.warp + NCW * j;
+    if (!mbar_wait(full + slot, ph, a.p.status)) break;
+    if (++j == GE::NSLOT) {
+      j = 0;
+      ph ^= 1;
+    }
     const int4 d = desc[slot];
     if (d.x != cur) {
       if (cur >= 0) K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);

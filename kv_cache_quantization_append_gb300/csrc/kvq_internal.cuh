@@ -122,23 +122,20 @@ __device__ __forceinline__ void hadamard_warp(float& x0, float& x1, float& x2, f
   x2 = __fsub_rn(a0, a2);
   x1 = __fadd_rn(a1, a3);
   x3 = __fsub_rn(a1, a3);
+  // cross-lane stages: the lower lane of a pair gets a + b, the upper one a - b, both as one
+  // fma(mine, +-1, partner): the product by +-1 is exact, so the single rounding equals that of the
+  // plain add / subtract
 #pragma unroll
   for (int m = 1; m < 32; m <<= 1) {
+    const float sg = (lane & m) ? -1.0f : 1.0f;
     const float y0 = __shfl_xor_sync(FULL, x0, m);
     const float y1 = __shfl_xor_sync(FULL, x1, m);
     const float y2 = __shfl_xor_sync(FULL, x2, m);
     const float y3 = __shfl_xor_sync(FULL, x3, m);
-    if (lane & m) {
-      x0 = __fsub_rn(y0, x0);
-      x1 = __fsub_rn(y1, x1);
-      x2 = __fsub_rn(y2, x2);
-      x3 = __fsub_rn(y3, x3);
-    } else {
-      x0 = __fadd_rn(x0, y0);
-      x1 = __fadd_rn(x1, y1);
-      x2 = __fadd_rn(x2, y2);
-      x3 = __fadd_rn(x3, y3);
-    }
+    x0 = __fmaf_rn(x0, sg, y0);
+    x1 = __fmaf_rn(x1, sg, y1);
+    x2 = __fmaf_rn(x2, sg, y2);
+    x3 = __fmaf_rn(x3, sg, y3);
   }
 }
 
