@@ -317,7 +317,9 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   a.out = out;
   a.seq_lens = seq_lens;
   a.counters = static_cast<int*>(scratch);
-  a.records = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256((size_t)n_units * sizeof(int)));
+  // scratch: arrival counters [n_units], merge flags [n_units + warps], partial records
+  const size_t slots = (size_t)n_units + (size_t)ctas * decode_consumer_warps(cache->cfg.k_format);
+  a.records = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256(((size_t)n_units + slots) * sizeof(int)));
   a.layer0 = l0;
   a.n_layers_call = nl;
   a.batch = batch;

@@ -11,17 +11,19 @@
 //    of one (layer, sequence, kv-head) unit, window chunks first.
 //  * The list is cut into equal contiguous ranges, one per consumer warp of every CTA (stream-K
 //    at warp granularity), so every warp streams the same bytes whatever the sequence lengths and
-//    touches only one to a few units.  Consumer warp w owns two shared-memory stages (slots w and
-//    w + 11 of 22); lane w of the producer warp streams exactly that warp's range with
-//    cp.async.bulk (the 1D TMA path) completing on mbarriers.
-//  * Consumer warps dequantise nibbles to fp16 in registers (exponent-bias trick: OR a nibble into
-//    the mantissa of 1024.0, subtract exactly) and run the logits and P.V as tensor-core
+//    touches only one to a few units.  Consumer warp w owns NSLOT shared-memory stages (slots
+//    w + 11 k); lane w of the producer warp streams exactly that warp's range with cp.async.bulk
+//    (the 1D TMA path) completing on mbarriers.  Every wait gives up after ~1 s and sets a status
+//    bit.
+//  * Consumer warps turn nibbles into exact fp16 values in registers (a nibble read as an FP8 E4M3
+//    bit pattern is c * 2^-9; the 2^9 is folded into q) and run the logits and P.V as tensor-core
 //    mma.sync m16n8k16 (fp32 accumulate): GQA query heads are the N axis (hi and lo halves of q
 //    in adjacent columns), per-group scales and zero points are folded out of the products.
 //  * Each warp keeps an online-softmax state per unit and, when it leaves the unit, writes a
 //    partial record (max, sum, accumulator) to scratch and bumps the unit's arrival counter; the
-//    last arrival merges the records in a fixed order (deterministic), undoes the rotation of the
-//    quantised part and combines it with the window part.  No spin-wait on other CTAs.
+//    last arrival marks the unit, and after its streaming loop the warp merges the units it marked
+//    from their records in a fixed order (deterministic), undoes the rotation of the quantised
+//    part and combines it with the window part.  No spin-wait on other CTAs.
 #include <cfloat>
 
 #include "kvq_internal.cuh"
@@ -34,6 +36,7 @@ constexpr int STAGE_BYTES = 5120;            // max half-page (Q4/Q4) and window
 constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
+constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): 11 consumer warps + 1 producer warp
 // (12 warps keep the 168-register budget per thread); measured faster than 15 consumer warps at 128
@@ -51,7 +54,6 @@ struct Geo {
 #endif
   static constexpr int NSLOT = TQ ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
   static constexpr int NSTAGE = NSLOT * NCW;
-  static constexpr bool UNROLL_TILES = NCW <= 11;      // unrolled m-tiles need the larger budget
   static constexpr int SM_STAGES = 0;
   static constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
   static constexpr int SM_DESC = SM_BARS + 2 * NSTAGE * 8;
@@ -59,9 +61,8 @@ struct Geo {
   static constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;                 // [NCW][4][128] (TQ)
   static constexpr int SM_QSUM = SM_SQ + (TQ ? NCW * MAX_GQA * D * 4 : 0);   // [NCW][4][4] float
   static constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                      // [64][32] u32 (TQ)
-  static constexpr int SM_LG = SM_LUT + (TQ ? 64 * 32 * 4 : 0);              // [NCW][4][32] float
-  static constexpr int SM_P = SM_LG + NCW * MAX_GQA * HALF * 4;              // [NCW][4][32] fp16
-  static constexpr int SM_WML = SM_P + NCW * MAX_GQA * HALF * 2;             // [NCW][8] float
+  static constexpr int SM_P = SM_LUT + (TQ ? 64 * 32 * 4 : 0);               // [NCW][2][4][32] fp16
+  static constexpr int SM_WML = SM_P + NCW * 2 * MAX_GQA * HALF * 2;         // [NCW][8] float
   static constexpr int SM_SEQ = SM_WML + NCW * 8 * 4;                        // 3 int[batch+1]
 };
 
@@ -198,7 +199,7 @@ __device__ __forceinline__ void advance(Pos& p, int by, int B, int H, const Seq&
 struct QuantState {
   uint32_t qb[8][2];   // B fragments of q~ (K logits), hi/lo interleaved columns
   uint32_t sb[8][2];   // B fragments of S q~ (TQ sign dot)
-  float qsum[4];       // per-group sum of q~ for head (lane & 3)  (Q4 zero-point term)
+  uint32_t zb;         // B fragment of the per-group sums of q~ (Q4 zero-point term), hi/lo columns
   float acc[8][4];     // P.V accumulators, m-tile j (16 channels), C fragment
   float zacc[4];       // sum_t p_t z_{t,G}: rows = groups, cols = heads
   float m, l;          // running max / partial sum for head (lane & 3)
@@ -219,7 +220,7 @@ struct Kernel {
   using GE = Geo<KF>;
   static constexpr int NCW = GE::NCW;
   static constexpr int SM_Q = GE::SM_Q, SM_SQ = GE::SM_SQ, SM_QSUM = GE::SM_QSUM, SM_LUT = GE::SM_LUT;
-  static constexpr int SM_LG = GE::SM_LG, SM_P = GE::SM_P;
+  static constexpr int SM_P = GE::SM_P;
   const DecodeArgs& a;
   uint8_t* smem;
   int lane, warp;
@@ -238,15 +239,31 @@ struct Kernel {
   __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * nw - 1) / S); }
 
   // ---------------------------------------------------------------- unit set-up
-  __device__ void load_q(int u, QuantState& st, WinState& ws, int kind) {
+  // issue the loads of unit u's g query vectors (lane holds channels 4*lane..+3 of each)
+  __device__ __forceinline__ void fetch_q(int u, float4 (&raw)[MAX_GQA]) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-    const int layer = a.layer0 + ll;
     const size_t qbase = (((size_t)ll * B + b) * Hq + (size_t)h * g) * D;
+#pragma unroll
+    for (int hh = 0; hh < MAX_GQA; ++hh) {
+      raw[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hh < g) raw[hh] = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
+    }
+  }
+
+  __device__ void load_q(int u, QuantState& st, WinState& ws, int kind) {
+    float4 raw[MAX_GQA];
+    fetch_q(u, raw);
+    build_q(u, raw, st, ws, kind);
+  }
+
+  // set up the per-unit state of the window part (kind 0) or the quantised part (kind 1)
+  __device__ void build_q(int u, const float4 (&raw)[MAX_GQA], QuantState& st, WinState& ws, int kind) {
+    const int h = u % H, ll = u / (H * B);
+    const int layer = a.layer0 + ll;
     if (kind == KIND_WINDOW) {
 #pragma unroll
       for (int hh = 0; hh < MAX_GQA; ++hh) {
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (hh < g) x = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
+        const float4 x = raw[hh];
         *reinterpret_cast<float4*>(ws.q + hh * D + 4 * lane) =
             make_float4(x.x * LOGIT_SCALE, x.y * LOGIT_SCALE, x.z * LOGIT_SCALE, x.w * LOGIT_SCALE);
         *reinterpret_cast<float4*>(ws.acc + hh * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -261,14 +278,7 @@ struct Kernel {
     const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
 #pragma unroll
     for (int hh = 0; hh < MAX_GQA; ++hh) {
-      float y0 = 0.f, y1 = 0.f, y2 = 0.f, y3 = 0.f;
-      if (hh < g) {
-        const float4 x = load4_in(a.q, qbase + (size_t)hh * D + 4 * lane, a.in_bf16);
-        y0 = x.x * sg.x;
-        y1 = x.y * sg.y;
-        y2 = x.z * sg.z;
-        y3 = x.w * sg.w;
-      }
+      float y0 = raw[hh].x * sg.x, y1 = raw[hh].y * sg.y, y2 = raw[hh].z * sg.z, y3 = raw[hh].w * sg.w;
       hadamard_warp(y0, y1, y2, y3, lane);
       float sc[4] = {C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE, C_WHT * LOGIT_SCALE};
       if (a.sinkhorn) {
@@ -344,8 +354,9 @@ struct Kernel {
         st.sb[kk][1] = s2 | (s3 << 16);
       }
     }
-#pragma unroll
-    for (int G = 0; G < 4; ++G) st.qsum[G] = (i < g) ? qsum[i * 4 + G] : 0.f;
+    // zero-point term as one more k-step: k = group G (0..3), column = head (hi | lo)
+    st.zb = (hv && i < 2) ? split_pick(qsum[head * 4 + 2 * i], lo) | (split_pick(qsum[head * 4 + 2 * i + 1], lo) << 16)
+                          : 0u;
 #pragma unroll
     for (int j = 0; j < 8; ++j) st.acc[j][0] = st.acc[j][1] = st.acc[j][2] = st.acc[j][3] = 0.f;
     st.zacc[0] = st.zacc[1] = st.zacc[2] = st.zacc[3] = 0.f;
@@ -505,16 +516,18 @@ struct Kernel {
       }
       const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
       const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
+      // zero-point term sum_G z_G * sum(q~_G) on the tensor core: A row = token, k = group
+      // (this thread's k pair 2i, 2i+1 is zero (G0, G1) for i = 0, (G2, G3) for i = 1)
+      float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t zla = i == 0 ? ma.z : (i == 1 ? ma.w : 0u);
+      const uint32_t zlb = i == 0 ? mb.z : (i == 1 ? mb.w : 0u);
+      mma16816(zacc, zla, zlb, 0u, 0u, st.zb, 0u);
       const float2 sa01 = __half22float2(u2h(ma.x)), sa23 = __half22float2(u2h(ma.y));
-      const float2 za01 = __half22float2(u2h(ma.z)), za23 = __half22float2(u2h(ma.w));
       const float2 sb01 = __half22float2(u2h(mb.x)), sb23 = __half22float2(u2h(mb.y));
-      const float2 zb01 = __half22float2(u2h(mb.z)), zb23 = __half22float2(u2h(mb.w));
-      la = za01.x * st.qsum[0] + za01.y * st.qsum[1] + za23.x * st.qsum[2] + za23.y * st.qsum[3];
-      lb = zb01.x * st.qsum[0] + zb01.y * st.qsum[1] + zb23.x * st.qsum[2] + zb23.y * st.qsum[3];
-      la += sa01.x * (acc[0][0] + acc[0][1]) + sa01.y * (acc[1][0] + acc[1][1]) +
-            sa23.x * (acc[2][0] + acc[2][1]) + sa23.y * (acc[3][0] + acc[3][1]);
-      lb += sb01.x * (acc[0][2] + acc[0][3]) + sb01.y * (acc[1][2] + acc[1][3]) +
-            sb23.x * (acc[2][2] + acc[2][3]) + sb23.y * (acc[3][2] + acc[3][3]);
+      la = (zacc[0] + zacc[1]) + sa01.x * (acc[0][0] + acc[0][1]) + sa01.y * (acc[1][0] + acc[1][1]) +
+           sa23.x * (acc[2][0] + acc[2][1]) + sa23.y * (acc[3][0] + acc[3][1]);
+      lb = (zacc[2] + zacc[3]) + sb01.x * (acc[0][2] + acc[0][3]) + sb01.y * (acc[1][2] + acc[1][3]) +
+           sb23.x * (acc[2][2] + acc[2][3]) + sb23.y * (acc[3][2] + acc[3][3]);
     }
   }
 
@@ -538,7 +551,7 @@ struct Kernel {
   }
 
   __device__ __forceinline__ void logits_tile(const uint8_t* stage, int mt, int ntok, bool tail, float lmask,
-                                              float* lgs, const QuantState& st, float& mx) {
+                                              float (&lg)[4], const QuantState& st) {
     const int r = lane >> 2;
     float la, lb;
     tile_logits(stage, mt, st, la, lb);
@@ -550,92 +563,115 @@ struct Kernel {
     }
     la += ma;
     lb += mb;
-    lgs[ta] = la;
-    lgs[ta + 8] = lb;
-    mx = fmaxf(mx, fmaxf(la, lb));
+    lg[2 * mt] = la;      // token 16mt + r
+    lg[2 * mt + 1] = lb;  // token 16mt + r + 8
   }
 
-  __device__ __forceinline__ void pv_tile(const uint8_t* stage, int mt, bool colok, const __half* pcol,
-                                          QuantState& st) {
+  // P.V of the stage's 32 tokens (two 16-token k-steps).
+  // * B column n < 4 carries the high fp16 part of head n's weights and column n + 4 the low part,
+  //   so p (and p * scale) enter with ~22 significant bits: the code term and the zero-point term
+  //   see the same weights, and their large opposite contributions (zero ~ group minimum) cancel
+  //   without the fp16 rounding of p showing through.
+  // * The tensor-core accumulator is used only within the stage, starting from zero; the running
+  //   sums over the unit are kept with round-to-nearest fp32 adds.  A unit can span tens of
+  //   thousands of tokens, and the mma adder's own rounding must not build up a drift in those
+  //   large, mutually cancelling sums.
+  __device__ __forceinline__ void pv_stage(const uint8_t* stage, bool colok, bool lo, const __half* pcol,
+                                           QuantState& st) {
     const int r = lane >> 2, i = lane & 3;
     const uint8_t* vmain = stage + OFF_VMAIN;
     const __half* vscale = reinterpret_cast<const __half*>(stage + OFF_VMETA);
     const __half* vzero = vscale + 4 * HALF;
 
-    const int t0 = 16 * mt + 2 * i;
-    const uint32_t pA = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
-    const uint32_t pB = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
-    // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = unscaled p
-    uint32_t zA = 0u, zB = 0u;
-    if (r < 4) {
-      zA = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0);
-      zB = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0 + 8);
+    // p_hi = fp16(p) and p_lo = fp16(p - p_hi) of this lane's column head, tokens (t0, t0+1), (t0+8, t0+9)
+    uint32_t pA[2], pB[2], plA[2], plB[2];
+    uint4 vab[2], vcd[2];
+    float zt[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int t0 = 16 * mt + 2 * i;
+      pA[mt] = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
+      pB[mt] = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
+      plA[mt] = (colok && lo) ? *reinterpret_cast<const uint32_t*>(pcol + MAX_GQA * HALF + t0) : 0u;
+      plB[mt] = (colok && lo) ? *reinterpret_cast<const uint32_t*>(pcol + MAX_GQA * HALF + t0 + 8) : 0u;
+      // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = p_hi | p_lo
+      uint32_t zA = 0u, zB = 0u;
+      if (r < 4) {
+        zA = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0);
+        zB = *reinterpret_cast<const uint32_t*>(vzero + r * HALF + t0 + 8);
+      }
+      mma16816(zt, zA, 0u, zB, 0u, lo ? plA[mt] : pA[mt], lo ? plB[mt] : pB[mt]);
+      // V codes of tokens (t0, t0+1) and (t0+8, t0+9) for channel row r: one 16-byte block per
+      // token pair, word G = [t0 byte0, t1 byte0, t0 byte1, t1 byte1] of group G's channels 32G+4r..+3
+      const int p0 = 8 * mt + i;
+      const int blk = 16 * ((r + 2 * (p0 & 3)) & 7);
+      vab[mt] = *reinterpret_cast<const uint4*>(vmain + p0 * 128 + blk);
+      vcd[mt] = *reinterpret_cast<const uint4*>(vmain + (p0 + 4) * 128 + blk);
     }
-    mma16816(st.zacc, zA, 0u, zB, 0u, pA, pB);
-    // V codes of tokens (t0, t0+1) and (t0+8, t0+9) for channel row r: one 16-byte block per token
-    // pair, word G = [t0 byte0, t1 byte0, t0 byte1, t1 byte1] of group G's channels 32G+4r..+3
-    const int p0 = 8 * mt + i;
-    const int blk = 16 * ((r + 2 * (p0 & 3)) & 7);
-    const uint4 vab = *reinterpret_cast<const uint4*>(vmain + p0 * 128 + blk);
-    const uint4 vcd = *reinterpret_cast<const uint4*>(vmain + (p0 + 4) * 128 + blk);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.zacc[e] = __fadd_rn(st.zacc[e], zt[e]);
 #pragma unroll
     for (int G = 0; G < 4; ++G) {
-      // B operand for group G: p * scale (fp16)
-      const uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0);
-      const uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0 + 8);
-      const uint32_t bA = h2u(__hmul2(u2h(pA), u2h(sA)));
-      const uint32_t bB = h2u(__hmul2(u2h(pB), u2h(sB)));
-      const uint32_t wab = G == 0 ? vab.x : G == 1 ? vab.y : G == 2 ? vab.z : vab.w;
-      const uint32_t wcd = G == 0 ? vcd.x : G == 1 ? vcd.y : G == 2 ? vcd.z : vcd.w;
-      uint32_t x0, x2, x1, x3, y0, y2, y1, y3;
-      cvt8(wab, x0, x2, x1, x3);  // channel 32G + 4r + {0, 2, 1, 3}, tokens (t0, t0 + 1)
-      cvt8(wcd, y0, y2, y1, y3);  // same channels, tokens (t0 + 8, t0 + 9)
-      mma16816(st.acc[2 * G], x0, x1, y0, y1, bA, bB);
-      mma16816(st.acc[2 * G + 1], x2, x3, y2, y3, bA, bB);
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const int t0 = 16 * mt + 2 * i;
+        // B operand for group G: p * scale.  High column: fp16(p_hi s); low column:
+        // fp16(p_lo s + (p_hi s - fp16(p_hi s))), the inner residual being exact.  px = p_hi in
+        // low columns and 0 in high ones; p_lo = 0 in high ones.
+        const uint32_t sA = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0);
+        const uint32_t sB = *reinterpret_cast<const uint32_t*>(vscale + G * HALF + t0 + 8);
+        const uint32_t pxA = lo ? pA[mt] : 0u, pxB = lo ? pB[mt] : 0u;
+        const uint32_t bA = h2u(__hfma2(u2h(plA[mt]), u2h(sA),
+                                        __hfma2(u2h(pA[mt]), u2h(sA), __hneg2(__hmul2(u2h(pxA), u2h(sA))))));
+        const uint32_t bB = h2u(__hfma2(u2h(plB[mt]), u2h(sB),
+                                        __hfma2(u2h(pB[mt]), u2h(sB), __hneg2(__hmul2(u2h(pxB), u2h(sB))))));
+        const uint4 va = vab[mt], vc = vcd[mt];
+        const uint32_t wab = G == 0 ? va.x : G == 1 ? va.y : G == 2 ? va.z : va.w;
+        const uint32_t wcd = G == 0 ? vc.x : G == 1 ? vc.y : G == 2 ? vc.z : vc.w;
+        uint32_t x0, x2, x1, x3, y0, y2, y1, y3;
+        cvt8(wab, x0, x2, x1, x3);  // channel 32G + 4r + {0, 2, 1, 3}, tokens (t0, t0 + 1)
+        cvt8(wcd, y0, y2, y1, y3);  // same channels, tokens (t0 + 8, t0 + 9)
+        mma16816(c0, x0, x1, y0, y1, bA, bB);
+        mma16816(c1, x2, x3, y2, y3, bA, bB);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        st.acc[2 * G][e] = __fadd_rn(st.acc[2 * G][e], c0[e]);
+        st.acc[2 * G + 1][e] = __fadd_rn(st.acc[2 * G + 1][e], c1[e]);
+      }
     }
   }
 
   __device__ void quant_step(uint8_t* stage, int ntok, QuantState& st) {
     const int r = lane >> 2, i = lane & 3;
-    const uint8_t* vmain = stage + OFF_VMAIN;
-    const __half* vscale = reinterpret_cast<const __half*>(stage + OFF_VMETA);
-    const __half* vzero = vscale + 4 * HALF;
-    float* lgs = reinterpret_cast<float*>(smem + SM_LG) + warp * MAX_GQA * HALF + i * HALF;
-    __half* pw = reinterpret_cast<__half*>(smem + SM_P) + warp * MAX_GQA * HALF;
+    __half* pw = reinterpret_cast<__half*>(smem + SM_P) + warp * 2 * MAX_GQA * HALF;
     const float lmask = (i < g) ? 0.f : -INFINITY;  // column pair of a missing head: never attended
     const bool tail = ntok < HALF;
     if (tail) sanitize_tail(stage, ntok);
 
     // ---- logits of the 32 tokens (two 16-token m-tiles)
-    float mx = -INFINITY;
-    if (GE::UNROLL_TILES) {
+    float lg[4];  // head i, tokens r, r + 8, r + 16, r + 24
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) logits_tile(stage, mt, ntok, tail, lmask, lgs, st, mx);
-    } else {
-#pragma unroll 1
-      for (int mt = 0; mt < 2; ++mt) logits_tile(stage, mt, ntok, tail, lmask, lgs, st, mx);
-    }
+    for (int mt = 0; mt < 2; ++mt) logits_tile(stage, mt, ntok, tail, lmask, lg, st);
 
-    // ---- online softmax update for head i (rows r = 0..7 share it); 2^(-inf - m) = 0 handles
-    // masked tokens, a finite reference max handles a head with nothing valid yet
-    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
-    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
-    const float mnew = fmaxf(st.m, mx);
-    const float mref = (mnew == -INFINITY) ? 0.f : mnew;
-    const float alpha = (mnew == -INFINITY) ? 1.f : ex2(st.m - mnew);
-    st.m = mnew;
-    float psum = 0.f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int t = 8 * k + r;  // tokens r, r+8, r+16, r+24
-      const float pv = ex2(lgs[t] - mref);
-      psum += pv;
-      pw[i * HALF + t] = __float2half_rn(pv);
-    }
-    st.l = st.l * alpha + psum;
-    if (__any_sync(FULL, alpha != 1.f)) {
-      // accumulator columns 2i, 2i+1 are heads 2i, 2i+1: their alpha lives in lanes (r, 2i), (r, 2i+1)
+    // ---- online softmax for head i (rows r = 0..7 share it) with a lazily raised reference: the
+    // weights are p = 2^(l - m) for the warp's reference m, which is raised (and the accumulators
+    // rescaled) only when a logit exceeds it by more than 2^4; otherwise p <= 16 and no cross-lane
+    // max is needed.  Any reference gives the same acc / l; 2^(-inf - m) = 0 handles masked tokens,
+    // and a head with nothing valid yet keeps m = -inf (reference 0).
+    const float lmax = fmaxf(fmaxf(lg[0], lg[1]), fmaxf(lg[2], lg[3]));
+    if (__any_sync(FULL, lmax > st.m + LAZY_RAISE)) {
+      float mx = lmax;
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 16));
+      const float mnew = fmaxf(st.m, mx);
+      const float alpha = (mnew == -INFINITY) ? 1.f : ex2(st.m - mnew);
+      st.m = mnew;
+      st.l *= alpha;
+      // accumulator columns 2i, 2i+1 are heads (2i) & 3, (2i+1) & 3: their alpha lives in lanes
+      // (r, (2i) & 3), (r, (2i+1) & 3)
       const float al0 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i) & 3));
       const float al1 = __shfl_sync(FULL, alpha, (lane & ~3) | ((2 * i + 1) & 3));
 #pragma unroll
@@ -650,18 +686,25 @@ struct Kernel {
       st.zacc[2] *= al0;
       st.zacc[3] *= al1;
     }
+    const float mref = (st.m == -INFINITY) ? 0.f : st.m;
+    float psum = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = 8 * k + r;  // tokens r, r+8, r+16, r+24
+      const float pv = ex2(lg[k] - mref);
+      psum += pv;
+      const __half ph = __float2half_rn(pv);
+      pw[i * HALF + t] = ph;
+      pw[MAX_GQA * HALF + i * HALF + t] = __float2half_rn(pv - __half2float(ph));
+    }
+    st.l += psum;
     __syncwarp();
 
-    // ---- P.V: k-step = 16 tokens; this thread's B column is head r (r < g), tokens t0, t0+1, +8, +9
-    const bool colok = r < g;
+    // ---- P.V: k-step = 16 tokens; this thread's B column is head r & 3 (high part for r < 4, low part
+    // for r >= 4), tokens t0, t0+1, +8, +9
+    const bool colok = (r & 3) < g, lo = r >= 4;
     const __half* pcol = pw + (r & 3) * HALF;
-    if (GE::UNROLL_TILES) {
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) pv_tile(stage, mt, colok, pcol, st);
-    } else {
-#pragma unroll 1
-      for (int mt = 0; mt < 2; ++mt) pv_tile(stage, mt, colok, pcol, st);
-    }
+    pv_stage(stage, colok, lo, pcol, st);
     __syncwarp();
   }
 
@@ -688,6 +731,11 @@ struct Kernel {
         st.acc[2 * G + e][3] = st.acc[2 * G + e][3] * CODE_UNSCALE + z1;
       }
     }
+    // add the low-part columns 4..7 (lanes i = 2, 3) to the high-part columns 0..3 (lanes i = 0, 1)
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) st.acc[j][e] += __shfl_xor_sync(FULL, st.acc[j][e], 2);
     float l = st.l;
     l += __shfl_xor_sync(FULL, l, 4);
     l += __shfl_xor_sync(FULL, l, 8);
@@ -728,97 +776,168 @@ struct Kernel {
     if (lane < 16) rec[lane] = v;
   }
 
-  __device__ void merge(int u) {
+  // Combine the unit's partial records (one per warp that streamed part of it) in record order.
+  // Latency-bound, so the round trips are few: per part (quantised, window) lane j reads record j's
+  // header (32 records at a time, with running maxima across chunks), weights are reduced in
+  // registers, and the accumulators of eight records (all heads) are requested together.  Runs
+  // after the warp's streaming loop, with the whole register budget.
+  __device__ __noinline__ void merge(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const int layer = a.layer0 + ll;
     const long long sb = steps_before(ll, b, h);
-    const int cf = owner(sb), cl = owner(sb + sq.S[b] - 1);
-    for (int hh = 0; hh < g; ++hh) {
-      float part[2][4];
-      float Mx[2], Lx[2];
+    const int cf = owner(sb), nrec = owner(sb + sq.S[b] - 1) - cf + 1;
+    float outp[2][MAX_GQA][4], Mk[2][MAX_GQA], Lk[2][MAX_GQA];
 #pragma unroll
-      for (int kind = 0; kind < 2; ++kind) {  // 0 = quantised (rotated space), 1 = window
-        const int mo = kind ? 8 : 0, lo = kind ? 12 : 4;
-        const int ao = 16 + (kind ? MAX_GQA * D : 0) + hh * D + 4 * lane;
-        float M = -INFINITY;
-        for (int gw = cf; gw <= cl; ++gw) {
-          const float* rec = record(u, gw);
-          if (__ldcg(rec + lo + hh) > 0.f) M = fmaxf(M, __ldcg(rec + mo + hh));
-        }
-        float L = 0.f;
-        float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int gw = cf; gw <= cl; ++gw) {
-            const float* rec = record(u, gw);
-            const float l = __ldcg(rec + lo + hh);
-            if (l > 0.f) {
-              const float f = exp2f(__ldcg(rec + mo + hh) - M);
-              const float4 x = __ldcg(reinterpret_cast<const float4*>(rec + ao));
-              L += l * f;
-              A.x += f * x.x;
-              A.y += f * x.y;
-              A.z += f * x.z;
-              A.w += f * x.w;
-            }
-          }
-        Mx[kind] = M;
-        Lx[kind] = L;
-        part[kind][0] = A.x;
-        part[kind][1] = A.y;
-        part[kind][2] = A.z;
-        part[kind][3] = A.w;
+    for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
+      float M[MAX_GQA], L[MAX_GQA];
+      float4 A[MAX_GQA];
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh) {
+        M[hh] = -INFINITY;
+        L[hh] = 0.f;
+        A[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (Lx[0] > 0.f) {
+      for (int base = 0; base < nrec; base += 32) {
+        float4 hm = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), hl = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (base + lane < nrec) {
+          const float4* hp = reinterpret_cast<const float4*>(record(u, cf + base + lane)) + 2 * k;
+          hm = __ldcg(hp);
+          hl = __ldcg(hp + 1);
+        }
+        const float mv[4] = {hm.x, hm.y, hm.z, hm.w}, lv[4] = {hl.x, hl.y, hl.z, hl.w};
+        float f[MAX_GQA];
+#pragma unroll
+        for (int hh = 0; hh < MAX_GQA; ++hh) {
+          float m = lv[hh] > 0.f ? mv[hh] : -INFINITY;
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+          const float mn = fmaxf(M[hh], m);
+          const float sc = (M[hh] == -INFINITY) ? 0.f : exp2f(M[hh] - mn);  // rescale earlier chunks
+          L[hh] *= sc;
+          A[hh].x *= sc;
+          A[hh].y *= sc;
+          A[hh].z *= sc;
+          A[hh].w *= sc;
+          M[hh] = mn;
+          f[hh] = lv[hh] > 0.f ? exp2f(mv[hh] - mn) : 0.f;
+          float lw = lv[hh] * f[hh];
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
+          L[hh] += lw;
+        }
+        const int cnt = min(32, nrec - base);
+        for (int jj = 0; jj < cnt; jj += 8) {
+          // eight records' accumulators (all heads) requested before any is used
+          float4 x[8][MAX_GQA];
+#pragma unroll
+          for (int r8 = 0; r8 < 8; ++r8) {
+            const float* rec = record(u, cf + base + min(jj + r8, cnt - 1)) + 16 + k * MAX_GQA * D + 4 * lane;
+#pragma unroll
+            for (int hh = 0; hh < MAX_GQA; ++hh)
+              x[r8][hh] = (hh < g && jj + r8 < cnt) ? __ldcg(reinterpret_cast<const float4*>(rec + hh * D))
+                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int r8 = 0; r8 < 8; ++r8)
+#pragma unroll
+            for (int hh = 0; hh < MAX_GQA; ++hh) {
+              const float fj = __shfl_sync(FULL, f[hh], (jj + r8) & 31);
+              if (jj + r8 < cnt && fj > 0.f) {  // a part with no tokens holds no accumulator
+                A[hh].x += fj * x[r8][hh].x;
+                A[hh].y += fj * x[r8][hh].y;
+                A[hh].z += fj * x[r8][hh].z;
+                A[hh].w += fj * x[r8][hh].w;
+              }
+            }
+        }
+      }
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh) {
+        Mk[k][hh] = M[hh];
+        Lk[k][hh] = L[hh];
+        outp[k][hh][0] = A[hh].x;
+        outp[k][hh][1] = A[hh].y;
+        outp[k][hh][2] = A[hh].z;
+        outp[k][hh][3] = A[hh].w;
+      }
+    }
+#pragma unroll
+    for (int hh = 0; hh < MAX_GQA; ++hh) {
+      if (hh >= g) break;
+      float q0 = outp[0][hh][0], q1 = outp[0][hh][1], q2 = outp[0][hh][2], q3 = outp[0][hh][3];
+      const bool hq = Lk[0][hh] > 0.f, hw = Lk[1][hh] > 0.f;
+      if (hq) {
         // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
         if (a.sinkhorn) {
           const __half* sig = a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) part[0][e] *= __half2float(sig[e]);
+          q0 *= __half2float(sig[0]);
+          q1 *= __half2float(sig[1]);
+          q2 *= __half2float(sig[2]);
+          q3 *= __half2float(sig[3]);
         }
-        hadamard_warp(part[0][0], part[0][1], part[0][2], part[0][3], lane);
+        hadamard_warp(q0, q1, q2, q3, lane);
         const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
-        part[0][0] *= C_WHT * sg.x;
-        part[0][1] *= C_WHT * sg.y;
-        part[0][2] *= C_WHT * sg.z;
-        part[0][3] *= C_WHT * sg.w;
+        q0 *= C_WHT * sg.x;
+        q1 *= C_WHT * sg.y;
+        q2 *= C_WHT * sg.z;
+        q3 *= C_WHT * sg.w;
       }
-      const float M = fmaxf(Lx[0] > 0.f ? Mx[0] : -INFINITY, Lx[1] > 0.f ? Mx[1] : -INFINITY);
-      const float f0 = Lx[0] > 0.f ? exp2f(Mx[0] - M) : 0.f;
-      const float f1 = Lx[1] > 0.f ? exp2f(Mx[1] - M) : 0.f;
-      const float den = Lx[0] * f0 + Lx[1] * f1;
+      const float Mt = fmaxf(hq ? Mk[0][hh] : -INFINITY, hw ? Mk[1][hh] : -INFINITY);
+      const float f0 = hq ? exp2f(Mk[0][hh] - Mt) : 0.f;
+      const float f1 = hw ? exp2f(Mk[1][hh] - Mt) : 0.f;
+      const float den = Lk[0][hh] * f0 + Lk[1][hh] * f1;
       const float inv = den > 0.f ? 1.f / den : 0.f;
       float4 o;
-      o.x = (part[0][0] * f0 + part[1][0] * f1) * inv;
-      o.y = (part[0][1] * f0 + part[1][1] * f1) * inv;
-      o.z = (part[0][2] * f0 + part[1][2] * f1) * inv;
-      o.w = (part[0][3] * f0 + part[1][3] * f1) * inv;
+      o.x = (q0 * f0 + outp[1][hh][0] * f1) * inv;
+      o.y = (q1 * f0 + outp[1][hh][1] * f1) * inv;
+      o.z = (q2 * f0 + outp[1][hh][2] * f1) * inv;
+      o.w = (q3 * f0 + outp[1][hh][3] * f1) * inv;
       *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * Hq + (size_t)h * g + hh) * D + 4 * lane) = o;
     }
+    if (lane == 0) a.counters[u] = 0;  // ready for the next call
   }
 
-  // publish this warp's record for unit u and merge if it was the last one
-  __device__ void arrive(int u) {
+  // publish this warp's record for unit u; true if it was the unit's last arrival (which merges)
+  __device__ bool arrive(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const long long sb = steps_before(ll, b, h);
     const int nwu = owner(sb + sq.S[b] - 1) - owner(sb) + 1;
+    // every lane makes its own record writes visible device-wide, then one lane counts the arrival
+    // (acquire-release: the last arrival then sees the other warps' records)
+    __threadfence();
     __syncwarp();
     int old = 0;
-    if (lane == 0) {
-      __threadfence();
-      old = atomicAdd(a.counters + u, 1);
-    }
+    if (lane == 0)
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
     old = __shfl_sync(FULL, old, 0);
     if (old == nwu - 1) {
       __threadfence();
-      merge(u);
-      if (lane == 0) a.counters[u] = 0;
+      return true;
     }
+    return false;
   }
 
+  // write this warp's record of unit u; if it was the last one, flag the unit for this warp to
+  // merge after its streaming loop (keeping the merge code out of the loop)
   __device__ void finish_unit(int u, int gw, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
     float* rec = record(u, gw);
     if (kind == KIND_QUANT) write_quant(rec, st);
     write_header(rec, hasq, st, hasw, ws);
-    arrive(u);
+    if (arrive(u) && lane == 0) a.counters[a.n_units + u + gw] = 1;
+  }
+
+  // merge the units of steps [xs, xe) that this warp flagged
+  __device__ __noinline__ void run_merges(int gw, long long xs, long long xe) {
+    const Pos pf = locate(xs, S_layer, B, H, sq);
+    const Pos pl = locate(xe - 1, S_layer, B, H, sq);
+    const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
+    for (int u = uf; u <= ul; ++u) {
+      int* flag = a.counters + a.n_units + u + gw;
+      if (__ldcg(flag) != 0) {
+        merge(u);
+        if (lane == 0) *flag = 0;
+      }
+    }
   }
 
 };
@@ -974,6 +1093,21 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   ws.ml = reinterpret_cast<float*>(smem + GE::SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
+  {
+    // set up the first unit while the pipeline fills
+    const Pos p0 = locate(gw * K.S / K.nw, K.S_layer, B, H, K.sq);
+    const int L0 = sL[p0.b];
+    const int nwin0 = W > 0 ? (min(L0, W) + WCHUNK - 1) / WCHUNK : 0;
+    cur = (p0.ll * B + p0.b) * H + p0.h;
+    kind = p0.local < nwin0 ? KIND_WINDOW : KIND_QUANT;
+    if (kind == KIND_WINDOW) {
+      ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
+      hasw = true;
+    } else {
+      hasq = true;
+    }
+    K.load_q(cur, st, ws, kind);
+  }
   // step k uses slot warp + NCW*(k mod NSLOT), phase k / NSLOT of that slot
   for (int k = 0, j = 0, ph = 0; k < n; ++k) {
     const int slot = K.warp + NCW * j;
@@ -984,13 +1118,16 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     }
     const int4 d = desc[slot];
     if (d.x != cur) {
-      if (cur >= 0) K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
+      float4 raw[MAX_GQA];
+      K.fetch_q(d.x, raw);  // in flight while the previous unit's record is published
+      K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
       cur = d.x;
-      kind = -1;
-      hasq = hasw = false;
-    }
-    if (d.y != kind) {
-      if (d.y == KIND_WINDOW) ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
+      kind = d.y;
+      hasq = kind == KIND_QUANT;
+      hasw = kind == KIND_WINDOW;
+      if (kind == KIND_WINDOW) ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
+      K.build_q(cur, raw, st, ws, kind);
+    } else if (d.y != kind) {
       K.load_q(cur, st, ws, d.y);
       kind = d.y;
       if (kind == KIND_WINDOW) hasw = true;
@@ -1004,14 +1141,21 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     __syncwarp();
     if (K.lane == 0) mbar_arrive(empty + slot);
   }
-  if (cur >= 0) K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
+  K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
+  K.run_merges((int)gw, gw * K.S / K.nw, (gw + 1) * K.S / K.nw);
 }
 
 }  // namespace
 
+int decode_consumer_warps(int k_format) {
+  return k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
+}
+
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
   const int ncw = k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
-  return align256((size_t)n_units * sizeof(int)) + (size_t)(n_units + (size_t)n_ctas * ncw) * REC_FLOATS * sizeof(float);
+  // arrival counters [n_units], merge flags [n_units + warps], then the partial records
+  const size_t slots = (size_t)n_units + (size_t)n_ctas * ncw;
+  return align256(((size_t)n_units + slots) * sizeof(int)) + slots * REC_FLOATS * sizeof(float);
 }
 
 template <int KF>

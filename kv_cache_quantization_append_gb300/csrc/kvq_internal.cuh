@@ -70,8 +70,10 @@ struct AppendArgs {
   const void* v;
   const int32_t* pos;
   int layer0, n_layers_call, batch, max_batch, T, Hkv, W, max_seq_len, k_format, sinkhorn, in_bf16;
+  int kv_lo, kv_n;  // vectors handled by one launch: K (0) and/or V (1), kv_lo .. kv_lo + kv_n - 1
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
+cudaError_t launch_append_bulk(const AppendArgs& a, cudaStream_t s);
 
 struct CalibArgs {
   DevPtrs p;
@@ -96,6 +98,7 @@ struct DecodeArgs {
 };
 int decode_ctas(int device);
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format);
+int decode_consumer_warps(int k_format);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---------------------------------------------------------------- device helpers

@@ -48,10 +48,13 @@ int decode_attention_noalloc(kvq_cache* cache, int32_t layer, const void* q, flo
   void* scratch = nullptr;
   const int rc = scratch_address(dev, &scratch);
   if (rc != KVQ_OK) return rc;
-  // The arrival counters at the start of the scratch must be zero when the kernel starts; the
-  // array keeps whatever the previous call left, so clear them on the call's stream first.
+  // The arrival counters and merge flags at the start of the scratch must be zero when the kernel
+  // starts; the array keeps whatever the previous call left, so clear them on the call's stream.
   const int nl = layer == -1 ? cache->cfg.n_layers : 1;
-  const size_t counters = (size_t)nl * batch * cache->cfg.n_kv_heads * sizeof(int);
+  const size_t n_units = (size_t)nl * batch * cache->cfg.n_kv_heads;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  const size_t counters = (2 * n_units + (size_t)sms * decode_consumer_warps(cache->cfg.k_format)) * sizeof(int);
   if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
   return kv_decode_attention(cache, layer, q, out, seq_lens, batch, scratch, NOALLOC_SCRATCH_BYTES, stream);
 }

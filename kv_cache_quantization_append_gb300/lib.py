@@ -106,6 +106,14 @@ def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _check_in_dtype(cache: kvq_cache, *tensors: torch.Tensor):
+    """k, v, q and calibration blocks must have the cache's input dtype (cfg.in_dtype)."""
+    want = torch.bfloat16 if cache.cfg.in_dtype == KVQ_IN_BF16 else torch.float32
+    for t in tensors:
+        if t.dtype != want:
+            raise KVQError(f"input dtype {t.dtype} does not match the cache's in_dtype ({want})")
+
+
 def make_config(n_layers, n_kv_heads, n_q_heads, max_batch, max_seq_len, window=128, n_pages=0,
                 k_format=KVQ_Q4G32, v_format=KVQ_Q4G32, sinkhorn=False, in_dtype=KVQ_IN_BF16,
                 seed=0) -> kvq_config:
@@ -136,6 +144,7 @@ def kv_calibrate_scratch_bytes(cache: kvq_cache, layer: int, n_tokens: int) -> i
 
 def kv_calibrate(cache: kvq_cache, layer: int, k_calib: torch.Tensor, v_calib: torch.Tensor,
                  scratch: torch.Tensor, stream=None):
+    _check_in_dtype(cache, k_calib, v_calib)
     n_tokens = k_calib.shape[-2]
     _check(load().kv_calibrate(ctypes.byref(cache), layer, _ptr(k_calib), _ptr(v_calib), n_tokens,
                                _ptr(scratch), scratch.numel() * scratch.element_size(),
@@ -147,6 +156,7 @@ def kv_quant_append(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch.Tens
     """k, v: [L?][B][Hkv][T][128]; pos: int32 [B] on the device."""
     if pos.dtype != torch.int32:
         raise KVQError("pos must be int32")
+    _check_in_dtype(cache, k, v)
     B, T = k.shape[-4], k.shape[-2]
     _check(load().kv_quant_append(ctypes.byref(cache), layer, _ptr(k), _ptr(v), _ptr(pos), B, T,
                                   _stream(stream)))
@@ -161,6 +171,7 @@ def kv_decode_attention(cache: kvq_cache, layer: int, q: torch.Tensor, out: torc
     """q: [L?][B][Hq][128]; out: float32 like q; seq_lens: int32 [B]; scratch: zeroed bytes."""
     if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
         raise KVQError("seq_lens must be int32 and out float32")
+    _check_in_dtype(cache, q)
     B = q.shape[-3]
     _check(load().kv_decode_attention(ctypes.byref(cache), layer, _ptr(q), _ptr(out), _ptr(seq_lens),
                                       B, _ptr(scratch), scratch.numel() * scratch.element_size(),
@@ -173,6 +184,7 @@ def kv_decode_attention_noalloc(cache: kvq_cache, layer: int, q: torch.Tensor, o
     callers that cannot allocate).  Same shapes as kv_decode_attention."""
     if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
         raise KVQError("seq_lens must be int32 and out float32")
+    _check_in_dtype(cache, q)
     B = q.shape[-3]
     _check(load().kv_decode_attention_noalloc(ctypes.byref(cache), layer, _ptr(q), _ptr(out),
                                               _ptr(seq_lens), B, _stream(stream)))

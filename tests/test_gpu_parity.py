@@ -15,8 +15,8 @@ from . import harness, layout
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(w, layer, B, H, Hq, T, t0=0):
-    k, v = synth.kv_tokens(w, layer, B, H, t0, T, device="cuda")
+def _inputs(w, layer, B, H, Hq, T, t0=0, dtype=None):
+    k, v = synth.kv_tokens(w, layer, B, H, t0, T, device="cuda", dtype=dtype)
     return k, v
 
 
@@ -224,3 +224,60 @@ def test_out_of_range_append_is_flagged_and_skipped(gpu_lib):
     assert gpu.status() == 2                        # KVQ_DEV_POS_RANGE
     assert torch.equal(before, gpu.buffer)
     assert gpu.status() == 0                        # read-and-clear
+
+
+@pytest.mark.parametrize("variant", ["bf16", "f32", "sinkhorn", "tq3_keys", "paged"])
+def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
+    """Appends of 1..257 tokens starting at odd, even, half-page and page offsets, with sequences
+    skipped (pos = -1) in some calls: every stored field of every written position and the window
+    ring bit-exact with the oracle (covers both append kernels and the split between them)."""
+    w = synth.WORKLOADS["qwen3-4b-kvarn-128k" if variant == "sinkhorn" else "llama3.2-3b-32k"]
+    B, H, Hq, cap, W = 4, 2, 4, 1024, 64
+    starts = np.array([0, 1, 31, 63], np.int32)
+    chunks = [16, 1, 17, 31, 5, 32, 33, 100, 15, 257]
+    bt, n_pages = None, 0
+    if variant == "paged":
+        maxpps = cap // 64
+        n_pages = B * maxpps + 5
+        perm = np.random.default_rng(5).permutation(n_pages)
+        bt = perm[:B * maxpps].reshape(B, maxpps).astype(np.int32)
+    gpu, ora, _ = harness.make_pair(1, H, Hq, B, cap, window=W, in_dtype="f32" if variant == "f32" else "bf16",
+                                    sinkhorn=variant == "sinkhorn",
+                                    k_format="tq3_qjl" if variant == "tq3_keys" else "q4g32",
+                                    n_pages=n_pages, block_table=bt)
+    if variant == "sinkhorn":
+        kc, vc = _inputs(w, 0, 1, H, Hq, 256, t0=4096)
+        gpu.calibrate(0, kc[0].contiguous(), vc[0].contiguous())
+        ora.calibrate(0, harness.to_np(kc[0]), harness.to_np(vc[0]))
+    pos = starts.copy()
+    last_T = np.zeros(B, np.int64)
+    t_in = 0
+    for i, T in enumerate(chunks):
+        k, v = _inputs(w, 0, B, H, Hq, T, t0=t_in, dtype=torch.float32 if variant == "f32" else None)
+        t_in += T
+        p = pos.copy()
+        if i % 3 == 1:
+            p[(i // 3) % B] = -1
+        gpu.append(0, k, v, torch.as_tensor(p, device="cuda"))
+        ora.append(0, harness.to_np(k), harness.to_np(v), p)
+        live = p >= 0
+        pos[live] += T
+        last_T[live] = T
+    torch.cuda.synchronize()
+    assert gpu.status() == 0
+    names = (("k_code", "code"), ("k_bits", "bits"), ("k_norm", "norm"), ("k_gamma", "gamma")) \
+        if variant == "tq3_keys" else (("k_code", "code"), ("k_scale", "scale"), ("k_zero", "zero"))
+    for b in range(B):
+        s0, s1 = int(starts[b]), int(pos[b])
+        for h in range(H):
+            got = layout.read_unit(gpu.buffer, gpu.cfg, 0, b, h, s1, bt)
+            for gname, oname in names:
+                assert np.array_equal(got[gname][s0:s1].view(np.uint8),
+                                      ora.k[oname][0, b, h, s0:s1].view(np.uint8)), (gname, b, h)
+            for oname in ("code", "scale", "zero"):
+                assert np.array_equal(got["v_" + oname][s0:s1].view(np.uint8),
+                                      ora.v[oname][0, b, h, s0:s1].view(np.uint8)), ("v_" + oname, b, h)
+            rk, rv = layout.read_ring(gpu.buffer, gpu.cfg, 0, b, h)
+            slots = np.arange(s1 - min(W, int(last_T[b])), s1) % W
+            assert np.array_equal(rk[slots].view(np.uint32), ora.ring_k[0, b, h, slots].view(np.uint32))
+            assert np.array_equal(rv[slots].view(np.uint32), ora.ring_v[0, b, h, slots].view(np.uint32))
