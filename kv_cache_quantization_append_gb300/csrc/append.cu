@@ -191,11 +191,12 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
   __shared__ uint32_t sbits[WARPS][12];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int nq = (a.T + VPW - 1) / VPW;
-  const long long total = (long long)a.n_layers_call * a.batch * a.Hkv * nq * a.kv_n;
-  const long long wid = (long long)blockIdx.x * WARPS + wl;
+  // 32-bit index arithmetic: the launcher keeps the warp count below 2^31
+  const unsigned total = (unsigned)a.n_layers_call * a.batch * a.Hkv * nq * a.kv_n;
+  const unsigned wid = blockIdx.x * WARPS + wl;
   if (wid >= total) return;
   const int kv = a.kv_lo + (int)(wid % a.kv_n);
-  long long rest = wid / a.kv_n;
+  unsigned rest = wid / a.kv_n;
   const int tq = (int)(rest % nq);
   rest /= nq;
   const int h = (int)(rest % a.Hkv);
@@ -228,19 +229,20 @@ cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s) {
   const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + VPW - 1) / VPW) * a.kv_n;
   const long long blocks = (warps + WARPS - 1) / WARPS;
   if (blocks <= 0) return cudaSuccess;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+  if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
   append_kernel<<<(unsigned)blocks, WARPS * 32, 0, s>>>(a);
   return cudaGetLastError();
 }
 
-// Appends of at least BULK_MIN_T tokens per sequence go to the thread-per-token kernel
+// Appends of at least BULK_MIN_T tokens per sequence go to the four-lanes-per-token kernel
 // (append_bulk.cu) for Q4G32 vectors; shorter ones, and TurboQuant keys, to the warp-per-vector
 // kernel above.  Both write identical bytes.
 constexpr int BULK_MIN_T = 16;
 
 cudaError_t launch_append(const AppendArgs& a0, cudaStream_t s) {
   AppendArgs a = a0;
-  if (a.T < BULK_MIN_T) {
+  // the bulk kernel's grid has y = (layer, kv-head, K|V) and z = sequence (at most 65535 each)
+  if (a.T < BULK_MIN_T || (long long)a.n_layers_call * a.Hkv * 2 > 65535 || a.batch > 65535) {
     a.kv_lo = 0;
     a.kv_n = 2;
     return launch_append_warps(a, s);

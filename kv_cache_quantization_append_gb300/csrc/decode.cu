@@ -38,19 +38,24 @@ constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
 
-// Per-format CTA geometry and shared-memory carve-up (bytes): 11 consumer warps + 1 producer warp
-// (12 warps keep the 168-register budget per thread); measured faster than 15 consumer warps at 128
-// registers for Q4G32 keys (the build flag KVQ_Q4_CONSUMER_WARPS selects the latter).
+// Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
+// Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
+// latency; measured faster than 11 warps with 3 stages at 168 registers); TQ3 keys, whose fragments
+// need more registers: 11 consumer warps.  Build flags KVQ_Q4_CONSUMER_WARPS, KVQ_Q4_SLOTS and
+// KVQ_TQ_CONSUMER_WARPS override the counts.
 template <int KF>
 struct Geo {
   static constexpr bool TQ = KF == KVQ_TQ3_QJL;
-#ifndef KVQ_Q4_CONSUMER_WARPS
-#define KVQ_Q4_CONSUMER_WARPS 11
+#ifndef KVQ_TQ_CONSUMER_WARPS
+#define KVQ_TQ_CONSUMER_WARPS 11
 #endif
-  static constexpr int NCW = TQ ? 11 : KVQ_Q4_CONSUMER_WARPS;  // consumer warps
+#ifndef KVQ_Q4_CONSUMER_WARPS
+#define KVQ_Q4_CONSUMER_WARPS 15
+#endif
+  static constexpr int NCW = TQ ? KVQ_TQ_CONSUMER_WARPS : KVQ_Q4_CONSUMER_WARPS;  // consumer warps
   static constexpr int NTHREADS = (NCW + 1) * 32;      // + 1 producer warp
 #ifndef KVQ_Q4_SLOTS
-#define KVQ_Q4_SLOTS 3
+#define KVQ_Q4_SLOTS 2
 #endif
   static constexpr int NSLOT = TQ ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
   static constexpr int NSTAGE = NSLOT * NCW;
@@ -84,6 +89,16 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// non-blocking: has the phase with this parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
       : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
@@ -1029,18 +1044,26 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   if ((long long)blockIdx.x * NCW >= K.nw) return;
 
   if (K.warp == NCW) {
-    // ======================= producer: lane w streams consumer warp w's contiguous step range
+    // ======================= producer: lane w streams consumer warp w's contiguous step range.
+    // The lanes poll their next stage without blocking and start, in the same pass, every copy
+    // whose stage has been released, so the warp stays converged; a pass that starts nothing
+    // sleeps briefly, and ~1 s without any progress ends the stream with a status bit.
     const int w = K.lane;
     const long long gw = (long long)blockIdx.x * NCW + w;
+    int n = 0;
+    Pos ps = {0, 0, 0, 0};
     if (w < NCW && gw < K.nw) {
       const long long xs = gw * K.S / K.nw, xe = (gw + 1) * K.S / K.nw;
-      const int n = (int)(xe - xs);
-      Pos ps = locate(xs, K.S_layer, B, H, K.sq);
-      int issued = 0;
-      constexpr int NS = GE::NSLOT;
-      for (int k = 0; k < n; ++k) {
-        const int slot = w + NCW * (k % NS);
-        if (k >= NS && !mbar_wait(empty + slot, ((k / NS) - 1) & 1, a.p.status)) break;
+      n = (int)(xe - xs);
+      ps = locate(xs, K.S_layer, B, H, K.sq);
+    }
+    constexpr int NS = GE::NSLOT;
+    int k = 0;
+    unsigned long long t_idle = 0;
+    while (__any_sync(FULL, k < n)) {
+      const int slot = w + NCW * (k % NS);
+      const bool ready = k < n && (k < NS || mbar_test(empty + slot, ((k / NS) - 1) & 1));
+      if (ready) {
         const int u = (ps.ll * B + ps.b) * H + ps.h;
         const int layer = a.layer0 + ps.ll;
         const int L = sL[ps.b];
@@ -1072,13 +1095,22 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
             bulk_g2s(dst, src, a.L.half_bytes, full + slot);
           }
         }
-        issued = k + 1;
-        if (k + 1 < n) advance(ps, 1, B, H, K.sq);
+        if (++k < n) advance(ps, 1, B, H, K.sq);
       }
-      // never leave the CTA with a copy still landing in shared memory
-      for (int k = max(0, issued - NS); k < issued; ++k)
-        mbar_wait(full + w + NCW * (k % NS), (k / NS) & 1, a.p.status);
+      if (__any_sync(FULL, ready)) {
+        t_idle = 0;
+      } else {
+        const unsigned long long now = globaltimer();
+        if (t_idle == 0) t_idle = now;
+        if (__any_sync(FULL, now - t_idle > WAIT_NS)) {
+          if (w == 0) atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
+          break;
+        }
+        __nanosleep(64);
+      }
     }
+    // never leave the CTA with a copy still landing in shared memory
+    for (int kk = max(0, k - NS); kk < k; ++kk) mbar_wait(full + w + NCW * (kk % NS), (kk / NS) & 1, a.p.status);
     return;
   }
 
