@@ -37,6 +37,10 @@ constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
+// Per-CTA queue of units ready to merge: [MQ_CAP] unit ids (-1 = not yet written), then tail, head
+// and the number of consumer warps whose streams have ended.
+constexpr int MQ_CAP = 256;
+constexpr int MQ_TAIL = MQ_CAP, MQ_HEAD = MQ_CAP + 1, MQ_DONE = MQ_CAP + 2;
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
@@ -68,7 +72,8 @@ struct Geo {
   static constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                      // [64][32] u32 (TQ)
   static constexpr int SM_P = SM_LUT + (TQ ? 64 * 32 * 4 : 0);               // [NCW][2][4][32] fp16
   static constexpr int SM_WML = SM_P + NCW * 2 * MAX_GQA * HALF * 2;         // [NCW][8] float
-  static constexpr int SM_SEQ = SM_WML + NCW * 8 * 4;                        // 3 int[batch+1]
+  static constexpr int SM_MQ = SM_WML + NCW * 8 * 4;                         // merge queue
+  static constexpr int SM_SEQ = SM_MQ + (MQ_CAP + 4) * 4;                     // 3 int[batch+1]
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -794,8 +799,8 @@ struct Kernel {
   // Combine the unit's partial records (one per warp that streamed part of it) in record order.
   // Latency-bound, so the round trips are few: per part (quantised, window) lane j reads record j's
   // header (32 records at a time, with running maxima across chunks), weights are reduced in
-  // registers, and the accumulators of eight records (all heads) are requested together.  Runs
-  // after the warp's streaming loop, with the whole register budget.
+  // registers, and the accumulators of four records holding the part (all heads) are requested
+  // together.  Runs once the merging warp's stream has ended.
   __device__ __noinline__ void merge(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const int layer = a.layer0 + ll;
@@ -840,28 +845,35 @@ struct Kernel {
           for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
           L[hh] += lw;
         }
-        const int cnt = min(32, nrec - base);
-        for (int jj = 0; jj < cnt; jj += 8) {
-          // eight records' accumulators (all heads) requested before any is used
-          float4 x[8][MAX_GQA];
+        // only records with a part k (a window part is usually in one record of the unit), four
+        // records' accumulators requested before any is used
+        bool has = false;
 #pragma unroll
-          for (int r8 = 0; r8 < 8; ++r8) {
-            const float* rec = record(u, cf + base + min(jj + r8, cnt - 1)) + 16 + k * MAX_GQA * D + 4 * lane;
+        for (int hh = 0; hh < MAX_GQA; ++hh) has |= f[hh] > 0.f;
+        unsigned act = __ballot_sync(FULL, has && base + lane < nrec);
+        while (act) {
+          int jr[4];
+          float4 x[4][MAX_GQA];
+#pragma unroll
+          for (int r4 = 0; r4 < 4; ++r4) {
+            jr[r4] = act ? __ffs(act) - 1 : -1;
+            act &= act - 1;
+            const float* rec = record(u, cf + base + max(jr[r4], 0)) + 16 + k * MAX_GQA * D + 4 * lane;
 #pragma unroll
             for (int hh = 0; hh < MAX_GQA; ++hh)
-              x[r8][hh] = (hh < g && jj + r8 < cnt) ? __ldcg(reinterpret_cast<const float4*>(rec + hh * D))
-                                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+              x[r4][hh] = (hh < g && jr[r4] >= 0) ? __ldcg(reinterpret_cast<const float4*>(rec + hh * D))
+                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int r8 = 0; r8 < 8; ++r8)
+          for (int r4 = 0; r4 < 4; ++r4)
 #pragma unroll
             for (int hh = 0; hh < MAX_GQA; ++hh) {
-              const float fj = __shfl_sync(FULL, f[hh], (jj + r8) & 31);
-              if (jj + r8 < cnt && fj > 0.f) {  // a part with no tokens holds no accumulator
-                A[hh].x += fj * x[r8][hh].x;
-                A[hh].y += fj * x[r8][hh].y;
-                A[hh].z += fj * x[r8][hh].z;
-                A[hh].w += fj * x[r8][hh].w;
+              const float fj = __shfl_sync(FULL, f[hh], max(jr[r4], 0));
+              if (jr[r4] >= 0 && fj > 0.f) {  // a head with no tokens in this part holds no accumulator
+                A[hh].x += fj * x[r4][hh].x;
+                A[hh].y += fj * x[r4][hh].y;
+                A[hh].z += fj * x[r4][hh].z;
+                A[hh].w += fj * x[r4][hh].w;
               }
             }
         }
@@ -932,13 +944,66 @@ struct Kernel {
     return false;
   }
 
-  // write this warp's record of unit u; if it was the last one, flag the unit for this warp to
-  // merge after its streaming loop (keeping the merge code out of the loop)
+  // Write this warp's record of unit u.  If it was the last one, queue the unit on the CTA's merge
+  // queue, which all the CTA's warps drain once their streams end (keeping the merge code out of
+  // the streaming loop and spreading the merges over the warps); when the queue is full, flag the
+  // unit for this warp to merge after its own loop.
   __device__ void finish_unit(int u, int gw, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
     float* rec = record(u, gw);
     if (kind == KIND_QUANT) write_quant(rec, st);
     write_header(rec, hasq, st, hasw, ws);
-    if (arrive(u) && lane == 0) a.counters[a.n_units + u + gw] = 1;
+    if (arrive(u) && lane == 0) {
+      int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
+      const int slot = atomicAdd(mq + MQ_TAIL, 1);
+      if (slot < MQ_CAP) {
+        // the records (acquired by the arrival above) before the queue entry that hands them on
+        __threadfence();
+        *reinterpret_cast<volatile int*>(mq + slot) = u;
+      } else {
+        a.counters[a.n_units + u + gw] = 1;
+      }
+    }
+  }
+
+  // Drain the CTA's merge queue until every consumer warp of the CTA has ended its stream and the
+  // queue is empty; gives up (status bit) after ~1 s without either.
+  __device__ __noinline__ void drain_merges(int nact) {
+    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
+    volatile int* vq = mq;
+    unsigned long long t0 = 0;
+    while (true) {
+      int u = -1, stop = 0;
+      if (lane == 0) {
+        const int h = vq[MQ_HEAD];
+        const int t = min(vq[MQ_TAIL], MQ_CAP);
+        if (h < t) {
+          if (atomicCAS(mq + MQ_HEAD, h, h + 1) == h) {
+            const unsigned long long tw = globaltimer();
+            while ((u = vq[h]) < 0 && globaltimer() - tw < WAIT_NS) {}
+            if (u < 0) {
+              atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
+              stop = 1;
+            }
+          }
+        } else if (vq[MQ_DONE] >= nact && vq[MQ_HEAD] >= min(vq[MQ_TAIL], MQ_CAP)) {
+          stop = 1;
+        } else {
+          if (t0 == 0) t0 = globaltimer();
+          if (globaltimer() - t0 > WAIT_NS) {
+            atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
+            stop = 1;
+          }
+          __nanosleep(128);
+        }
+      }
+      u = __shfl_sync(FULL, u, 0);
+      if (__shfl_sync(FULL, stop, 0)) break;
+      if (u >= 0) {
+        __threadfence();
+        merge(u);
+        t0 = 0;
+      }
+    }
   }
 
   // merge the units of steps [xs, xe) that this warp flagged
@@ -1009,6 +1074,10 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       run += sS[b];
     }
     if (lane == 31) sPre[B] = incl;
+  }
+  {
+    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
+    for (int i = tid; i < MQ_CAP + 4; i += NTHREADS) mq[i] = i < MQ_CAP ? -1 : 0;
   }
   if (tid == 0) {
     for (int i = 0; i < NSTAGE; ++i) {
@@ -1175,6 +1244,11 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   }
   K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
   K.run_merges((int)gw, gw * K.S / K.nw, (gw + 1) * K.S / K.nw);
+  if (K.lane == 0) {
+    __threadfence_block();
+    atomicAdd(reinterpret_cast<int*>(smem + GE::SM_MQ) + MQ_DONE, 1);
+  }
+  K.drain_merges((int)min((long long)NCW, K.nw - (long long)blockIdx.x * NCW));
 }
 
 }  // namespace
