@@ -73,7 +73,7 @@ struct Geo {
   static constexpr int SM_P = SM_LUT + (TQ ? 64 * 32 * 4 : 0);               // [NCW][2][4][32] fp16
   static constexpr int SM_WML = SM_P + NCW * 2 * MAX_GQA * HALF * 2;         // [NCW][8] float
   static constexpr int SM_MQ = SM_WML + NCW * 8 * 4;                         // merge queue
-  static constexpr int SM_SEQ = SM_MQ + (MQ_CAP + 4) * 4;                     // 3 int[batch+1]
+  static constexpr int SM_SEQ = SM_MQ + (MQ_CAP + 4) * 4;                     // 6 int[batch+1]
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -172,10 +172,23 @@ __device__ __forceinline__ uint32_t split_pick(float v, bool lo) {
 }
 
 struct Seq {
-  const int* S;    // steps per sequence
-  const int* pre;  // exclusive prefix of S, [batch + 1]
-  const int* L;    // validated lengths
+  const int* S;     // steps per sequence
+  const int* pre;   // exclusive prefix of S, [batch + 1]
+  const int* L;     // validated lengths
+  const int* NW;    // window steps per sequence
+  const int* C;     // cost of one unit of the sequence (0 when it has no steps)
+  const int* cpre;  // exclusive prefix of C, [batch + 1]
 };
+
+// Relative costs used to split a call's steps over the warps, in sixteenths of a quantised
+// half-page step (measured with per-warp timestamps): a window chunk costs about as much as a
+// half-page, and the set-up of a unit (query rotation, its record) about two, charged to the
+// unit's first step.  Relative speeds of the consumer warps: the three (two) that share an SM
+// sub-partition with the producer warp get about 10 % more issue slots than the others and
+// finish their ranges that much earlier, so they get proportionally longer ranges.
+constexpr int COST_Q = 16, COST_WIN = 16, COST_UNIT = 32;
+constexpr int COST_MAX_STEP = COST_UNIT + COST_Q;
+constexpr int SPEED_NORMAL = 10, SPEED_FAST = 11;
 
 struct Pos {
   int ll, b, h, local;
@@ -225,13 +238,12 @@ struct QuantState {
   float m, l;          // running max / partial sum for head (lane & 3)
 };
 
-// Window-part state of a warp, kept out of registers while the warp streams quantised pages:
-// q [4][128] in its shared-memory q slice (reused by the quantised part only after the window
-// steps of the unit), acc [4][128] directly in the warp's own partial record (global scratch,
-// written and read back only by this warp's lanes), m and l in a small shared slice.
+// Window-part state of a warp: q [4][128] in its shared-memory q slice (reused by the quantised
+// part only after the window steps of the unit), m and l in a small shared slice; the accumulator
+// [4][128] (16 values per lane) borrows the first four rows of the quantised part's accumulator
+// registers, which the unit's quantised steps only start using after its window steps.
 struct WinState {
   float* q;
-  float* acc;
   float* ml;
 };
 
@@ -245,8 +257,10 @@ struct Kernel {
   uint8_t* smem;
   int lane, warp;
   int B, H, W, g, Hq;
-  long long S_layer, S;
-  long long nw;  // warps that own steps: min(gridDim.x * NCW, S), each owns at least one
+  long long S_layer, S;  // steps per layer, steps of the call
+  long long C_layer, C;  // costs per layer, cost of the call
+  long long nw;     // warps that own steps; every warp's cost range holds at least one step start
+  long long SPtot;  // summed speeds of the nw warps
   Seq sq;
 
   __device__ Kernel(const DecodeArgs& args, uint8_t* s) : a(args), smem(s) {}
@@ -254,9 +268,69 @@ struct Kernel {
   __device__ __forceinline__ long long steps_before(int ll, int b, int h) const {
     return (long long)ll * S_layer + (long long)H * sq.pre[b] + (long long)h * sq.S[b];
   }
-  // global consumer warp whose contiguous step range holds step x; the ranges split the S steps
-  // over nw warps (warp gw = CTA * NCW + warp owns [gw*S/nw, (gw+1)*S/nw))
-  __device__ __forceinline__ int owner(long long x) const { return (int)(((x + 1) * nw - 1) / S); }
+  // Work split: the steps are laid on a cost line in order (step `local` of unit (ll, b, h)
+  // starts at cost_at(...)), the line is cut into nw ranges in proportion to the warps' speeds,
+  // and warp gw (= CTA * NCW + warp) owns the steps that start in [lb(gw), lb(gw + 1)) with
+  // lb(g) = floor(C * SP(g) / SPtot), SP(g) = the summed speeds of warps 0 .. g-1.
+  // summed speeds of consumer warps 0 .. w-1 of a CTA
+  __device__ __forceinline__ long long speed_prefix(int w) const {
+    const int f = NCW & 3;  // sub-partition of the producer warp (warp NCW)
+    const int nf = w > f ? (w - f - 1) / 4 + 1 : 0;
+    return (long long)SPEED_NORMAL * w + (long long)(SPEED_FAST - SPEED_NORMAL) * nf;
+  }
+  __device__ __forceinline__ long long speed_before(long long g) const {
+    return (g / NCW) * speed_prefix(NCW) + speed_prefix((int)(g % NCW));
+  }
+  __device__ __forceinline__ long long lb(long long g) const { return C * speed_before(g) / SPtot; }
+  __device__ __forceinline__ long long cost_at(int ll, int b, int h, int local) const {
+    long long c = (long long)ll * C_layer + (long long)H * sq.cpre[b] + (long long)h * sq.C[b];
+    if (local > 0) {
+      const int nwin = sq.NW[b];
+      c += COST_UNIT + (long long)min(local, nwin) * COST_WIN + (long long)max(0, local - nwin) * COST_Q;
+    }
+    return c;
+  }
+  // warp whose cost range holds cost position c: the last g with speed_before(g) <= T, where
+  // lb(g) <= c  <=>  speed_before(g) <= T = floor(((c + 1) SPtot - 1) / C)
+  __device__ __forceinline__ int owner(long long c) const {
+    const long long T = ((c + 1) * SPtot - 1) / C;
+    const long long scta = speed_prefix(NCW);
+    const long long cta = T / scta, rem = T - cta * scta;
+    int w = NCW - 1;
+    while (speed_prefix(w) > rem) --w;
+    return (int)(cta * NCW + w);
+  }
+  // global step index of a position
+  __device__ __forceinline__ long long step_index(const Pos& p) const {
+    return steps_before(p.ll, p.b, p.h) + p.local;
+  }
+  // first step of warp gw (gw < nw): the first step starting at or after lb(gw)
+  __device__ Pos first_step(long long gw) const {
+    const long long y = lb(gw);
+    Pos p;
+    p.ll = (int)(y / C_layer);
+    const long long r = y - (long long)p.ll * C_layer;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if ((long long)H * sq.cpre[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    p.b = lo;
+    const long long r2 = r - (long long)H * sq.cpre[lo];
+    p.h = (int)(r2 / sq.C[lo]);
+    const int r3 = (int)(r2 - (long long)p.h * sq.C[lo]);
+    const int nwin = sq.NW[lo];
+    p.local = (r3 < COST_UNIT + nwin * COST_WIN) ? max(0, r3 - COST_UNIT) / COST_WIN
+                                                 : nwin + (r3 - COST_UNIT - nwin * COST_WIN) / COST_Q;
+    if (cost_at(p.ll, p.b, p.h, p.local) < y) advance(p, 1, B, H, sq);
+    return p;
+  }
+  // [first, last] cost positions of unit u's steps' starts, as owner() arguments
+  __device__ __forceinline__ void unit_owners(int ll, int b, int h, int& first, int& count) const {
+    first = owner(cost_at(ll, b, h, 0));
+    count = owner(cost_at(ll, b, h, sq.S[b] - 1)) - first + 1;
+  }
 
   // ---------------------------------------------------------------- unit set-up
   // issue the loads of unit u's g query vectors (lane holds channels 4*lane..+3 of each)
@@ -286,7 +360,7 @@ struct Kernel {
         const float4 x = raw[hh];
         *reinterpret_cast<float4*>(ws.q + hh * D + 4 * lane) =
             make_float4(x.x * LOGIT_SCALE, x.y * LOGIT_SCALE, x.z * LOGIT_SCALE, x.w * LOGIT_SCALE);
-        *reinterpret_cast<float4*>(ws.acc + hh * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+        st.acc[hh][0] = st.acc[hh][1] = st.acc[hh][2] = st.acc[hh][3] = 0.f;
       }
       if (lane < 8) ws.ml[lane] = lane < 4 ? -INFINITY : 0.f;
       __syncwarp();
@@ -386,7 +460,7 @@ struct Kernel {
   }
 
   // ---------------------------------------------------------------- window chunk (raw fp32)
-  __device__ void window_step(const uint8_t* stage, int ntok, WinState& ws) {
+  __device__ void window_step(const uint8_t* stage, int ntok, WinState& ws, QuantState& st) {
     const float* Ks = reinterpret_cast<const float*>(stage);
     const float* Vs = Ks + WCHUNK * D;
     float4 q4[MAX_GQA];
@@ -436,7 +510,7 @@ struct Kernel {
     for (int k = 0; k < MAX_GQA; ++k) lk[k] = ws.ml[4 + k] * alpha[k] + __shfl_sync(FULL, ps, 2 * k);
 #pragma unroll
     for (int k = 0; k < MAX_GQA; ++k) {
-      float4 acc = *reinterpret_cast<const float4*>(ws.acc + k * D + 4 * lane);
+      float4 acc = make_float4(st.acc[k][0], st.acc[k][1], st.acc[k][2], st.acc[k][3]);
       acc.x *= alpha[k];
       acc.y *= alpha[k];
       acc.z *= alpha[k];
@@ -452,7 +526,10 @@ struct Kernel {
           acc.w += pt * v4.w;
         }
       }
-      *reinterpret_cast<float4*>(ws.acc + k * D + 4 * lane) = acc;
+      st.acc[k][0] = acc.x;
+      st.acc[k][1] = acc.y;
+      st.acc[k][2] = acc.z;
+      st.acc[k][3] = acc.w;
     }
     __syncwarp();
     if (lane < MAX_GQA) {
@@ -804,8 +881,8 @@ struct Kernel {
   __device__ __noinline__ void merge(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const int layer = a.layer0 + ll;
-    const long long sb = steps_before(ll, b, h);
-    const int cf = owner(sb), nrec = owner(sb + sq.S[b] - 1) - cf + 1;
+    int cf, nrec;
+    unit_owners(ll, b, h, cf, nrec);
     float outp[2][MAX_GQA][4], Mk[2][MAX_GQA], Lk[2][MAX_GQA];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
@@ -925,35 +1002,45 @@ struct Kernel {
   }
 
   // publish this warp's record for unit u; true if it was the unit's last arrival (which merges)
-  __device__ bool arrive(int u) {
-    const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-    const long long sb = steps_before(ll, b, h);
-    const int nwu = owner(sb + sq.S[b] - 1) - owner(sb) + 1;
-    // every lane makes its own record writes visible device-wide, then one lane counts the arrival
-    // (acquire-release: the last arrival then sees the other warps' records)
-    __threadfence();
-    __syncwarp();
-    int old = 0;
-    if (lane == 0)
-      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
-    old = __shfl_sync(FULL, old, 0);
-    if (old == nwu - 1) {
-      __threadfence();
-      return true;
-    }
-    return false;
+  // window accumulator of this warp's part of unit u into its record
+  __device__ __forceinline__ void store_window_acc(int u, int gw, const QuantState& st) {
+    float* dst = record(u, gw) + 16 + MAX_GQA * D + 4 * lane;
+#pragma unroll
+    for (int k = 0; k < MAX_GQA; ++k)
+      *reinterpret_cast<float4*>(dst + k * D) = make_float4(st.acc[k][0], st.acc[k][1], st.acc[k][2], st.acc[k][3]);
   }
 
-  // Write this warp's record of unit u.  If it was the last one, queue the unit on the CTA's merge
-  // queue, which all the CTA's warps drain once their streams end (keeping the merge code out of
-  // the streaming loop and spreading the merges over the warps); when the queue is full, flag the
-  // unit for this warp to merge after its own loop.
+  // Write this warp's record of unit u (its arrival is counted after the warp's stream ends).
   __device__ void finish_unit(int u, int gw, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
     float* rec = record(u, gw);
     if (kind == KIND_QUANT) write_quant(rec, st);
+    else store_window_acc(u, gw, st);
     write_header(rec, hasq, st, hasw, ws);
-    if (arrive(u) && lane == 0) {
-      int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
+  }
+
+  // Count this warp's arrival at each unit of steps [xs, xe) (their records are written).  No part
+  // of a unit this warp leaves early completes before the warp's stream ends anyway: the other
+  // warps of the unit end their parts at the ends of their own ranges.  The last arrival queues
+  // the unit on the CTA's merge queue, which all the CTA's warps drain once their streams end
+  // (keeping the merge code out of the streaming loop and spreading the merges over the warps);
+  // when the queue is full, it flags the unit for this warp to merge after its own loop.
+  __device__ __noinline__ void arrive_units(int gw, long long xs, long long xe) {
+    const Pos pf = locate(xs, S_layer, B, H, sq);
+    const Pos pl = locate(xe - 1, S_layer, B, H, sq);
+    const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
+    // every lane makes its own record writes visible device-wide before lane 0 counts them
+    __threadfence();
+    __syncwarp();
+    if (lane != 0) return;
+    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
+    for (int u = uf; u <= ul; ++u) {
+      const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+      if (sq.S[b] == 0) continue;  // no steps, no records
+      int cf, nwu;
+      unit_owners(ll, b, h, cf, nwu);
+      int old;
+      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
+      if (old != nwu - 1) continue;
       const int slot = atomicAdd(mq + MQ_TAIL, 1);
       if (slot < MQ_CAP) {
         // the records (acquired by the arrival above) before the queue entry that hands them on
@@ -1040,6 +1127,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   int* sS = reinterpret_cast<int*>(smem + GE::SM_SEQ);
   int* sPre = sS + (B + 1);
   int* sL = sPre + (B + 1);
+  int* sNW = sL + (B + 1);
+  int* sC = sNW + (B + 1);
+  int* sCpre = sC + (B + 1);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + GE::SM_BARS);
   uint64_t* empty = full + NSTAGE;
   int4* desc = reinterpret_cast<int4*>(smem + GE::SM_DESC);
@@ -1053,27 +1143,42 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     }
     const int Lq = W > 0 ? max(0, L - W) : L;
     const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
+    const int nq = (Lq + HALF - 1) / HALF;
     sL[b] = L;
-    sS[b] = nw + (Lq + HALF - 1) / HALF;
+    sNW[b] = nw;
+    sS[b] = nw + nq;
+    sC[b] = (nw + nq) > 0 ? COST_UNIT + nw * COST_WIN + nq * COST_Q : 0;
   }
   __syncthreads();
   if (K.warp == 0) {
     const int lane = K.lane;
     const int per = (B + 31) / 32, b0 = lane * per, b1 = min(B, b0 + per);
-    int s = 0;
-    for (int b = b0; b < b1; ++b) s += sS[b];
-    int incl = s;
+    int s = 0, c = 0;
+    for (int b = b0; b < b1; ++b) {
+      s += sS[b];
+      c += sC[b];
+    }
+    int incl = s, cincl = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(FULL, incl, o);
-      if (lane >= o) incl += y;
+      const int z = __shfl_up_sync(FULL, cincl, o);
+      if (lane >= o) {
+        incl += y;
+        cincl += z;
+      }
     }
-    int run = incl - s;
+    int run = incl - s, crun = cincl - c;
     for (int b = b0; b < b1; ++b) {
       sPre[b] = run;
       run += sS[b];
+      sCpre[b] = crun;
+      crun += sC[b];
     }
-    if (lane == 31) sPre[B] = incl;
+    if (lane == 31) {
+      sPre[B] = incl;
+      sCpre[B] = cincl;
+    }
   }
   {
     int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
@@ -1095,6 +1200,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   K.sq.S = sS;
   K.sq.pre = sPre;
   K.sq.L = sL;
+  K.sq.NW = sNW;
+  K.sq.C = sC;
+  K.sq.cpre = sCpre;
 
   // empty sequences produce zeros (no step belongs to them)
   if (blockIdx.x == 0) {
@@ -1108,8 +1216,12 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
 
   K.S_layer = (long long)H * sPre[B];
   K.S = K.S_layer * a.n_layers_call;
+  K.C_layer = (long long)H * sCpre[B];
+  K.C = K.C_layer * a.n_layers_call;
   if (K.S == 0) return;
-  K.nw = min((long long)gridDim.x * NCW, K.S);
+  // every range, even a normal-speed one, must span at least the longest step
+  K.nw = max(1LL, min((long long)gridDim.x * NCW, K.C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
+  K.SPtot = K.speed_before(K.nw);
   if ((long long)blockIdx.x * NCW >= K.nw) return;
 
   if (K.warp == NCW) {
@@ -1122,9 +1234,10 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     int n = 0;
     Pos ps = {0, 0, 0, 0};
     if (w < NCW && gw < K.nw) {
-      const long long xs = gw * K.S / K.nw, xe = (gw + 1) * K.S / K.nw;
+      ps = K.first_step(gw);
+      const long long xs = K.step_index(ps);
+      const long long xe = gw + 1 < K.nw ? K.step_index(K.first_step(gw + 1)) : K.S;
       n = (int)(xe - xs);
-      ps = locate(xs, K.S_layer, B, H, K.sq);
     }
     constexpr int NS = GE::NSLOT;
     int k = 0;
@@ -1183,26 +1296,26 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     return;
   }
 
-  // ======================= consumers: warp gw processes steps [gw*S/nw, (gw+1)*S/nw) in order
+  // ======================= consumers: warp gw processes its steps (see first_step) in order
   const long long gw = (long long)blockIdx.x * NCW + K.warp;
   if (gw >= K.nw) return;
-  const int n = (int)((gw + 1) * K.S / K.nw - gw * K.S / K.nw);
+  const Pos p0 = K.first_step(gw);
+  const long long xs = K.step_index(p0);
+  const long long xe = gw + 1 < K.nw ? K.step_index(K.first_step(gw + 1)) : K.S;
+  const int n = (int)(xe - xs);
   QuantState st;
   WinState ws;
   ws.q = reinterpret_cast<float*>(smem + GE::SM_Q) + K.warp * MAX_GQA * D;
-  ws.acc = nullptr;  // set to the unit's record when its window steps start
   ws.ml = reinterpret_cast<float*>(smem + GE::SM_WML) + K.warp * 8;
   int cur = -1, kind = -1;
   bool hasq = false, hasw = false;
   {
     // set up the first unit while the pipeline fills
-    const Pos p0 = locate(gw * K.S / K.nw, K.S_layer, B, H, K.sq);
     const int L0 = sL[p0.b];
     const int nwin0 = W > 0 ? (min(L0, W) + WCHUNK - 1) / WCHUNK : 0;
     cur = (p0.ll * B + p0.b) * H + p0.h;
     kind = p0.local < nwin0 ? KIND_WINDOW : KIND_QUANT;
     if (kind == KIND_WINDOW) {
-      ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
       hasw = true;
     } else {
       hasq = true;
@@ -1226,9 +1339,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       kind = d.y;
       hasq = kind == KIND_QUANT;
       hasw = kind == KIND_WINDOW;
-      if (kind == KIND_WINDOW) ws.acc = K.record(cur, (int)gw) + 16 + MAX_GQA * D;
       K.build_q(cur, raw, st, ws, kind);
     } else if (d.y != kind) {
+      if (kind == KIND_WINDOW) K.store_window_acc(cur, (int)gw, st);
       K.load_q(cur, st, ws, d.y);
       kind = d.y;
       if (kind == KIND_WINDOW) hasw = true;
@@ -1236,14 +1349,15 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     }
     uint8_t* stage = smem + GE::SM_STAGES + slot * STAGE_BYTES;
     if (d.z > 0) {
-      if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws);
+      if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws, st);
       else K.quant_step(stage, d.z, st);
     }
     __syncwarp();
     if (K.lane == 0) mbar_arrive(empty + slot);
   }
   K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
-  K.run_merges((int)gw, gw * K.S / K.nw, (gw + 1) * K.S / K.nw);
+  K.arrive_units((int)gw, xs, xe);
+  K.run_merges((int)gw, xs, xe);
   if (K.lane == 0) {
     __threadfence_block();
     atomicAdd(reinterpret_cast<int*>(smem + GE::SM_MQ) + MQ_DONE, 1);
@@ -1266,7 +1380,7 @@ size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
 
 template <int KF>
 static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
-  const size_t smem = Geo<KF>::SM_SEQ + 3 * (size_t)(a.batch + 1) * sizeof(int);
+  const size_t smem = Geo<KF>::SM_SEQ + 6 * (size_t)(a.batch + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   decode_kernel<KF><<<a.n_ctas, Geo<KF>::NTHREADS, smem, s>>>(a);
