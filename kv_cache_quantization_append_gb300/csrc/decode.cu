@@ -874,60 +874,70 @@ struct Kernel {
   }
 
   // Combine the unit's partial records (one per warp that streamed part of it) in record order.
-  // Latency-bound, so the round trips are few: per part (quantised, window) lane j reads record j's
-  // header (32 records at a time, with running maxima across chunks), weights are reduced in
-  // registers, and the accumulators of four records holding the part (all heads) are requested
-  // together.  Runs once the merging warp's stream has ended.
+  // Latency-bound, so the round trips are few: lane j reads both parts' headers of record j in
+  // one request (32 records at a time, with running maxima across chunks), weights are reduced in
+  // registers, then per part (quantised, window) the accumulators of four records holding the part
+  // (all heads) are requested together.  Runs once the merging warp's stream has ended.
   __device__ __noinline__ void merge(int u) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const int layer = a.layer0 + ll;
     int cf, nrec;
     unit_owners(ll, b, h, cf, nrec);
+    // constants of the output phase, requested first
+    const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+    float4 sv = make_float4(1.f, 1.f, 1.f, 1.f);
+    if (a.sinkhorn) {
+      const __half2* sig = reinterpret_cast<const __half2*>(a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane);
+      const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
+      sv = make_float4(s01.x, s01.y, s23.x, s23.y);
+    }
     float outp[2][MAX_GQA][4], Mk[2][MAX_GQA], Lk[2][MAX_GQA];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
-      float M[MAX_GQA], L[MAX_GQA];
-      float4 A[MAX_GQA];
+    for (int k = 0; k < 2; ++k)
 #pragma unroll
       for (int hh = 0; hh < MAX_GQA; ++hh) {
-        M[hh] = -INFINITY;
-        L[hh] = 0.f;
-        A[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+        Mk[k][hh] = -INFINITY;
+        Lk[k][hh] = 0.f;
+        outp[k][hh][0] = outp[k][hh][1] = outp[k][hh][2] = outp[k][hh][3] = 0.f;
       }
-      for (int base = 0; base < nrec; base += 32) {
-        float4 hm = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), hl = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (base + lane < nrec) {
-          const float4* hp = reinterpret_cast<const float4*>(record(u, cf + base + lane)) + 2 * k;
-          hm = __ldcg(hp);
-          hl = __ldcg(hp + 1);
-        }
-        const float mv[4] = {hm.x, hm.y, hm.z, hm.w}, lv[4] = {hl.x, hl.y, hl.z, hl.w};
+    for (int base = 0; base < nrec; base += 32) {
+      // both parts' headers of record base + lane, [Qm[4], Ql[4], Wm[4], Wl[4]], in one request
+      float4 hd[4] = {make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), make_float4(0.f, 0.f, 0.f, 0.f),
+                      make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), make_float4(0.f, 0.f, 0.f, 0.f)};
+      if (base + lane < nrec) {
+        const float4* hp = reinterpret_cast<const float4*>(record(u, cf + base + lane));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + i);
+      }
+      const int cnt = min(32, nrec - base);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
+        const float mv[4] = {hd[2 * k].x, hd[2 * k].y, hd[2 * k].z, hd[2 * k].w};
+        const float lv[4] = {hd[2 * k + 1].x, hd[2 * k + 1].y, hd[2 * k + 1].z, hd[2 * k + 1].w};
         float f[MAX_GQA];
+        float4 A[MAX_GQA];
 #pragma unroll
         for (int hh = 0; hh < MAX_GQA; ++hh) {
           float m = lv[hh] > 0.f ? mv[hh] : -INFINITY;
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-          const float mn = fmaxf(M[hh], m);
-          const float sc = (M[hh] == -INFINITY) ? 0.f : exp2f(M[hh] - mn);  // rescale earlier chunks
-          L[hh] *= sc;
-          A[hh].x *= sc;
-          A[hh].y *= sc;
-          A[hh].z *= sc;
-          A[hh].w *= sc;
-          M[hh] = mn;
+          const float mn = fmaxf(Mk[k][hh], m);
+          const float sc = (Mk[k][hh] == -INFINITY) ? 0.f : exp2f(Mk[k][hh] - mn);  // rescale earlier chunks
+          Lk[k][hh] *= sc;
+          A[hh] = make_float4(outp[k][hh][0] * sc, outp[k][hh][1] * sc, outp[k][hh][2] * sc, outp[k][hh][3] * sc);
+          Mk[k][hh] = mn;
           f[hh] = lv[hh] > 0.f ? exp2f(mv[hh] - mn) : 0.f;
           float lw = lv[hh] * f[hh];
 #pragma unroll
           for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
-          L[hh] += lw;
+          Lk[k][hh] += lw;
         }
         // only records with a part k (a window part is usually in one record of the unit), four
         // records' accumulators requested before any is used
         bool has = false;
 #pragma unroll
         for (int hh = 0; hh < MAX_GQA; ++hh) has |= f[hh] > 0.f;
-        unsigned act = __ballot_sync(FULL, has && base + lane < nrec);
+        unsigned act = __ballot_sync(FULL, has && lane < cnt);
         while (act) {
           int jr[4];
           float4 x[4][MAX_GQA];
@@ -954,15 +964,13 @@ struct Kernel {
               }
             }
         }
-      }
 #pragma unroll
-      for (int hh = 0; hh < MAX_GQA; ++hh) {
-        Mk[k][hh] = M[hh];
-        Lk[k][hh] = L[hh];
-        outp[k][hh][0] = A[hh].x;
-        outp[k][hh][1] = A[hh].y;
-        outp[k][hh][2] = A[hh].z;
-        outp[k][hh][3] = A[hh].w;
+        for (int hh = 0; hh < MAX_GQA; ++hh) {
+          outp[k][hh][0] = A[hh].x;
+          outp[k][hh][1] = A[hh].y;
+          outp[k][hh][2] = A[hh].z;
+          outp[k][hh][3] = A[hh].w;
+        }
       }
     }
 #pragma unroll
@@ -972,15 +980,11 @@ struct Kernel {
       const bool hq = Lk[0][hh] > 0.f, hw = Lk[1][hh] > 0.f;
       if (hq) {
         // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
-        if (a.sinkhorn) {
-          const __half* sig = a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane;
-          q0 *= __half2float(sig[0]);
-          q1 *= __half2float(sig[1]);
-          q2 *= __half2float(sig[2]);
-          q3 *= __half2float(sig[3]);
-        }
+        q0 *= sv.x;
+        q1 *= sv.y;
+        q2 *= sv.z;
+        q3 *= sv.w;
         hadamard_warp(q0, q1, q2, q3, lane);
-        const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
         q0 *= C_WHT * sg.x;
         q1 *= C_WHT * sg.y;
         q2 *= C_WHT * sg.z;
@@ -1001,7 +1005,6 @@ struct Kernel {
     if (lane == 0) a.counters[u] = 0;  // ready for the next call
   }
 
-  // publish this warp's record for unit u; true if it was the unit's last arrival (which merges)
   // window accumulator of this warp's part of unit u into its record
   __device__ __forceinline__ void store_window_acc(int u, int gw, const QuantState& st) {
     float* dst = record(u, gw) + 16 + MAX_GQA * D + 4 * lane;
@@ -1028,12 +1031,13 @@ struct Kernel {
     const Pos pf = locate(xs, S_layer, B, H, sq);
     const Pos pl = locate(xe - 1, S_layer, B, H, sq);
     const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
-    // every lane makes its own record writes visible device-wide before lane 0 counts them
-    __threadfence();
+    // every lane orders its own record writes before the arrivals (release fence, then the warp
+    // barrier); lane j counts the warp's arrival at unit uf + j (+ 32 k), so the atomics are in
+    // flight together
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     __syncwarp();
-    if (lane != 0) return;
     int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
-    for (int u = uf; u <= ul; ++u) {
+    for (int u = uf + lane; u <= ul; u += 32) {
       const int h = u % H, b = (u / H) % B, ll = u / (H * B);
       if (sq.S[b] == 0) continue;  // no steps, no records
       int cf, nwu;
@@ -1043,13 +1047,13 @@ struct Kernel {
       if (old != nwu - 1) continue;
       const int slot = atomicAdd(mq + MQ_TAIL, 1);
       if (slot < MQ_CAP) {
-        // the records (acquired by the arrival above) before the queue entry that hands them on
-        __threadfence();
-        *reinterpret_cast<volatile int*>(mq + slot) = u;
+        // release: the records acquired by the arrival above go with the queue entry
+        asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot)), "r"(u) : "memory");
       } else {
         a.counters[a.n_units + u + gw] = 1;
       }
     }
+    __syncwarp();
   }
 
   // Drain the CTA's merge queue until every consumer warp of the CTA has ended its stream and the
@@ -1066,7 +1070,9 @@ struct Kernel {
         if (h < t) {
           if (atomicCAS(mq + MQ_HEAD, h, h + 1) == h) {
             const unsigned long long tw = globaltimer();
-            while ((u = vq[h]) < 0 && globaltimer() - tw < WAIT_NS) {}
+            do {
+              asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(u) : "r"(smem_addr(mq + h)) : "memory");
+            } while (u < 0 && globaltimer() - tw < WAIT_NS);
             if (u < 0) {
               atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
               stop = 1;
@@ -1086,7 +1092,7 @@ struct Kernel {
       u = __shfl_sync(FULL, u, 0);
       if (__shfl_sync(FULL, stop, 0)) break;
       if (u >= 0) {
-        __threadfence();
+        __syncwarp();  // the other lanes' record reads after lane 0's acquire
         merge(u);
         t0 = 0;
       }
