@@ -41,6 +41,7 @@ constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (w
 // and the number of consumer warps whose streams have ended.
 constexpr int MQ_CAP = 256;
 constexpr int MQ_TAIL = MQ_CAP, MQ_HEAD = MQ_CAP + 1, MQ_DONE = MQ_CAP + 2;
+constexpr int MQ_SKIP = -2;  // a taken slot with nothing to merge
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
@@ -873,12 +874,14 @@ struct Kernel {
     if (lane < 16) rec[lane] = v;
   }
 
-  // Combine the unit's partial records (one per warp that streamed part of it) in record order.
-  // Latency-bound, so the round trips are few: lane j reads both parts' headers of record j in
-  // one request (32 records at a time, with running maxima across chunks), weights are reduced in
-  // registers, then per part (quantised, window) the accumulators of four records holding the part
-  // (all heads) are requested together.  Runs once the merging warp's stream has ended.
-  __device__ __noinline__ void merge(int u) {
+  // Combine the partial records of query head hh of unit u (one record per warp that streamed part
+  // of the unit) in record order.  Latency-bound, so the round trips are few: lane j reads both
+  // parts' (m, l) of record j in one request (32 records at a time, with running maxima across
+  // chunks), weights are reduced in registers, then per part (quantised, window) the head's
+  // accumulators of up to eight records holding the part are requested together.  One head per
+  // call, so that the CTA's warps share a unit's merge.  Runs once the merging warp's stream has
+  // ended.
+  __device__ __noinline__ void merge(int u, int hh) {
     const int h = u % H, b = (u / H) % B, ll = u / (H * B);
     const int layer = a.layer0 + ll;
     int cf, nrec;
@@ -891,118 +894,86 @@ struct Kernel {
       const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
       sv = make_float4(s01.x, s01.y, s23.x, s23.y);
     }
-    float outp[2][MAX_GQA][4], Mk[2][MAX_GQA], Lk[2][MAX_GQA];
-#pragma unroll
-    for (int k = 0; k < 2; ++k)
-#pragma unroll
-      for (int hh = 0; hh < MAX_GQA; ++hh) {
-        Mk[k][hh] = -INFINITY;
-        Lk[k][hh] = 0.f;
-        outp[k][hh][0] = outp[k][hh][1] = outp[k][hh][2] = outp[k][hh][3] = 0.f;
-      }
+    float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
     for (int base = 0; base < nrec; base += 32) {
-      // both parts' headers of record base + lane, [Qm[4], Ql[4], Wm[4], Wl[4]], in one request
-      float4 hd[4] = {make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), make_float4(0.f, 0.f, 0.f, 0.f),
-                      make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY), make_float4(0.f, 0.f, 0.f, 0.f)};
+      // head hh's (m, l) of both parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
+      float hd[4] = {-INFINITY, 0.f, -INFINITY, 0.f};
       if (base + lane < nrec) {
-        const float4* hp = reinterpret_cast<const float4*>(record(u, cf + base + lane));
+        const float* hp = record(u, cf + base + lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + i);
+        for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + 4 * i + hh);
       }
       const int cnt = min(32, nrec - base);
 #pragma unroll
       for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
-        const float mv[4] = {hd[2 * k].x, hd[2 * k].y, hd[2 * k].z, hd[2 * k].w};
-        const float lv[4] = {hd[2 * k + 1].x, hd[2 * k + 1].y, hd[2 * k + 1].z, hd[2 * k + 1].w};
-        float f[MAX_GQA];
-        float4 A[MAX_GQA];
+        const float mv = hd[2 * k], lv = hd[2 * k + 1];
+        float m = lv > 0.f ? mv : -INFINITY;
 #pragma unroll
-        for (int hh = 0; hh < MAX_GQA; ++hh) {
-          float m = lv[hh] > 0.f ? mv[hh] : -INFINITY;
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+        const float mn = fmaxf(Mk[k], m);
+        const float sc = (Mk[k] == -INFINITY) ? 0.f : exp2f(Mk[k] - mn);  // rescale earlier chunks
+        Lk[k] *= sc;
+        float4 A = make_float4(O[k].x * sc, O[k].y * sc, O[k].z * sc, O[k].w * sc);
+        Mk[k] = mn;
+        const float f = lv > 0.f ? exp2f(mv - mn) : 0.f;
+        float lw = lv * f;
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-          const float mn = fmaxf(Mk[k][hh], m);
-          const float sc = (Mk[k][hh] == -INFINITY) ? 0.f : exp2f(Mk[k][hh] - mn);  // rescale earlier chunks
-          Lk[k][hh] *= sc;
-          A[hh] = make_float4(outp[k][hh][0] * sc, outp[k][hh][1] * sc, outp[k][hh][2] * sc, outp[k][hh][3] * sc);
-          Mk[k][hh] = mn;
-          f[hh] = lv[hh] > 0.f ? exp2f(mv[hh] - mn) : 0.f;
-          float lw = lv[hh] * f[hh];
-#pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
-          Lk[k][hh] += lw;
-        }
-        // only records with a part k (a window part is usually in one record of the unit), four
-        // records' accumulators requested before any is used
-        bool has = false;
-#pragma unroll
-        for (int hh = 0; hh < MAX_GQA; ++hh) has |= f[hh] > 0.f;
-        unsigned act = __ballot_sync(FULL, has && lane < cnt);
+        for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
+        Lk[k] += lw;
+        // only records with a part k for this head (a window part is usually in one record)
+        unsigned act = __ballot_sync(FULL, f > 0.f && lane < cnt);
         while (act) {
-          int jr[4];
-          float4 x[4][MAX_GQA];
+          int jr[8];
+          float4 x[8];
 #pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4) {
-            jr[r4] = act ? __ffs(act) - 1 : -1;
+          for (int r = 0; r < 8; ++r) {
+            jr[r] = act ? __ffs(act) - 1 : -1;
             act &= act - 1;
-            const float* rec = record(u, cf + base + max(jr[r4], 0)) + 16 + k * MAX_GQA * D + 4 * lane;
-#pragma unroll
-            for (int hh = 0; hh < MAX_GQA; ++hh)
-              x[r4][hh] = (hh < g && jr[r4] >= 0) ? __ldcg(reinterpret_cast<const float4*>(rec + hh * D))
-                                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float* rec = record(u, cf + base + max(jr[r], 0)) + 16 + (k * MAX_GQA + hh) * D + 4 * lane;
+            x[r] = jr[r] >= 0 ? __ldcg(reinterpret_cast<const float4*>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int r4 = 0; r4 < 4; ++r4)
-#pragma unroll
-            for (int hh = 0; hh < MAX_GQA; ++hh) {
-              const float fj = __shfl_sync(FULL, f[hh], max(jr[r4], 0));
-              if (jr[r4] >= 0 && fj > 0.f) {  // a head with no tokens in this part holds no accumulator
-                A[hh].x += fj * x[r4][hh].x;
-                A[hh].y += fj * x[r4][hh].y;
-                A[hh].z += fj * x[r4][hh].z;
-                A[hh].w += fj * x[r4][hh].w;
-              }
+          for (int r = 0; r < 8; ++r) {
+            const float fj = __shfl_sync(FULL, f, max(jr[r], 0));
+            if (jr[r] >= 0) {
+              A.x += fj * x[r].x;
+              A.y += fj * x[r].y;
+              A.z += fj * x[r].z;
+              A.w += fj * x[r].w;
             }
+          }
         }
-#pragma unroll
-        for (int hh = 0; hh < MAX_GQA; ++hh) {
-          outp[k][hh][0] = A[hh].x;
-          outp[k][hh][1] = A[hh].y;
-          outp[k][hh][2] = A[hh].z;
-          outp[k][hh][3] = A[hh].w;
-        }
+        O[k] = A;
       }
     }
-#pragma unroll
-    for (int hh = 0; hh < MAX_GQA; ++hh) {
-      if (hh >= g) break;
-      float q0 = outp[0][hh][0], q1 = outp[0][hh][1], q2 = outp[0][hh][2], q3 = outp[0][hh][3];
-      const bool hq = Lk[0][hh] > 0.f, hw = Lk[1][hh] > 0.f;
-      if (hq) {
-        // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
-        q0 *= sv.x;
-        q1 *= sv.y;
-        q2 *= sv.z;
-        q3 *= sv.w;
-        hadamard_warp(q0, q1, q2, q3, lane);
-        q0 *= C_WHT * sg.x;
-        q1 *= C_WHT * sg.y;
-        q2 *= C_WHT * sg.z;
-        q3 *= C_WHT * sg.w;
-      }
-      const float Mt = fmaxf(hq ? Mk[0][hh] : -INFINITY, hw ? Mk[1][hh] : -INFINITY);
-      const float f0 = hq ? exp2f(Mk[0][hh] - Mt) : 0.f;
-      const float f1 = hw ? exp2f(Mk[1][hh] - Mt) : 0.f;
-      const float den = Lk[0][hh] * f0 + Lk[1][hh] * f1;
-      const float inv = den > 0.f ? 1.f / den : 0.f;
-      float4 o;
-      o.x = (q0 * f0 + outp[1][hh][0] * f1) * inv;
-      o.y = (q1 * f0 + outp[1][hh][1] * f1) * inv;
-      o.z = (q2 * f0 + outp[1][hh][2] * f1) * inv;
-      o.w = (q3 * f0 + outp[1][hh][3] * f1) * inv;
-      *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * Hq + (size_t)h * g + hh) * D + 4 * lane) = o;
+    float q0 = O[0].x, q1 = O[0].y, q2 = O[0].z, q3 = O[0].w;
+    const bool hq = Lk[0] > 0.f, hw = Lk[1] > 0.f;
+    if (hq) {
+      // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
+      q0 *= sv.x;
+      q1 *= sv.y;
+      q2 *= sv.z;
+      q3 *= sv.w;
+      hadamard_warp(q0, q1, q2, q3, lane);
+      q0 *= C_WHT * sg.x;
+      q1 *= C_WHT * sg.y;
+      q2 *= C_WHT * sg.z;
+      q3 *= C_WHT * sg.w;
     }
-    if (lane == 0) a.counters[u] = 0;  // ready for the next call
+    const float Mt = fmaxf(hq ? Mk[0] : -INFINITY, hw ? Mk[1] : -INFINITY);
+    const float f0 = hq ? exp2f(Mk[0] - Mt) : 0.f;
+    const float f1 = hw ? exp2f(Mk[1] - Mt) : 0.f;
+    const float den = Lk[0] * f0 + Lk[1] * f1;
+    const float inv = den > 0.f ? 1.f / den : 0.f;
+    float4 o;
+    o.x = (q0 * f0 + O[1].x * f1) * inv;
+    o.y = (q1 * f0 + O[1].y * f1) * inv;
+    o.z = (q2 * f0 + O[1].z * f1) * inv;
+    o.w = (q3 * f0 + O[1].w * f1) * inv;
+    *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * Hq + (size_t)h * g + hh) * D + 4 * lane) = o;
+    // ready for the next call: the unit's counter is only read by the next launch
+    if (lane == 0 && hh == 0) a.counters[u] = 0;
   }
 
   // window accumulator of this warp's part of unit u into its record
@@ -1045,11 +1016,20 @@ struct Kernel {
       int old;
       asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
       if (old != nwu - 1) continue;
-      const int slot = atomicAdd(mq + MQ_TAIL, 1);
-      if (slot < MQ_CAP) {
-        // release: the records acquired by the arrival above go with the queue entry
-        asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot)), "r"(u) : "memory");
+      // one queue entry per query head, unit * MAX_GQA + head
+      const int slot = atomicAdd(mq + MQ_TAIL, g);
+      if (slot + g <= MQ_CAP) {
+        // release: the records acquired by the arrival above go with the queue entries
+        for (int hh = 0; hh < g; ++hh)
+          asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot + hh)), "r"(u * MAX_GQA + hh)
+                       : "memory");
       } else {
+        // no room for all of them: the unit is merged by this warp after its own loop, and the
+        // slots taken inside the queue are marked as empty for the other warps
+        for (int hh = 0; hh < g; ++hh)
+          if (slot + hh < MQ_CAP)
+            asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot + hh)), "r"(MQ_SKIP)
+                         : "memory");
         a.counters[a.n_units + u + gw] = 1;
       }
     }
@@ -1072,8 +1052,8 @@ struct Kernel {
             const unsigned long long tw = globaltimer();
             do {
               asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(u) : "r"(smem_addr(mq + h)) : "memory");
-            } while (u < 0 && globaltimer() - tw < WAIT_NS);
-            if (u < 0) {
+            } while (u == -1 && globaltimer() - tw < WAIT_NS);
+            if (u == -1) {
               atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
               stop = 1;
             }
@@ -1091,9 +1071,11 @@ struct Kernel {
       }
       u = __shfl_sync(FULL, u, 0);
       if (__shfl_sync(FULL, stop, 0)) break;
-      if (u >= 0) {
+      if (u == MQ_SKIP) {
+        t0 = 0;
+      } else if (u >= 0) {
         __syncwarp();  // the other lanes' record reads after lane 0's acquire
-        merge(u);
+        merge(u / MAX_GQA, u % MAX_GQA);
         t0 = 0;
       }
     }
@@ -1107,7 +1089,7 @@ struct Kernel {
     for (int u = uf; u <= ul; ++u) {
       int* flag = a.counters + a.n_units + u + gw;
       if (__ldcg(flag) != 0) {
-        merge(u);
+        for (int hh = 0; hh < g; ++hh) merge(u, hh);
         if (lane == 0) *flag = 0;
       }
     }

@@ -281,3 +281,29 @@ def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
             slots = np.arange(s1 - min(W, int(last_T[b])), s1) % W
             assert np.array_equal(rk[slots].view(np.uint32), ora.ring_k[0, b, h, slots].view(np.uint32))
             assert np.array_equal(rv[slots].view(np.uint32), ora.ring_v[0, b, h, slots].view(np.uint32))
+
+
+def test_many_tiny_units(gpu_lib):
+    """4096 (layer, sequence, kv-head) units of 0..5 tokens: far more units than warps, so warps
+    stream dozens of units each and the per-CTA merge queue overflows into the fallback path."""
+    w = synth.WORKLOADS["llama3.2-3b-32k"]
+    Lyr, H, Hq, B = 2, 4, 12, 512
+    lens = (np.arange(B) % 6).astype(np.int32)          # 0..5 tokens, window 4 (ring only for most)
+    gpu, ora, _ = harness.make_pair(Lyr, H, Hq, B, 64, window=4)
+    for l in range(Lyr):
+        k, v = _inputs(w, l, B, H, Hq, 5)
+        gpu.append(l, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+        ora.append(l, harness.to_np(k), harness.to_np(v), np.zeros(B, np.int64))
+    torch.cuda.synchronize()
+    q = torch.stack([synth.queries(w, l, B, Hq, device="cuda") for l in range(Lyr)]).contiguous()
+    sl = torch.as_tensor(lens, device="cuda")
+    out = gpu.decode(-1, q, sl)
+    torch.cuda.synchronize()
+    assert gpu.status() == 0
+    for l in range(Lyr):
+        want = ora.decode(l, harness.to_np(q[l]), lens)
+        harness.assert_attention_close(harness.to_np(out[l]), want)
+    # a second call on the same scratch (counters and flags must have been reset)
+    out2 = gpu.decode(-1, q, sl)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int32), out2.view(torch.int32))
