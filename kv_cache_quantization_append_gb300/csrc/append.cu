@@ -190,6 +190,8 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, uint32_t (&sb
 __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
   __shared__ uint32_t sbits[WARPS][12];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  // a dependent decode launch may start its set-up now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   const int nq = (a.T + VPW - 1) / VPW;
   // 32-bit index arithmetic: the launcher keeps the warp count below 2^31
   const unsigned total = (unsigned)a.n_layers_call * a.batch * a.Hkv * nq * a.kv_n;

@@ -36,6 +36,8 @@ constexpr float FAST_Q_LIMIT = 0.5f - 7.62939453125e-6f;  // 0.5 - 2^-17
 __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_constant__ AppendArgs a) {
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int G = lane & 3, tv = lane >> 2;  // group (channels 32G ..) and token of this lane
+  // a dependent decode launch may start its set-up now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
   const int H = a.Hkv, T = a.T;
   // grid: x = 8-position blocks of a sequence's call (8 per CTA), y = (layer, kv-head, K|V), z = sequence
   const int bi = blockIdx.x * BW + wl;

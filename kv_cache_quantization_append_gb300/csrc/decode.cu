@@ -999,20 +999,27 @@ struct Kernel {
   // (keeping the merge code out of the streaming loop and spreading the merges over the warps);
   // when the queue is full, it flags the unit for this warp to merge after its own loop.
   __device__ __noinline__ void arrive_units(int gw, long long xs, long long xe) {
+    // the index arithmetic first, while the record just written drains
     const Pos pf = locate(xs, S_layer, B, H, sq);
     const Pos pl = locate(xe - 1, S_layer, B, H, sq);
     const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
-    // every lane orders its own record writes before the arrivals (release fence, then the warp
-    // barrier); lane j counts the warp's arrival at unit uf + j (+ 32 k), so the atomics are in
-    // flight together
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
-    __syncwarp();
     int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
-    for (int u = uf + lane; u <= ul; u += 32) {
-      const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-      if (sq.S[b] == 0) continue;  // no steps, no records
-      int cf, nwu;
-      unit_owners(ll, b, h, cf, nwu);
+    for (int u0 = uf; u0 <= ul; u0 += 32) {
+      // lane j counts the warp's arrival at unit u0 + j, so the atomics are in flight together
+      const int u = u0 + lane;
+      int nwu = 0;
+      if (u <= ul) {
+        const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+        int cf;
+        if (sq.S[b] > 0) unit_owners(ll, b, h, cf, nwu);  // a sequence without steps has no records
+      }
+      if (u0 == uf) {
+        // every lane orders its own record writes before the arrivals (release fence, then the
+        // warp barrier)
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+      }
+      __syncwarp();
+      if (nwu == 0) continue;
       int old;
       asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
       if (old != nwu - 1) continue;
@@ -1102,6 +1109,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   using GE = Geo<KF>;
   constexpr int NCW = GE::NCW, NSTAGE = GE::NSTAGE, NTHREADS = GE::NTHREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // launched as a programmatic dependent: the previous kernel of the stream may still be running
+  // and writing the inputs (the cache, q, lengths); wait for it before reading any of them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   Kernel<KF> K(a, smem);
   const int tid = threadIdx.x;
   K.warp = tid >> 5;
@@ -1371,8 +1381,20 @@ static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem = Geo<KF>::SM_SEQ + 6 * (size_t)(a.batch + 1) * sizeof(int);
   cudaError_t e = cudaFuncSetAttribute(decode_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_kernel<KF><<<a.n_ctas, Geo<KF>::NTHREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs may be launched while the previous kernel of the
+  // stream (typically the append of the step's new tokens) is finishing; each waits for it
+  // (griddepcontrol.wait) before reading anything
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_ctas);
+  cfg.blockDim = dim3(Geo<KF>::NTHREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<KF>, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
