@@ -193,6 +193,21 @@ def bulk_append_bytes(w, layers, T) -> int:
     return layers * w["batch"] * w["n_kv_heads"] * per_seq_head
 
 
+def bench_config(name, w, layers, lens, world) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    cfg = {"workload": name, "layers": layers, "batch": int(w["batch"]),
+           "n_q_heads": w["n_q_heads"], "n_kv_heads": w["n_kv_heads"], "seq_len_sum": int(lens.sum()),
+           "window": w["window"], "k_format": w["k_format"], "v_format": w["v_format"],
+           "sinkhorn": bool(w["sinkhorn"]), "parallelism": f"replicas x{world}",
+           "l2": f"{algorithmic_bytes(w, layers, lens) / 1e9:.2f} GB of cache streamed each step (> 126 MB L2)"}
+    if layers < w["n_layers"]:
+        # only `layers` of the model's layers are allocated and timed; the whole-model step repeats
+        # the same per-layer work
+        cfg["timed_layers"] = layers
+        cfg["model_layers"] = w["n_layers"]
+    return cfg
+
+
 def algorithmic_bytes(w, layers, lens) -> int:
     """Bytes the decode step must move: packed records of the quantised tokens, the FP32 window,
     q and out (per launch over all layers)."""
@@ -348,11 +363,7 @@ def run_gpu(args):
             "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "q4/fp16-mma,f32-accum" if w["k_format"] == "q4g32" else "tq3+qjl/q4,f32-accum",
             "data": "synthetic (seeded N(0,1) with outlier channels, shapes of the workload; no weights)",
-            "config": {"workload": args.workload, "layers": layers, "batch": int(w["batch"]),
-                       "n_q_heads": Hq, "n_kv_heads": H, "seq_len_sum": int(lens.sum()),
-                       "window": w["window"], "k_format": w["k_format"], "v_format": w["v_format"],
-                       "sinkhorn": bool(w["sinkhorn"]), "parallelism": f"replicas x{world}",
-                       "l2": f"cache of {cache.buffer.numel() / 1e9:.2f} GB streamed each step (> 126 MB L2)"},
+            "config": bench_config(args.workload, w, layers, lens, world),
             "hbm_gbs": achieved,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_src,
@@ -369,8 +380,6 @@ def run_gpu(args):
             # only `layers` of the model's layers are allocated and timed; the whole-model step
             # repeats the same per-layer work
             f = w["n_layers"] / layers
-            result["config"]["timed_layers"] = layers
-            result["config"]["model_layers"] = w["n_layers"]
             result["value"] = value / f
             result["ms_per_step"] = ms_step * f
             result["us_per_step"] = ms_step * f * 1e3
@@ -414,11 +423,11 @@ def cpu_baseline(w, layers, lens, budget_s=12.0, max_units=3):
         tokens += L
         n += 1
     per_token_head = spent / tokens                      # seconds per (token, kv-head) attended
-    step_s = per_token_head * float(lens.sum()) * H * layers
+    step_s = per_token_head * float(lens.sum()) * H * w["n_layers"]  # the whole model's step
     return {"value": float(lens.sum()) / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
             "sample": f"numpy oracle decode of {len(units)} (layer, kv-head) units ({n} timed calls, "
-                      f"{spent:.1f} s), scaled by tokens to the {layers * len(lens) * H} units of one step; "
-                      f"their encode not timed; one thread"}
+                      f"{spent:.1f} s), scaled by tokens to the {w['n_layers'] * len(lens) * H} units of one "
+                      f"step; their encode not timed; one thread"}
 
 
 def run_reference(args):
@@ -439,7 +448,7 @@ def run_reference(args):
             "value": value, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64 attention, f32 codec", "data": "synthetic",
-            "config": {"workload": args.workload, "layers": layers, "batch": int(w["batch"])},
+            "config": bench_config(args.workload, w, layers, lens, 1),
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -462,7 +471,7 @@ def main():
         return
     res, cache, w, layers, lens = run_gpu(args)
     if res is not None:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and res["n_gpus"] == 1:
             res["cpu_baseline"] = cpu_baseline(w, layers, lens)
         print(json.dumps(res))
 

@@ -114,30 +114,34 @@ __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_co
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const float4 s = sg[c];
-      x[4 * c] = __fmul_rn(x[4 * c], s.x);
-      x[4 * c + 1] = __fmul_rn(x[4 * c + 1], s.y);
-      x[4 * c + 2] = __fmul_rn(x[4 * c + 2], s.z);
-      x[4 * c + 3] = __fmul_rn(x[4 * c + 3], s.w);
+      mul2(x[4 * c], x[4 * c + 1], s.x, s.y);
+      mul2(x[4 * c + 2], x[4 * c + 3], s.z, s.w);
     }
   }
+  // stage h = 1 pairs neighbours (scalar); stages h = 2 .. 16 pair (j, j+1) with (j+h, j+h+1)
 #pragma unroll
-  for (int hs = 1; hs < 32; hs <<= 1) {
+  for (int j = 0; j < 32; j += 2) {
+    const float u = x[j], v = x[j + 1];
+    x[j] = __fadd_rn(u, v);
+    x[j + 1] = __fsub_rn(u, v);
+  }
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+  for (int hs = 2; hs < 32; hs <<= 1) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
       if (j & hs) continue;
-      const float u = x[j], v = x[j + hs];
-      x[j] = __fadd_rn(u, v);
-      x[j + hs] = __fsub_rn(u, v);
+      bfly2(x[j], x[j + 1], x[j + hs], x[j + hs + 1]);
     }
   }
 #pragma unroll
   for (int m = 1; m <= 2; m <<= 1) {  // h = 32 m: partner lane G ^ m holds the other channel
     const float sg = (G & m) ? -1.0f : 1.0f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) x[j] = __fmaf_rn(x[j], sg, __shfl_xor_sync(FULL, x[j], m));
+    for (int j = 0; j < 32; j += 2)
+      fma2(x[j], x[j + 1], sg, sg, __shfl_xor_sync(FULL, x[j], m), __shfl_xor_sync(FULL, x[j + 1], m));
   }
 #pragma unroll
-  for (int j = 0; j < 32; ++j) x[j] = __fmul_rn(x[j], C_WHT);
+  for (int j = 0; j < 32; j += 2) mul2(x[j], x[j + 1], C_WHT, C_WHT);
   if (a.sinkhorn) {
     const __half2* sg = reinterpret_cast<const __half2*>((kv ? a.p.sigv : a.p.sigk) + ((size_t)layer * H + h) * D + 32 * G);
 #pragma unroll
@@ -165,21 +169,33 @@ __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_co
   const float s = __half2float(s16), z = __half2float(z16);
   const float inv = __frcp_rn(s);
   uint32_t w[4];  // nibble m of w[i] = code of channel 32G + 8i + m
-  bool redo = false;
+  float dmax = 0.f;   // largest distance of a quotient from its rounded integer
+  uint32_t cmax = 0;  // largest code (as unsigned: a negative one wraps to a huge value)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t word = 0;
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const float qt = __fmul_rn(__fsub_rn(x[8 * i + m], z), inv);
-      const float t = __fadd_rn(qt, RINT_MAGIC);
-      const float r = __fsub_rn(t, RINT_MAGIC);
-      const uint32_t c = __float_as_uint(t) - __float_as_uint(RINT_MAGIC);
-      redo |= (fabsf(__fsub_rn(qt, r)) > FAST_Q_LIMIT) | (c > 15u);
-      word |= c << (4 * m);
+    for (int m = 0; m < 8; m += 2) {
+      // qt = (y - z) * inv, t = qt + 1.5 * 2^23, r = t - 1.5 * 2^23, d = qt - r: pairwise
+      float q0 = x[8 * i + m], q1 = x[8 * i + m + 1];
+      sub2(q0, q1, z, z);
+      mul2(q0, q1, inv, inv);
+      float t0 = q0, t1 = q1;
+      add2(t0, t1, RINT_MAGIC, RINT_MAGIC);
+      float r0 = t0, r1 = t1;
+      sub2(r0, r1, RINT_MAGIC, RINT_MAGIC);
+      float d0 = q0, d1 = q1;
+      sub2(d0, d1, r0, r1);
+      const uint32_t c0 = __float_as_uint(t0) - __float_as_uint(RINT_MAGIC);
+      const uint32_t c1 = __float_as_uint(t1) - __float_as_uint(RINT_MAGIC);
+      dmax = fmaxf(dmax, fmaxf(fabsf(d0), fabsf(d1)));
+      cmax = max(cmax, max(c0, c1));
+      word += (c0 + (c1 << 4)) << (4 * m);  // disjoint nibbles while both codes are in range
     }
     w[i] = word;
   }
+  // a NaN quotient (never with a positive scale and finite inputs) shows up as a huge code
+  const bool redo = dmax > FAST_Q_LIMIT || cmax > 15u;
   if (!(s > 0.0f)) {
     w[0] = w[1] = w[2] = w[3] = 0u;
   } else if (redo && valid) {

@@ -116,6 +116,47 @@ __device__ __forceinline__ float4 load4_in(const void* base, size_t elem_off, in
   return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem_off);
 }
 
+// Packed pairs of IEEE fp32 operations (sm_100+ `add/sub/mul/fma.rn.f32x2`): each half is rounded
+// exactly like the scalar __fadd_rn / __fsub_rn / __fmul_rn / __fmaf_rn, two values per instruction.
+__device__ __forceinline__ unsigned long long pk2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(unsigned long long r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)));
+  up2(r, a0, a1);
+}
+__device__ __forceinline__ void sub2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)));
+  up2(r, a0, a1);
+}
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)));
+  up2(r, a0, a1);
+}
+// a = a * b + c, pairwise
+__device__ __forceinline__ void fma2(float& a0, float& a1, float b0, float b1, float c0, float c1) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk2(a0, a1)), "l"(pk2(b0, b1)), "l"(pk2(c0, c1)));
+  up2(r, a0, a1);
+}
+// butterfly of two pairs: (a, b) -> (a + b, a - b), element by element
+__device__ __forceinline__ void bfly2(float& a0, float& a1, float& b0, float& b1) {
+  const float u0 = a0, u1 = a1;
+  add2(a0, a1, b0, b1);
+  float d0 = u0, d1 = u1;
+  sub2(d0, d1, b0, b1);
+  b0 = d0;
+  b1 = d1;
+}
+
 // Unnormalised Hadamard butterfly over a warp: lane l holds elements 4l..4l+3.  Stages
 // h = 1, 2 inside the lane, h = 4..64 across lanes (xor 1..16); every add/sub rounds once.
 __device__ __forceinline__ void hadamard_warp(float& x0, float& x1, float& x2, float& x3, int lane) {
