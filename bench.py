@@ -223,6 +223,25 @@ def algorithmic_bytes(w, layers, lens) -> int:
     return per_layer * layers
 
 
+# ------------------------------------------------------------------ ranks
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over the ranks of the default process group (x itself without one):
+    every rank's timed region ends when the slowest rank's does."""
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_step_per_rank: float, world: int, ms_per_step_max: float) -> float:
+    """Whole-job throughput: the cached tokens every rank's replica attends per step, summed over
+    the ranks, over the slowest rank's time per step."""
+    return tokens_per_step_per_rank * world / (ms_per_step_max / 1e3)
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
@@ -276,12 +295,8 @@ def run_gpu(args):
             cache.decode(-1, qs[i % nbuf], seq, out)
             ev[i][1].record(stream)
         torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), dev)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
     if cache.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
@@ -305,11 +320,7 @@ def run_gpu(args):
         out_h.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     # bulk (prefill-sized) append, timed on its own after the decode measurements: the workload's
     # prefill chunk written at the end of every sequence where the workload names one (the cache has
@@ -347,9 +358,9 @@ def run_gpu(args):
                   "kernel": "append_bulk_kernel" + (" + append_kernel (TQ3 keys)" if w["k_format"] == "tq3_qjl" else "")}
     del kc, vc
 
-    tokens_per_step = float(lens.sum()) * world   # sequence lengths summed; every layer attends them
+    tokens_per_rank = float(lens.sum())  # sequence lengths summed; every layer attends them
     ms_step = total_ms / args.steps
-    value = tokens_per_step / (ms_step / 1e3)
+    value = weak_scaling_value(tokens_per_rank, world, ms_step)
     alg = algorithmic_bytes(w, layers, lens)
     dec_avg_s = statistics.mean(dec_ms) / 1e3
     peak, peak_src = hbm_peak()
@@ -370,7 +381,7 @@ def run_gpu(args):
                          "traffic": traffic, "algorithmic_bytes_per_launch": alg,
                          "kernel": "decode_kernel (all layers, one launch)",
                          "decode_us_avg": dec_avg_s * 1e6},
-            "e2e": {"value": tokens_per_step / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
+            "e2e": {"value": weak_scaling_value(tokens_per_rank, world, e2e_ms / args.steps), "unit": "tokens/s",
                     "h2d_bytes_per_step": int(qs[0].numel() * qs[0].element_size() + 2 * knew.numel() * knew.element_size()),
                     "d2h_bytes_per_step": int(out.numel() * 4), "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": 2 * args.steps,
