@@ -176,11 +176,12 @@ int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* 
  *              j / (n_q_heads / n_kv_heads)
  *   out        device float [L?][batch][n_q_heads][128]
  *   seq_lens   device int32 [batch]
- *   scratch    device, >= kv_decode_scratch_bytes(cache, layer, batch) bytes, zero-filled before
- *              its first use; every successful call leaves its counters at zero again.  Calls
- *              that share a scratch buffer must not overlap on the GPU.
- * Splits the token axis over all SMs, runs a bulk-copy pipeline per SM and merges the partial
- * softmax states inside the same launch; results do not depend on timing (fixed merge order).
+ *   scratch    device, >= kv_decode_scratch_bytes(cache, layer, batch) bytes, any contents
+ *              (every call writes what it reads).  Calls that share a scratch buffer must not
+ *              overlap on the GPU.
+ * Splits the token axis over all SMs and runs a bulk-copy pipeline per SM (one launch); a second,
+ * small launch on the same stream merges the partial softmax states.  Results do not depend on
+ * timing (fixed merge order).
  */
 size_t kv_decode_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t batch);
 int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* out,
@@ -198,9 +199,8 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
  *     return KVQ_ERR_CAPACITY and launch nothing.
  *   - The first call on a device looks up the array's device address (once per device, with that
  *     device current); make that first call before any stream capture.
- *   - Every call shares the one array: the call clears the arrival counters it needs on ``stream``
- *     before its kernel, but calls that overlap on the GPU (other streams, other host threads)
- *     race on the array and must be serialised by the caller.
+ *   - Every call shares the one array: calls that overlap on the GPU (other streams, other host
+ *     threads) race on it and must be serialised by the caller.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.
  */
 #define KVQ_NOALLOC_SCRATCH_MAX (32u * 1024u * 1024u)

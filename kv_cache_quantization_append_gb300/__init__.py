@@ -30,12 +30,12 @@ class QuantKVCache:
         self._scratch = {}
 
     def scratch(self, layer: int, batch: int) -> torch.Tensor:
-        """Zero-filled decode scratch, kept per (layer-mode, batch) and reused across calls."""
+        """Decode scratch (uninitialised), kept per (layer-mode, batch) and reused across calls."""
         key = (layer == -1, batch)
         need = kv_decode_scratch_bytes(self.handle, layer, batch)
         t = self._scratch.get(key)
         if t is None or t.numel() < need:
-            t = torch.zeros(need, dtype=torch.uint8, device=self.buffer.device)
+            t = torch.empty(need, dtype=torch.uint8, device=self.buffer.device)
             self._scratch[key] = t
         return t
 

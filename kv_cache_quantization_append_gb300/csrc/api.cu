@@ -316,10 +316,9 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   a.q = q;
   a.out = out;
   a.seq_lens = seq_lens;
-  a.counters = static_cast<int*>(scratch);
-  // scratch: arrival counters [n_units], merge flags [n_units + warps], partial records
-  const size_t slots = (size_t)n_units + (size_t)ctas * decode_consumer_warps(cache->cfg.k_format);
-  a.records = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256(((size_t)n_units + slots) * sizeof(int)));
+  // scratch: record ranges int2 [n_units], then the partial records
+  a.unit_info = static_cast<int2*>(scratch);
+  a.records = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + align256((size_t)n_units * sizeof(int2)));
   a.layer0 = l0;
   a.n_layers_call = nl;
   a.batch = batch;
@@ -332,6 +331,7 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   a.in_bf16 = cache->cfg.in_dtype == KVQ_IN_BF16;
   a.max_batch = cache->cfg.max_batch;
   a.max_pages_per_seq = cache->max_pages_per_seq;
+  a.identity_pages = cache->block_table == reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(cache->dev) + L.off_bt);
   a.n_units = n_units;
   a.n_ctas = ctas;
   return cuda_err(launch_decode(a, static_cast<cudaStream_t>(stream)));

@@ -6,24 +6,26 @@
 // where tokens t < L - window are read from the packed pages and scored in rotated space
 // (q~ = c H (s . q) [. sigma_k]), and the last `window` tokens come raw from the FP32 ring.
 //
-// Design for GB300 (one CTA per SM: 11 consumer warps + 1 producer warp):
+// Design for GB300 (one CTA per SM: 15 consumer warps for Q4G32 keys, 11 for TQ3 keys, + 1
+// producer warp):
 //  * The work of a call is a list of "steps" -- one 32-token half-page or one 4-slot window chunk
 //    of one (layer, sequence, kv-head) unit, window chunks first.
-//  * The list is cut into equal contiguous ranges, one per consumer warp of every CTA (stream-K
-//    at warp granularity), so every warp streams the same bytes whatever the sequence lengths and
-//    touches only one to a few units.  Consumer warp w owns NSLOT shared-memory stages (slots
-//    w + 11 k); lane w of the producer warp streams exactly that warp's range with cp.async.bulk
-//    (the 1D TMA path) completing on mbarriers.  Every wait gives up after ~1 s and sets a status
-//    bit.
+//  * The list is cut into contiguous ranges of equal cost, one per consumer warp of every CTA
+//    (stream-K at warp granularity), so every warp streams about the same bytes whatever the
+//    sequence lengths and touches only one to a few units.  Consumer warp w owns NSLOT
+//    shared-memory stages (slots w + NCW k); lane w of the producer warp streams exactly that
+//    warp's range with cp.async.bulk (the 1D TMA path) completing on mbarriers.  Every wait gives
+//    up after ~1 s and sets a status bit.
 //  * Consumer warps turn nibbles into exact fp16 values in registers (a nibble read as an FP8 E4M3
 //    bit pattern is c * 2^-9; the 2^9 is folded into q) and run the logits and P.V as tensor-core
 //    mma.sync m16n8k16 (fp32 accumulate): GQA query heads are the N axis (hi and lo halves of q
 //    in adjacent columns), per-group scales and zero points are folded out of the products.
 //  * Each warp keeps an online-softmax state per unit and, when it leaves the unit, writes a
-//    partial record (max, sum, accumulator) to scratch and bumps the unit's arrival counter; the
-//    last arrival marks the unit, and after its streaming loop the warp merges the units it marked
-//    from their records in a fixed order (deterministic), undoes the rotation of the quantised
-//    part and combines it with the window part.  No spin-wait on other CTAs.
+//    partial record (max, sum, accumulator) to scratch.  A second, small kernel, launched as a
+//    programmatic dependent of the first (it starts as the streaming grid completes), merges each
+//    query head's records in a fixed order (deterministic), undoes the rotation of the quantised
+//    part and combines it with the window part.  No inter-CTA flags, fences or atomics inside the
+//    streaming kernel.
 #include <cfloat>
 
 #include "kvq_internal.cuh"
@@ -37,11 +39,7 @@ constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
-// Per-CTA queue of units ready to merge: [MQ_CAP] unit ids (-1 = not yet written), then tail, head
-// and the number of consumer warps whose streams have ended.
-constexpr int MQ_CAP = 256;
-constexpr int MQ_TAIL = MQ_CAP, MQ_HEAD = MQ_CAP + 1, MQ_DONE = MQ_CAP + 2;
-constexpr int MQ_SKIP = -2;  // a taken slot with nothing to merge
+constexpr int MERGE_WARPS = 8;  // warps per CTA of the merge kernel, one query head each
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
@@ -73,8 +71,8 @@ struct Geo {
   static constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                      // [64][32] u32 (TQ)
   static constexpr int SM_P = SM_LUT + (TQ ? 64 * 32 * 4 : 0);               // [NCW][2][4][32] fp16
   static constexpr int SM_WML = SM_P + NCW * 2 * MAX_GQA * HALF * 2;         // [NCW][8] float
-  static constexpr int SM_MQ = SM_WML + NCW * 8 * 4;                         // merge queue
-  static constexpr int SM_SEQ = SM_MQ + (MQ_CAP + 4) * 4;                     // 6 int[batch+1]
+  static constexpr int SM_WPOS = SM_WML + NCW * 8 * 4;                       // [NCW+1] int4, i64
+  static constexpr int SM_SEQ = SM_WPOS + (NCW + 1) * 24;                     // 6 int[batch+1]
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -172,6 +170,12 @@ __device__ __forceinline__ uint32_t split_pick(float v, bool lo) {
   return lo ? (uint32_t)__half_as_ushort(__float2half_rn(v - __half2float(hi))) : (uint32_t)__half_as_ushort(hi);
 }
 
+// floor(n / d) for n >= 0, d > 0: a 32-bit division when both fit (the usual case), else 64-bit
+__device__ __forceinline__ long long div_nn(long long n, long long d) {
+  if (((unsigned long long)n | (unsigned long long)d) < 0x80000000ull) return (long long)((unsigned)n / (unsigned)d);
+  return n / d;
+}
+
 struct Seq {
   const int* S;     // steps per sequence
   const int* pre;   // exclusive prefix of S, [batch + 1]
@@ -194,23 +198,6 @@ constexpr int SPEED_NORMAL = 10, SPEED_FAST = 11;
 struct Pos {
   int ll, b, h, local;
 };
-
-__device__ __forceinline__ Pos locate(long long x, long long S_layer, int B, int H, const Seq& sq) {
-  Pos p;
-  p.ll = (int)(x / S_layer);
-  const long long r = x - (long long)p.ll * S_layer;
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if ((long long)H * sq.pre[mid] <= r) lo = mid;
-    else hi = mid - 1;
-  }
-  p.b = lo;
-  const int r2 = (int)(r - (long long)H * sq.pre[lo]);
-  p.h = r2 / sq.S[lo];
-  p.local = r2 - p.h * sq.S[lo];
-  return p;
-}
 
 // move a position forward by `by` steps (only called while the target step exists)
 __device__ __forceinline__ void advance(Pos& p, int by, int B, int H, const Seq& sq) {
@@ -248,6 +235,13 @@ struct WinState {
   float* ml;
 };
 
+// Partial record of (unit u, global consumer warp gw): [header 16][quantised acc MAX_GQA][128]
+// [window acc MAX_GQA][128] floats.  The index u + gw is unique because both the units and the
+// warps' step ranges are ordered along the step list.
+__device__ __forceinline__ float* record_at(const DecodeArgs& a, int u, int gw) {
+  return a.records + (size_t)(u + gw) * REC_FLOATS;
+}
+
 template <int KF>
 struct Kernel {
   using GE = Geo<KF>;
@@ -282,7 +276,7 @@ struct Kernel {
   __device__ __forceinline__ long long speed_before(long long g) const {
     return (g / NCW) * speed_prefix(NCW) + speed_prefix((int)(g % NCW));
   }
-  __device__ __forceinline__ long long lb(long long g) const { return C * speed_before(g) / SPtot; }
+  __device__ __forceinline__ long long lb(long long g) const { return div_nn(C * speed_before(g), SPtot); }
   __device__ __forceinline__ long long cost_at(int ll, int b, int h, int local) const {
     long long c = (long long)ll * C_layer + (long long)H * sq.cpre[b] + (long long)h * sq.C[b];
     if (local > 0) {
@@ -294,7 +288,7 @@ struct Kernel {
   // warp whose cost range holds cost position c: the last g with speed_before(g) <= T, where
   // lb(g) <= c  <=>  speed_before(g) <= T = floor(((c + 1) SPtot - 1) / C)
   __device__ __forceinline__ int owner(long long c) const {
-    const long long T = ((c + 1) * SPtot - 1) / C;
+    const long long T = div_nn((c + 1) * SPtot - 1, C);
     const long long scta = speed_prefix(NCW);
     const long long cta = T / scta, rem = T - cta * scta;
     int w = NCW - 1;
@@ -309,7 +303,7 @@ struct Kernel {
   __device__ Pos first_step(long long gw) const {
     const long long y = lb(gw);
     Pos p;
-    p.ll = (int)(y / C_layer);
+    p.ll = (int)div_nn(y, C_layer);
     const long long r = y - (long long)p.ll * C_layer;
     int lo = 0, hi = B - 1;
     while (lo < hi) {
@@ -319,13 +313,23 @@ struct Kernel {
     }
     p.b = lo;
     const long long r2 = r - (long long)H * sq.cpre[lo];
-    p.h = (int)(r2 / sq.C[lo]);
+    p.h = (int)div_nn(r2, sq.C[lo]);
     const int r3 = (int)(r2 - (long long)p.h * sq.C[lo]);
     const int nwin = sq.NW[lo];
     p.local = (r3 < COST_UNIT + nwin * COST_WIN) ? max(0, r3 - COST_UNIT) / COST_WIN
                                                  : nwin + (r3 - COST_UNIT - nwin * COST_WIN) / COST_Q;
     if (cost_at(p.ll, p.b, p.h, p.local) < y) advance(p, 1, B, H, sq);
     return p;
+  }
+  // This thread's share (index i of the grid's NCW * 32 * gridDim consumer threads) of the record
+  // ranges of all units, for the merge kernel (a unit of an empty sequence has none)
+  __device__ void unit_info_share(long long i) const {
+    for (long long u = i; u < a.n_units; u += (long long)NCW * 32 * gridDim.x) {
+      const int h = (int)(u % H), b = (int)((u / H) % B), ll = (int)(u / ((long long)H * B));
+      int2 info = make_int2(0, 0);
+      if (sq.S[b] > 0) unit_owners(ll, b, h, info.x, info.y);
+      a.unit_info[u] = info;
+    }
   }
   // [first, last] cost positions of unit u's steps' starts, as owner() arguments
   __device__ __forceinline__ void unit_owners(int ll, int b, int h, int& first, int& count) const {
@@ -806,12 +810,8 @@ struct Kernel {
     __syncwarp();
   }
 
-  // ---------------------------------------------------------------- records and merge
-  // partial record of (unit u, global warp gw): the index u + gw is unique because both the units
-  // and the warps' step ranges are ordered along the step list
-  __device__ __forceinline__ float* record(int u, int gw) const {
-    return a.records + (size_t)(u + gw) * REC_FLOATS;
-  }
+  // ---------------------------------------------------------------- records
+  __device__ __forceinline__ float* record(int u, int gw) const { return record_at(a, u, gw); }
 
   __device__ void write_quant(float* rec, QuantState& st) {
     const int r = lane >> 2, i = lane & 3;
@@ -874,108 +874,6 @@ struct Kernel {
     if (lane < 16) rec[lane] = v;
   }
 
-  // Combine the partial records of query head hh of unit u (one record per warp that streamed part
-  // of the unit) in record order.  Latency-bound, so the round trips are few: lane j reads both
-  // parts' (m, l) of record j in one request (32 records at a time, with running maxima across
-  // chunks), weights are reduced in registers, then per part (quantised, window) the head's
-  // accumulators of up to eight records holding the part are requested together.  One head per
-  // call, so that the CTA's warps share a unit's merge.  Runs once the merging warp's stream has
-  // ended.
-  __device__ __noinline__ void merge(int u, int hh) {
-    const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-    const int layer = a.layer0 + ll;
-    int cf, nrec;
-    unit_owners(ll, b, h, cf, nrec);
-    // constants of the output phase, requested first
-    const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
-    float4 sv = make_float4(1.f, 1.f, 1.f, 1.f);
-    if (a.sinkhorn) {
-      const __half2* sig = reinterpret_cast<const __half2*>(a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane);
-      const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
-      sv = make_float4(s01.x, s01.y, s23.x, s23.y);
-    }
-    float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-    float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
-    for (int base = 0; base < nrec; base += 32) {
-      // head hh's (m, l) of both parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
-      float hd[4] = {-INFINITY, 0.f, -INFINITY, 0.f};
-      if (base + lane < nrec) {
-        const float* hp = record(u, cf + base + lane);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + 4 * i + hh);
-      }
-      const int cnt = min(32, nrec - base);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
-        const float mv = hd[2 * k], lv = hd[2 * k + 1];
-        float m = lv > 0.f ? mv : -INFINITY;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
-        const float mn = fmaxf(Mk[k], m);
-        const float sc = (Mk[k] == -INFINITY) ? 0.f : exp2f(Mk[k] - mn);  // rescale earlier chunks
-        Lk[k] *= sc;
-        float4 A = make_float4(O[k].x * sc, O[k].y * sc, O[k].z * sc, O[k].w * sc);
-        Mk[k] = mn;
-        const float f = lv > 0.f ? exp2f(mv - mn) : 0.f;
-        float lw = lv * f;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
-        Lk[k] += lw;
-        // only records with a part k for this head (a window part is usually in one record)
-        unsigned act = __ballot_sync(FULL, f > 0.f && lane < cnt);
-        while (act) {
-          int jr[8];
-          float4 x[8];
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            jr[r] = act ? __ffs(act) - 1 : -1;
-            act &= act - 1;
-            const float* rec = record(u, cf + base + max(jr[r], 0)) + 16 + (k * MAX_GQA + hh) * D + 4 * lane;
-            x[r] = jr[r] >= 0 ? __ldcg(reinterpret_cast<const float4*>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int r = 0; r < 8; ++r) {
-            const float fj = __shfl_sync(FULL, f, max(jr[r], 0));
-            if (jr[r] >= 0) {
-              A.x += fj * x[r].x;
-              A.y += fj * x[r].y;
-              A.z += fj * x[r].z;
-              A.w += fj * x[r].w;
-            }
-          }
-        }
-        O[k] = A;
-      }
-    }
-    float q0 = O[0].x, q1 = O[0].y, q2 = O[0].z, q3 = O[0].w;
-    const bool hq = Lk[0] > 0.f, hw = Lk[1] > 0.f;
-    if (hq) {
-      // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
-      q0 *= sv.x;
-      q1 *= sv.y;
-      q2 *= sv.z;
-      q3 *= sv.w;
-      hadamard_warp(q0, q1, q2, q3, lane);
-      q0 *= C_WHT * sg.x;
-      q1 *= C_WHT * sg.y;
-      q2 *= C_WHT * sg.z;
-      q3 *= C_WHT * sg.w;
-    }
-    const float Mt = fmaxf(hq ? Mk[0] : -INFINITY, hw ? Mk[1] : -INFINITY);
-    const float f0 = hq ? exp2f(Mk[0] - Mt) : 0.f;
-    const float f1 = hw ? exp2f(Mk[1] - Mt) : 0.f;
-    const float den = Lk[0] * f0 + Lk[1] * f1;
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    float4 o;
-    o.x = (q0 * f0 + O[1].x * f1) * inv;
-    o.y = (q1 * f0 + O[1].y * f1) * inv;
-    o.z = (q2 * f0 + O[1].z * f1) * inv;
-    o.w = (q3 * f0 + O[1].w * f1) * inv;
-    *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * Hq + (size_t)h * g + hh) * D + 4 * lane) = o;
-    // ready for the next call: the unit's counter is only read by the next launch
-    if (lane == 0 && hh == 0) a.counters[u] = 0;
-  }
-
   // window accumulator of this warp's part of unit u into its record
   __device__ __forceinline__ void store_window_acc(int u, int gw, const QuantState& st) {
     float* dst = record(u, gw) + 16 + MAX_GQA * D + 4 * lane;
@@ -984,7 +882,7 @@ struct Kernel {
       *reinterpret_cast<float4*>(dst + k * D) = make_float4(st.acc[k][0], st.acc[k][1], st.acc[k][2], st.acc[k][3]);
   }
 
-  // Write this warp's record of unit u (its arrival is counted after the warp's stream ends).
+  // Write this warp's record of unit u (read by the merge kernel once this grid has ended).
   __device__ void finish_unit(int u, int gw, int kind, bool hasq, bool hasw, QuantState& st, WinState& ws) {
     float* rec = record(u, gw);
     if (kind == KIND_QUANT) write_quant(rec, st);
@@ -992,117 +890,129 @@ struct Kernel {
     write_header(rec, hasq, st, hasw, ws);
   }
 
-  // Count this warp's arrival at each unit of steps [xs, xe) (their records are written).  No part
-  // of a unit this warp leaves early completes before the warp's stream ends anyway: the other
-  // warps of the unit end their parts at the ends of their own ranges.  The last arrival queues
-  // the unit on the CTA's merge queue, which all the CTA's warps drain once their streams end
-  // (keeping the merge code out of the streaming loop and spreading the merges over the warps);
-  // when the queue is full, it flags the unit for this warp to merge after its own loop.
-  __device__ __noinline__ void arrive_units(int gw, long long xs, long long xe) {
-    // the index arithmetic first, while the record just written drains
-    const Pos pf = locate(xs, S_layer, B, H, sq);
-    const Pos pl = locate(xe - 1, S_layer, B, H, sq);
-    const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
-    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
-    for (int u0 = uf; u0 <= ul; u0 += 32) {
-      // lane j counts the warp's arrival at unit u0 + j, so the atomics are in flight together
-      const int u = u0 + lane;
-      int nwu = 0;
-      if (u <= ul) {
-        const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-        int cf;
-        if (sq.S[b] > 0) unit_owners(ll, b, h, cf, nwu);  // a sequence without steps has no records
-      }
-      if (u0 == uf) {
-        // every lane orders its own record writes before the arrivals (release fence, then the
-        // warp barrier)
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-      }
-      __syncwarp();
-      if (nwu == 0) continue;
-      int old;
-      asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(a.counters + u) : "memory");
-      if (old != nwu - 1) continue;
-      // one queue entry per query head, unit * MAX_GQA + head
-      const int slot = atomicAdd(mq + MQ_TAIL, g);
-      if (slot + g <= MQ_CAP) {
-        // release: the records acquired by the arrival above go with the queue entries
-        for (int hh = 0; hh < g; ++hh)
-          asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot + hh)), "r"(u * MAX_GQA + hh)
-                       : "memory");
-      } else {
-        // no room for all of them: the unit is merged by this warp after its own loop, and the
-        // slots taken inside the queue are marked as empty for the other warps
-        for (int hh = 0; hh < g; ++hh)
-          if (slot + hh < MQ_CAP)
-            asm volatile("st.release.cta.shared::cta.s32 [%0], %1;" ::"r"(smem_addr(mq + slot + hh)), "r"(MQ_SKIP)
-                         : "memory");
-        a.counters[a.n_units + u + gw] = 1;
-      }
-    }
-    __syncwarp();
-  }
+};
 
-  // Drain the CTA's merge queue until every consumer warp of the CTA has ended its stream and the
-  // queue is empty; gives up (status bit) after ~1 s without either.
-  __device__ __noinline__ void drain_merges(int nact) {
-    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
-    volatile int* vq = mq;
-    unsigned long long t0 = 0;
-    while (true) {
-      int u = -1, stop = 0;
-      if (lane == 0) {
-        const int h = vq[MQ_HEAD];
-        const int t = min(vq[MQ_TAIL], MQ_CAP);
-        if (h < t) {
-          if (atomicCAS(mq + MQ_HEAD, h, h + 1) == h) {
-            const unsigned long long tw = globaltimer();
-            do {
-              asm volatile("ld.acquire.cta.shared::cta.s32 %0, [%1];" : "=r"(u) : "r"(smem_addr(mq + h)) : "memory");
-            } while (u == -1 && globaltimer() - tw < WAIT_NS);
-            if (u == -1) {
-              atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
-              stop = 1;
-            }
-          }
-        } else if (vq[MQ_DONE] >= nact && vq[MQ_HEAD] >= min(vq[MQ_TAIL], MQ_CAP)) {
-          stop = 1;
-        } else {
-          if (t0 == 0) t0 = globaltimer();
-          if (globaltimer() - t0 > WAIT_NS) {
-            atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
-            stop = 1;
-          }
-          __nanosleep(128);
+// Combine the partial records of query head hh of unit u (records cf .. cf + nrec - 1, one per
+// warp that streamed part of the unit) in record order and write the head's output.  Latency-bound,
+// so the round trips are few: the unit's record range; then lane j reads both parts' (m, l) of
+// record j (32 records at a time, with running maxima across chunks) and the weights are reduced
+// in registers; then the head's accumulators of every record that holds a part (quantised, window)
+// are requested together, up to MERGE_BATCH per round, and summed per part in record order.  A
+// unit without records (empty sequence) gets zeros.
+constexpr int MERGE_BATCH = 16;
+__device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
+  const int H = a.Hkv, B = a.batch, g = a.g;
+  const int h = u % H, b = (u / H) % B, ll = u / (H * B);
+  const int layer = a.layer0 + ll;
+  const int2 info = __ldcg(a.unit_info + u);
+  const int cf = info.x, nrec = info.y;
+  // constants of the output phase, requested together with the unit's record range
+  const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+  float4 sv = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (a.sinkhorn) {
+    const __half2* sig = reinterpret_cast<const __half2*>(a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane);
+    const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
+    sv = make_float4(s01.x, s01.y, s23.x, s23.y);
+  }
+  float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
+  for (int base = 0; base < nrec; base += 32) {
+    // head hh's (m, l) of both parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
+    float hd[4] = {-INFINITY, 0.f, -INFINITY, 0.f};
+    if (base + lane < nrec) {
+      const float* hp = record_at(a, u, cf + base + lane);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + 4 * i + hh);
+    }
+    const int cnt = min(32, nrec - base);
+    float f[2];
+    unsigned act[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
+      const float mv = hd[2 * k], lv = hd[2 * k + 1];
+      float m = lv > 0.f ? mv : -INFINITY;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, o));
+      const float mn = fmaxf(Mk[k], m);
+      const float sc = (Mk[k] == -INFINITY) ? 0.f : exp2f(Mk[k] - mn);  // rescale earlier chunks
+      Lk[k] *= sc;
+      O[k] = make_float4(O[k].x * sc, O[k].y * sc, O[k].z * sc, O[k].w * sc);
+      Mk[k] = mn;
+      f[k] = lv > 0.f ? exp2f(mv - mn) : 0.f;
+      float lw = lv * f[k];
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
+      Lk[k] += lw;
+      // only records with a part k for this head (a window part is usually in one record)
+      act[k] = __ballot_sync(FULL, f[k] > 0.f && lane < cnt);
+    }
+    // entries e = 32 k + j (record j, part k), lowest first: each part's records in order
+    unsigned long long todo = ((unsigned long long)act[1] << 32) | act[0];
+    while (todo) {
+      int e[MERGE_BATCH];
+      float4 x[MERGE_BATCH];
+#pragma unroll
+      for (int r = 0; r < MERGE_BATCH; ++r) {
+        e[r] = todo ? __ffsll((long long)todo) - 1 : -1;
+        todo &= todo - 1;
+        const int j = max(e[r], 0) & 31, k = max(e[r], 0) >> 5;
+        const float* rec = record_at(a, u, cf + base + j) + 16 + (k * MAX_GQA + hh) * D + 4 * lane;
+        x[r] = e[r] >= 0 ? __ldcg(reinterpret_cast<const float4*>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int r = 0; r < MERGE_BATCH; ++r) {
+        const int j = max(e[r], 0) & 31, k = max(e[r], 0) >> 5;
+        const float f0j = __shfl_sync(FULL, f[0], j), f1j = __shfl_sync(FULL, f[1], j);
+        if (e[r] >= 0 && k == 0) {
+          O[0].x += f0j * x[r].x;
+          O[0].y += f0j * x[r].y;
+          O[0].z += f0j * x[r].z;
+          O[0].w += f0j * x[r].w;
+        } else if (e[r] >= 0) {
+          O[1].x += f1j * x[r].x;
+          O[1].y += f1j * x[r].y;
+          O[1].z += f1j * x[r].z;
+          O[1].w += f1j * x[r].w;
         }
       }
-      u = __shfl_sync(FULL, u, 0);
-      if (__shfl_sync(FULL, stop, 0)) break;
-      if (u == MQ_SKIP) {
-        t0 = 0;
-      } else if (u >= 0) {
-        __syncwarp();  // the other lanes' record reads after lane 0's acquire
-        merge(u / MAX_GQA, u % MAX_GQA);
-        t0 = 0;
-      }
     }
   }
-
-  // merge the units of steps [xs, xe) that this warp flagged
-  __device__ __noinline__ void run_merges(int gw, long long xs, long long xe) {
-    const Pos pf = locate(xs, S_layer, B, H, sq);
-    const Pos pl = locate(xe - 1, S_layer, B, H, sq);
-    const int uf = (pf.ll * B + pf.b) * H + pf.h, ul = (pl.ll * B + pl.b) * H + pl.h;
-    for (int u = uf; u <= ul; ++u) {
-      int* flag = a.counters + a.n_units + u + gw;
-      if (__ldcg(flag) != 0) {
-        for (int hh = 0; hh < g; ++hh) merge(u, hh);
-        if (lane == 0) *flag = 0;
-      }
-    }
+  float q0 = O[0].x, q1 = O[0].y, q2 = O[0].z, q3 = O[0].w;
+  const bool hq = Lk[0] > 0.f, hw = Lk[1] > 0.f;
+  if (hq) {
+    // undo the balancing scale and the rotation: v = s . (c H (sigma . y))
+    q0 *= sv.x;
+    q1 *= sv.y;
+    q2 *= sv.z;
+    q3 *= sv.w;
+    hadamard_warp(q0, q1, q2, q3, lane);
+    q0 *= C_WHT * sg.x;
+    q1 *= C_WHT * sg.y;
+    q2 *= C_WHT * sg.z;
+    q3 *= C_WHT * sg.w;
   }
+  const float Mt = fmaxf(hq ? Mk[0] : -INFINITY, hw ? Mk[1] : -INFINITY);
+  const float f0 = hq ? exp2f(Mk[0] - Mt) : 0.f;
+  const float f1 = hw ? exp2f(Mk[1] - Mt) : 0.f;
+  const float den = Lk[0] * f0 + Lk[1] * f1;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float4 o;
+  o.x = (q0 * f0 + O[1].x * f1) * inv;
+  o.y = (q1 * f0 + O[1].y * f1) * inv;
+  o.z = (q2 * f0 + O[1].z * f1) * inv;
+  o.w = (q3 * f0 + O[1].w * f1) * inv;
+  *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * H * g + (size_t)h * g + hh) * D + 4 * lane) = o;
+}
 
-};
+// One warp per (unit, query head).  Launched as a programmatic dependent of decode_kernel; waits
+// for the whole grid (its records and record ranges) before reading anything.
+__global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * MERGE_WARPS + (threadIdx.x >> 5);
+  if (t >= (long long)a.n_units * a.g) return;
+  merge_head(a, (int)(t / a.g), (int)(t % a.g), lane);
+}
 
 template <int KF>
 __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __grid_constant__ DecodeArgs a) {
@@ -1110,7 +1020,8 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   constexpr int NCW = GE::NCW, NSTAGE = GE::NSTAGE, NTHREADS = GE::NTHREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
   // launched as a programmatic dependent: the previous kernel of the stream may still be running
-  // and writing the inputs (the cache, q, lengths); wait for it before reading any of them
+  // and writing the inputs (the cache, q, lengths); wait for it before reading any of them.  (No
+  // early trigger for the merge kernel: its CTAs, resident early, slowed the streaming warps.)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   Kernel<KF> K(a, smem);
   const int tid = threadIdx.x;
@@ -1178,15 +1089,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       sCpre[B] = cincl;
     }
   }
-  {
-    int* mq = reinterpret_cast<int*>(smem + GE::SM_MQ);
-    for (int i = tid; i < MQ_CAP + 4; i += NTHREADS) mq[i] = i < MQ_CAP ? -1 : 0;
-  }
-  if (tid == 0) {
-    for (int i = 0; i < NSTAGE; ++i) {
-      mbar_init(full + i, 1);
-      mbar_init(empty + i, 1);
-    }
+  if (tid >= 32 && tid < 32 + 2 * NSTAGE) {
+    // one barrier per thread of warps 1-2 (full[NSTAGE] then empty[NSTAGE], contiguous)
+    mbar_init(full + (tid - 32), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -1202,25 +1107,39 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   K.sq.C = sC;
   K.sq.cpre = sCpre;
 
-  // empty sequences produce zeros (no step belongs to them)
-  if (blockIdx.x == 0) {
-    for (int b = K.warp; b < B; b += NCW + 1)
-      if (sL[b] == 0)
-        for (int ll = 0; ll < a.n_layers_call; ++ll)
-          for (int hq = 0; hq < K.Hq; ++hq)
-            *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * K.Hq + hq) * D + 4 * K.lane) =
-                make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
   K.S_layer = (long long)H * sPre[B];
   K.S = K.S_layer * a.n_layers_call;
   K.C_layer = (long long)H * sCpre[B];
   K.C = K.C_layer * a.n_layers_call;
-  if (K.S == 0) return;
-  // every range, even a normal-speed one, must span at least the longest step
-  K.nw = max(1LL, min((long long)gridDim.x * NCW, K.C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
-  K.SPtot = K.speed_before(K.nw);
-  if ((long long)blockIdx.x * NCW >= K.nw) return;
+  if (K.S > 0) {
+    // every range, even a normal-speed one, must span at least the longest step
+    K.nw = max(1LL, min((long long)gridDim.x * NCW, K.C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
+    K.SPtot = K.speed_before(K.nw);
+  }
+  // the record ranges of all units, for the merge kernel: a share per consumer thread of the grid,
+  // computed by warps with steps once their first copies are in flight
+  const long long info_i = (long long)tid * gridDim.x + blockIdx.x;
+  if (K.S == 0 || (long long)blockIdx.x * NCW >= K.nw) {
+    if (tid < NCW * 32) K.unit_info_share(info_i);
+    return;
+  }
+
+  // ---- the step ranges of this CTA's warps, located once: lane j of the producer warp finds the
+  // first step of consumer warp j, lane NCW that of the next CTA's first warp (this CTA's end)
+  int4* sWpos = reinterpret_cast<int4*>(smem + GE::SM_WPOS);
+  long long* sWxs = reinterpret_cast<long long*>(smem + GE::SM_WPOS + (NCW + 1) * 16);
+  if (K.warp == NCW && K.lane <= NCW) {
+    const long long gwj = (long long)blockIdx.x * NCW + K.lane;
+    Pos p = {0, 0, 0, 0};
+    long long x = K.S;
+    if (gwj < K.nw) {
+      p = K.first_step(gwj);
+      x = K.step_index(p);
+    }
+    sWpos[K.lane] = make_int4(p.ll, p.b, p.h, p.local);
+    sWxs[K.lane] = x;
+  }
+  __syncthreads();
 
   if (K.warp == NCW) {
     // ======================= producer: lane w streams consumer warp w's contiguous step range.
@@ -1232,11 +1151,11 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     int n = 0;
     Pos ps = {0, 0, 0, 0};
     if (w < NCW && gw < K.nw) {
-      ps = K.first_step(gw);
-      const long long xs = K.step_index(ps);
-      const long long xe = gw + 1 < K.nw ? K.step_index(K.first_step(gw + 1)) : K.S;
-      n = (int)(xe - xs);
+      const int4 p = sWpos[w];
+      ps = {p.x, p.y, p.z, p.w};
+      n = (int)(sWxs[w + 1] - sWxs[w]);
     }
+    int bt_page = -1, bt_phys = 0;  // the last block-table entry read by this lane
     constexpr int NS = GE::NSLOT;
     int k = 0;
     unsigned long long t_idle = 0;
@@ -1261,7 +1180,13 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
           const int hp = ps.local - nwin;  // half-page index within the sequence
           const int Lq = W > 0 ? max(0, L - W) : L;
           const int ntok = min(HALF, Lq - hp * HALF);
-          const int phys = a.block_table[(size_t)ps.b * a.max_pages_per_seq + (hp >> 1)];
+          const int page = ps.b * a.max_pages_per_seq + (hp >> 1);
+          if (page != bt_page) {
+            // the cache's own table is the identity: no read
+            bt_phys = a.identity_pages ? page : a.block_table[page];
+            bt_page = page;
+          }
+          const int phys = bt_phys;
           if (phys < 0 || phys >= a.L.n_pages) {
             atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
             desc[slot] = make_int4(u, KIND_QUANT, 0, ps.local);
@@ -1296,11 +1221,16 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
 
   // ======================= consumers: warp gw processes its steps (see first_step) in order
   const long long gw = (long long)blockIdx.x * NCW + K.warp;
-  if (gw >= K.nw) return;
-  const Pos p0 = K.first_step(gw);
-  const long long xs = K.step_index(p0);
-  const long long xe = gw + 1 < K.nw ? K.step_index(K.first_step(gw + 1)) : K.S;
-  const int n = (int)(xe - xs);
+  if (gw >= K.nw) {
+    K.unit_info_share(info_i);
+    return;
+  }
+  Pos p0;
+  {
+    const int4 p = sWpos[K.warp];
+    p0 = {p.x, p.y, p.z, p.w};
+  }
+  const int n = (int)(sWxs[K.warp + 1] - sWxs[K.warp]);
   QuantState st;
   WinState ws;
   ws.q = reinterpret_cast<float*>(smem + GE::SM_Q) + K.warp * MAX_GQA * D;
@@ -1320,6 +1250,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     }
     K.load_q(cur, st, ws, kind);
   }
+  K.unit_info_share(info_i);
   // step k uses slot warp + NCW*(k mod NSLOT), phase k / NSLOT of that slot
   for (int k = 0, j = 0, ph = 0; k < n; ++k) {
     const int slot = K.warp + NCW * j;
@@ -1354,13 +1285,6 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     if (K.lane == 0) mbar_arrive(empty + slot);
   }
   K.finish_unit(cur, (int)gw, kind, hasq, hasw, st, ws);
-  K.arrive_units((int)gw, xs, xe);
-  K.run_merges((int)gw, xs, xe);
-  if (K.lane == 0) {
-    __threadfence_block();
-    atomicAdd(reinterpret_cast<int*>(smem + GE::SM_MQ) + MQ_DONE, 1);
-  }
-  K.drain_merges((int)min((long long)NCW, K.nw - (long long)blockIdx.x * NCW));
 }
 
 }  // namespace
@@ -1370,10 +1294,12 @@ int decode_consumer_warps(int k_format) {
 }
 
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
-  const int ncw = k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
-  // arrival counters [n_units], merge flags [n_units + warps], then the partial records
-  const size_t slots = (size_t)n_units + (size_t)n_ctas * ncw;
-  return align256(((size_t)n_units + slots) * sizeof(int)) + slots * REC_FLOATS * sizeof(float);
+  // record ranges int2 [n_units], then the partial records (index unit + warp)
+  return align256((size_t)n_units * sizeof(int2)) + decode_record_slots(n_units, n_ctas, k_format) * REC_FLOATS * sizeof(float);
+}
+
+size_t decode_record_slots(int n_units, int n_ctas, int k_format) {
+  return (size_t)n_units + (size_t)n_ctas * decode_consumer_warps(k_format);
 }
 
 template <int KF>
@@ -1394,7 +1320,15 @@ static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<KF>, a);
+  e = cudaLaunchKernelEx(&cfg, decode_kernel<KF>, a);
+  if (e != cudaSuccess) return e;
+  // the merge, as a programmatic dependent of the decode grid
+  const long long tasks = (long long)a.n_units * a.g;
+  cudaLaunchConfig_t mcfg = cfg;
+  mcfg.gridDim = dim3((unsigned)((tasks + MERGE_WARPS - 1) / MERGE_WARPS));
+  mcfg.blockDim = dim3(MERGE_WARPS * 32);
+  mcfg.dynamicSmemBytes = 0;
+  return cudaLaunchKernelEx(&mcfg, merge_kernel, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {

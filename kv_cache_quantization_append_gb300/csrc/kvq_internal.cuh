@@ -91,13 +91,15 @@ struct DecodeArgs {
   const void* q;
   float* out;
   const int32_t* seq_lens;
-  int* counters;
-  float* records;
+  int2* unit_info;  // [n_units] first record index and record count of each unit
+  float* records;   // partial records, index unit + global consumer warp
   int layer0, n_layers_call, batch, max_batch, Hkv, g, W, max_seq_len, k_format, sinkhorn, in_bf16;
   int max_pages_per_seq, n_units, n_ctas;
+  int identity_pages;  // block_table is the cache's own identity table (page p of sequence b = b * max_pages_per_seq + p)
 };
 int decode_ctas(int device);
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format);
+size_t decode_record_slots(int n_units, int n_ctas, int k_format);
 int decode_consumer_warps(int k_format);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 

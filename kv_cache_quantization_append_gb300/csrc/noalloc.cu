@@ -12,7 +12,7 @@ namespace kvq {
 
 namespace {
 
-// The scratch every call of this entry point shares (counters, then partial records).  It lives in
+// The scratch every call of this entry point shares (record ranges, then partial records).  It lives in
 // the library's module on each device that uses it, until the process exits.
 constexpr size_t NOALLOC_SCRATCH_BYTES = (size_t)KVQ_NOALLOC_SCRATCH_MAX;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
@@ -48,14 +48,7 @@ int decode_attention_noalloc(kvq_cache* cache, int32_t layer, const void* q, flo
   void* scratch = nullptr;
   const int rc = scratch_address(dev, &scratch);
   if (rc != KVQ_OK) return rc;
-  // The arrival counters and merge flags at the start of the scratch must be zero when the kernel
-  // starts; the array keeps whatever the previous call left, so clear them on the call's stream.
-  const int nl = layer == -1 ? cache->cfg.n_layers : 1;
-  const size_t n_units = (size_t)nl * batch * cache->cfg.n_kv_heads;
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  const size_t counters = (2 * n_units + (size_t)sms * decode_consumer_warps(cache->cfg.k_format)) * sizeof(int);
-  if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  // every decode call writes the parts of the scratch it reads, so it needs no clearing
   return kv_decode_attention(cache, layer, q, out, seq_lens, batch, scratch, NOALLOC_SCRATCH_BYTES, stream);
 }
 

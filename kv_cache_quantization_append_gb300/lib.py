@@ -168,7 +168,8 @@ def kv_decode_scratch_bytes(cache: kvq_cache, layer: int, batch: int) -> int:
 
 def kv_decode_attention(cache: kvq_cache, layer: int, q: torch.Tensor, out: torch.Tensor,
                         seq_lens: torch.Tensor, scratch: torch.Tensor, stream=None):
-    """q: [L?][B][Hq][128]; out: float32 like q; seq_lens: int32 [B]; scratch: zeroed bytes."""
+    """q: [L?][B][Hq][128]; out: float32 like q; seq_lens: int32 [B]; scratch: device bytes (any
+    contents), at least kv_decode_scratch_bytes."""
     if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
         raise KVQError("seq_lens must be int32 and out float32")
     _check_in_dtype(cache, q)
