@@ -154,6 +154,12 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 // byte and converted as an FP8 E4M3 value, which for bit patterns 0..15 (exponent field 0 or 1)
 // is exactly c * 2^-9.  lo0 = (n0, n2), lo1 = (n4, n6), hi0 = (n1, n3), hi1 = (n5, n7) where n_m is
 // the m-th nibble (low nibble of byte k is n_2k).
+// a * b + c as an integer multiply-add (the FMA pipe; kept as written, not turned into ALU shifts)
+__device__ __forceinline__ uint32_t imad_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
 __device__ __forceinline__ void cvt8(uint32_t w, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
   const uint32_t hi = __umulhi(w, 1u << 28) & 0x0F0F0F0Fu;  // w >> 4 on the multiply pipe
@@ -589,10 +595,12 @@ struct Kernel {
       for (int kk = 0; kk < 8; ++kk) {
         // half2 index k' = 2kk + eps holds bits (k', k'+16) as +-1.0
         const int k0 = 2 * kk, k1 = 2 * kk + 1;
-        const uint32_t a0 = ((sa << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
-        const uint32_t a1 = ((sbw << (15 - k0)) & 0x80008000u) | 0x3C003C00u;
-        const uint32_t a2 = ((sa << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
-        const uint32_t a3 = ((sbw << (15 - k1)) & 0x80008000u) | 0x3C003C00u;
+        // the bit moves to the fp16 sign by a multiply-add that also adds 1.0 (0x3C00) to both halves:
+        // one and on the ALU pipe, one integer mad on the FMA pipe
+        const uint32_t a0 = imad_u32(sa & (0x00010001u << k0), 1u << (15 - k0), 0x3C003C00u);
+        const uint32_t a1 = imad_u32(sbw & (0x00010001u << k0), 1u << (15 - k0), 0x3C003C00u);
+        const uint32_t a2 = imad_u32(sa & (0x00010001u << k1), 1u << (15 - k1), 0x3C003C00u);
+        const uint32_t a3 = imad_u32(sbw & (0x00010001u << k1), 1u << (15 - k1), 0x3C003C00u);
         mma16816(sacc, a0, a1, a2, a3, st.sb[kk][0], st.sb[kk][1]);
       }
       const __half* nrm = reinterpret_cast<const __half*>(kmeta);
