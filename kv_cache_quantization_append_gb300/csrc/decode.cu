@@ -162,7 +162,8 @@ __device__ __forceinline__ uint32_t imad_u32(uint32_t a, uint32_t b, uint32_t c)
 }
 __device__ __forceinline__ void cvt8(uint32_t w, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
-  const uint32_t hi = __umulhi(w, 1u << 28) & 0x0F0F0F0Fu;  // w >> 4 on the multiply pipe
+  // a plain shift: the multiply-high form of w >> 4 (integer pipe) measured 4-5 % slower here
+  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
   asm("{\n .reg .b16 a, b, c, d;\n mov.b32 {a, b}, %4;\n mov.b32 {c, d}, %5;\n"
       " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n"
       " cvt.rn.f16x2.e4m3x2 %2, c;\n cvt.rn.f16x2.e4m3x2 %3, d;\n}"
