@@ -230,7 +230,9 @@ __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_co
   // = half (R & 1) of w[R / 2].  The even token stores rows 0-3, the odd one rows 4-7, each with
   // its partner's halfwords (lane ^ 4) for those rows.
   const bool odd = tin & 1;
-  const bool paired = valid && (__shfl_xor_sync(FULL, valid ? 1 : 0, 4) != 0);
+  // every lane takes part in the shuffle (a short-circuited one would leave lanes of the mask out)
+  const int partner_valid = __shfl_xor_sync(FULL, valid ? 1 : 0, 4);
+  const bool paired = valid && partner_valid != 0;
   const uint32_t pa = __shfl_xor_sync(FULL, odd ? w[0] : w[2], 4);
   const uint32_t pb = __shfl_xor_sync(FULL, odd ? w[1] : w[3], 4);
   uint8_t* vmain = pg + a.L.off_vmain;

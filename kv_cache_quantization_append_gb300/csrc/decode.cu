@@ -848,8 +848,9 @@ struct Kernel {
     l += __shfl_xor_sync(FULL, l, 8);
     l += __shfl_xor_sync(FULL, l, 16);
     // heads 2i, 2i+1 in columns; channel of m-tile 2G+e row r is 32G + 4r + 2e, row r+8 adds 1
-    const bool anyl = __shfl_sync(FULL, l, 0) > 0.f || __shfl_sync(FULL, l, 1) > 0.f ||
-                      __shfl_sync(FULL, l, 2) > 0.f || __shfl_sync(FULL, l, 3) > 0.f;
+    const float l0 = __shfl_sync(FULL, l, 0), l1 = __shfl_sync(FULL, l, 1);
+    const float l2 = __shfl_sync(FULL, l, 2), l3 = __shfl_sync(FULL, l, 3);
+    const bool anyl = l0 > 0.f || l1 > 0.f || l2 > 0.f || l3 > 0.f;
     if (anyl) {
 #pragma unroll
       for (int cidx = 0; cidx < 2; ++cidx) {
