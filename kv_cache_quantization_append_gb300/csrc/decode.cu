@@ -160,6 +160,12 @@ __device__ __forceinline__ uint32_t imad_u32(uint32_t a, uint32_t b, uint32_t c)
   asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+// 32-bit shared-memory load at a shared-window address (data written before the loop that reads it)
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ void cvt8(uint32_t w, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
   // a plain shift: the multiply-high form of w >> 4 (integer pipe) measured 4-5 % slower here
@@ -574,7 +580,9 @@ struct Kernel {
     const uint8_t* kmeta = stage + OFF_KMETA;
     if (KF == KVQ_TQ3_QJL) {
       float cacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t* lut = reinterpret_cast<const uint32_t*>(smem + SM_LUT) + lane;
+      // this lane's column of the centroid-pair table (entry j at byte 128 j): the entry address is
+      // formed by one integer multiply-add (FMA pipe) from the extracted 6-bit field
+      const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(smem + SM_LUT) + 4u * lane;
       const uint32_t* ca = reinterpret_cast<const uint32_t*>(kmain + ta * 48 + 12 * i);
       const uint32_t* cbp = reinterpret_cast<const uint32_t*>(kmain + tb * 48 + 12 * i);
       const uint32_t wa[4] = {ca[0], ca[1], ca[2], 0u};
@@ -585,8 +593,8 @@ struct Kernel {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int bit = 6 * (2 * kk + e), wi = bit >> 5, sh = bit & 31;
-          pa[e] = lut[(__funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u) * 32];
-          pb[e] = lut[(__funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u) * 32];
+          pa[e] = lds_u32(imad_u32(__funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u, 128u, lutb));
+          pb[e] = lds_u32(imad_u32(__funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u, 128u, lutb));
         }
         mma16816(cacc, pa[0], pb[0], pa[1], pb[1], st.qb[kk][0], st.qb[kk][1]);
       }
