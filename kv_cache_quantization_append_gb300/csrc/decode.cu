@@ -636,10 +636,11 @@ struct Kernel {
       const uint4 ma = *reinterpret_cast<const uint4*>(kmeta + ta * 16);
       const uint4 mb = *reinterpret_cast<const uint4*>(kmeta + tb * 16);
       // zero-point term sum_G z_G * sum(q~_G) on the tensor core: A row = token, k = group
-      // (this thread's k pair 2i, 2i+1 is zero (G0, G1) for i = 0, (G2, G3) for i = 1)
+      // (this thread's k pair 2i, 2i+1 is zero (G0, G1) for i = 0, (G2, G3) for i = 1; lanes i = 2, 3
+      // meet a zero B fragment, so any finite pair does there and no lane needs a second select)
       float zacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t zla = i == 0 ? ma.z : (i == 1 ? ma.w : 0u);
-      const uint32_t zlb = i == 0 ? mb.z : (i == 1 ? mb.w : 0u);
+      const uint32_t zla = (i & 1) ? ma.w : ma.z;
+      const uint32_t zlb = (i & 1) ? mb.w : mb.z;
       mma16816(zacc, zla, zlb, 0u, 0u, st.zb, 0u);
       const float2 sa01 = __half22float2(u2h(ma.x)), sa23 = __half22float2(u2h(ma.y));
       const float2 sb01 = __half22float2(u2h(mb.x)), sb23 = __half22float2(u2h(mb.y));
@@ -709,8 +710,9 @@ struct Kernel {
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
       const int t0 = 16 * mt + 2 * i;
-      pA[mt] = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0) : 0u;
-      pB[mt] = colok ? *reinterpret_cast<const uint32_t*>(pcol + t0 + 8) : 0u;
+      // a missing head's weights are written as zeros by the softmax (its logits are -inf)
+      pA[mt] = *reinterpret_cast<const uint32_t*>(pcol + t0);
+      pB[mt] = *reinterpret_cast<const uint32_t*>(pcol + t0 + 8);
       plA[mt] = (colok && lo) ? *reinterpret_cast<const uint32_t*>(pcol + MAX_GQA * HALF + t0) : 0u;
       plB[mt] = (colok && lo) ? *reinterpret_cast<const uint32_t*>(pcol + MAX_GQA * HALF + t0 + 8) : 0u;
       // zero-point term: rows = groups r (< 4), k = tokens: A = zero, B = p_hi | p_lo
