@@ -2,7 +2,8 @@
 
 kv_decode_attention_noalloc takes its scratch from a fixed array inside the library instead of a
 caller buffer.  Its results must match kv_decode_attention's on the same cache, call after call
-(the shared array keeps the previous call's contents, so a second call checks the clearing), and a
+(the shared array keeps the previous call's contents, so a second call checks that nothing depends
+on them), and a
 call that needs more scratch than the array holds must be refused without launching anything.
 This file is collected last so that a run stopping at its first failure has run everything else.
 """
@@ -41,7 +42,7 @@ def test_noalloc_matches_scratch_entry_point_on_consecutive_calls():
         assert cache.status() == 0
         err = (out - ref).abs().max().item()
         assert err <= 2e-3 * scale, f"call {call}: max abs err {err:.3e} vs {scale:.3e}"
-    # a per-layer call reuses the same array with a different counter range
+    # a per-layer call reuses the same array with a different layout of record ranges and records
     one = torch.empty(q.shape[1:], dtype=torch.float32, device="cuda")
     lib.kv_decode_attention_noalloc(cache.handle, 1, q[1].contiguous(), one, seq)
     torch.cuda.synchronize()
