@@ -301,6 +301,37 @@ def run_gpu(args):
     if cache.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
+    # the second form of the decode step: one decode call per layer (two launches each), the calls of
+    # a step captured in one CUDA graph and replayed (the first calls, outside the capture, allocate
+    # the per-layer scratch and set the kernels' attributes)
+    per_layer = None
+    if layers > 1:
+        q0 = qs[0].contiguous()
+        ql = [q0[l] for l in range(layers)]
+        ol = [out[l] for l in range(layers)]
+        for l in range(layers):
+            cache.decode(l, ql[l], seq, ol[l])
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for l in range(layers):
+                cache.decode(l, ql[l], seq, ol[l])
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize()
+        if cache.status() != 0:
+            raise RuntimeError("device status set during the per-layer graph timing")
+        g_s = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps / 1e3
+        per_layer = {"form": "per-layer decode calls captured in one CUDA graph", "decode_us_per_step": g_s * 1e6,
+                     "launches_per_step": 2 * layers, "tokens_per_s": weak_scaling_value(float(lens.sum()), world, g_s * 1e3)}
+        del graph
+
     # end-to-end through the public API: host inputs in, host output out, every step
     q_h = [q.cpu().pin_memory() for q in qs]
     k_h, v_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
@@ -386,6 +417,7 @@ def run_gpu(args):
                     "h2d_bytes_per_step": int(qs[0].numel() * qs[0].element_size() + 2 * knew.numel() * knew.element_size()),
                     "d2h_bytes_per_step": int(out.numel() * 4), "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": 3 * args.steps,
+            "decode_per_layer_graph": per_layer,
             "clocks": clk.summary(),
         }
         if layers < w["n_layers"]:

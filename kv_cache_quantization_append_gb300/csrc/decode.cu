@@ -26,6 +26,7 @@
 //    query head's records in a fixed order (deterministic), undoes the rotation of the quantised
 //    part and combines it with the window part.  No inter-CTA flags, fences or atomics inside the
 //    streaming kernel.
+#include <atomic>
 #include <cfloat>
 
 #include "kvq_internal.cuh"
@@ -39,7 +40,8 @@ constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
-constexpr int MERGE_WARPS = 8;  // warps per CTA of the merge kernel, one query head each
+constexpr int MERGE_WARPS = 8;  // warps per CTA of the merge kernels
+constexpr long long WIDE_MERGE_RECORDS = 48;  // above this many records per unit, merge with a CTA per head
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
@@ -920,31 +922,21 @@ struct Kernel {
 // are requested together, up to MERGE_BATCH per round, and summed per part in record order.  A
 // unit without records (empty sequence) gets zeros.
 constexpr int MERGE_BATCH = 16;
-__device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
-  const int H = a.Hkv, B = a.batch, g = a.g;
-  const int h = u % H, b = (u / H) % B, ll = u / (H * B);
-  const int layer = a.layer0 + ll;
-  const int2 info = __ldcg(a.unit_info + u);
-  const int cf = info.x, nrec = info.y;
-  // constants of the output phase, requested together with the unit's record range
-  const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
-  float4 sv = make_float4(1.f, 1.f, 1.f, 1.f);
-  if (a.sinkhorn) {
-    const __half2* sig = reinterpret_cast<const __half2*>(a.p.sigv + ((size_t)layer * H + h) * D + 4 * lane);
-    const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
-    sv = make_float4(s01.x, s01.y, s23.x, s23.y);
-  }
-  float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-  float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
-  for (int base = 0; base < nrec; base += 32) {
+
+// Merge records cf + r0 .. cf + r1 - 1 of unit u, query head hh, into the running state of both
+// parts (0 = quantised, rotated space; 1 = window): maxima Mk, sums Lk and this lane's channels
+// 4 lane .. +3 of the accumulators O, in record order.
+__device__ __forceinline__ void merge_records(const DecodeArgs& a, int u, int hh, int lane, int cf, int r0, int r1,
+                                              float4 (&O)[2], float (&Mk)[2], float (&Lk)[2]) {
+  for (int base = r0; base < r1; base += 32) {
     // head hh's (m, l) of both parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
     float hd[4] = {-INFINITY, 0.f, -INFINITY, 0.f};
-    if (base + lane < nrec) {
+    if (base + lane < r1) {
       const float* hp = record_at(a, u, cf + base + lane);
 #pragma unroll
       for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + 4 * i + hh);
     }
-    const int cnt = min(32, nrec - base);
+    const int cnt = min(32, r1 - base);
     float f[2];
     unsigned act[2];
 #pragma unroll
@@ -997,6 +989,28 @@ __device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
       }
     }
   }
+}
+
+// This lane's channels of the rotation signs and of the unit's V balancing scales (ones without
+// Sinkhorn), for the output phase: requested early, while the records are read.
+__device__ __forceinline__ void merge_constants(const DecodeArgs& a, int u, int lane, float4& sg, float4& sv) {
+  const int H = a.Hkv, B = a.batch;
+  const int h = u % H, ll = u / (H * B);
+  sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+  sv = make_float4(1.f, 1.f, 1.f, 1.f);
+  if (a.sinkhorn) {
+    const __half2* sig = reinterpret_cast<const __half2*>(a.p.sigv + ((size_t)(a.layer0 + ll) * H + h) * D + 4 * lane);
+    const float2 s01 = __half22float2(sig[0]), s23 = __half22float2(sig[1]);
+    sv = make_float4(s01.x, s01.y, s23.x, s23.y);
+  }
+}
+
+// The head's output from the merged state: undo the balancing scale and the rotation of the
+// quantised part, combine it with the window part, divide by the sum.
+__device__ __forceinline__ void merge_output(const DecodeArgs& a, int u, int hh, int lane, const float4 (&O)[2],
+                                             const float (&Mk)[2], const float (&Lk)[2], float4 sg, float4 sv) {
+  const int H = a.Hkv, B = a.batch, g = a.g;
+  const int h = u % H, b = (u / H) % B, ll = u / (H * B);
   float q0 = O[0].x, q1 = O[0].y, q2 = O[0].z, q3 = O[0].w;
   const bool hq = Lk[0] > 0.f, hw = Lk[1] > 0.f;
   if (hq) {
@@ -1024,14 +1038,88 @@ __device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
   *reinterpret_cast<float4*>(a.out + (((size_t)ll * B + b) * H * g + (size_t)h * g + hh) * D + 4 * lane) = o;
 }
 
+
+// Combine the partial records of query head hh of unit u (records cf .. cf + nrec - 1, one per
+// warp that streamed part of the unit) in record order and write the head's output.  Latency-bound,
+// so the round trips are few: the unit's record range; then lane j reads both parts' (m, l) of
+// record j (32 records at a time, with running maxima across chunks) and the weights are reduced
+// in registers; then the head's accumulators of every record that holds a part (quantised, window)
+// are requested together, up to MERGE_BATCH per round, and summed per part in record order.  A
+// unit without records (empty sequence) gets zeros.
+__device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
+  const int2 info = __ldcg(a.unit_info + u);
+  float4 sg, sv;
+  merge_constants(a, u, lane, sg, sv);
+  float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
+  merge_records(a, u, hh, lane, info.x, 0, info.y, O, Mk, Lk);
+  merge_output(a, u, hh, lane, O, Mk, Lk, sg, sv);
+}
+
 // One warp per (unit, query head).  Launched as a programmatic dependent of decode_kernel; waits
 // for the whole grid (its records and record ranges) before reading anything.
 __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // a following decode launched as a programmatic dependent (the next layer's call) may run its
+  // set-up now: it writes nothing outside shared memory before its own wait for this grid
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int lane = threadIdx.x & 31;
   const long long t = (long long)blockIdx.x * MERGE_WARPS + (threadIdx.x >> 5);
   if (t >= (long long)a.n_units * a.g) return;
   merge_head(a, (int)(t / a.g), (int)(t % a.g), lane);
+}
+
+// Calls whose units have many records each (a single layer's decode spread over every warp of
+// the GPU: hundreds of records per unit): one CTA per (unit, query head), its warps merging
+// consecutive slices of the records in parallel; the eight partial states are then combined in
+// slice order by the first warp (a fixed order: deterministic), which writes the output.
+__global__ void __launch_bounds__(MERGE_WARPS * 32) merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float4 sO[MERGE_WARPS][2][32];
+  __shared__ float sM[MERGE_WARPS][2], sL[MERGE_WARPS][2];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int u = blockIdx.x / a.g, hh = blockIdx.x % a.g;
+  const int2 info = __ldcg(a.unit_info + u);
+  float4 sg, sv;
+  if (w == 0) merge_constants(a, u, lane, sg, sv);
+  const int per = (info.y + MERGE_WARPS - 1) / MERGE_WARPS;
+  const int r0 = min(info.y, w * per), r1 = min(info.y, r0 + per);
+  float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
+  merge_records(a, u, hh, lane, info.x, r0, r1, O, Mk, Lk);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    sO[w][k][lane] = O[k];
+    if (lane == 0) {
+      sM[w][k] = Mk[k];
+      sL[w][k] = Lk[k];
+    }
+  }
+  __syncthreads();
+  if (w != 0) return;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    float M = -INFINITY;
+    for (int j = 0; j < MERGE_WARPS; ++j)
+      if (sL[j][k] > 0.f) M = fmaxf(M, sM[j][k]);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    for (int j = 0; j < MERGE_WARPS; ++j) {
+      if (!(sL[j][k] > 0.f)) continue;
+      const float f = exp2f(sM[j][k] - M);
+      const float4 x = sO[j][k][lane];
+      L += sL[j][k] * f;
+      acc.x += f * x.x;
+      acc.y += f * x.y;
+      acc.z += f * x.z;
+      acc.w += f * x.w;
+    }
+    O[k] = acc;
+    Mk[k] = M;
+    Lk[k] = L;
+  }
+  merge_output(a, u, hh, lane, O, Mk, Lk, sg, sv);
 }
 
 template <int KF>
@@ -1322,11 +1410,28 @@ size_t decode_record_slots(int n_units, int n_ctas, int k_format) {
   return (size_t)n_units + (size_t)n_ctas * decode_consumer_warps(k_format);
 }
 
+// largest dynamic shared-memory size granted so far to decode_kernel<KF>, per device: the attribute
+// is set again only when a call needs more (no host call per launch, none during stream capture
+// once a call of the same or a larger batch has run)
+constexpr int MAX_DEVICES = 64;
+template <int KF>
+std::atomic<int> g_smem_granted[MAX_DEVICES];
+
 template <int KF>
 static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem = Geo<KF>::SM_SEQ + 6 * (size_t)(a.batch + 1) * sizeof(int);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= MAX_DEVICES || g_smem_granted<KF>[dev].load() < (int)smem) {
+    e = cudaFuncSetAttribute(decode_kernel<KF>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < MAX_DEVICES) {
+      int cur = g_smem_granted<KF>[dev].load();
+      while (cur < (int)smem && !g_smem_granted<KF>[dev].compare_exchange_weak(cur, (int)smem)) {
+      }
+    }
+  }
   // programmatic dependent launch: the CTAs may be launched while the previous kernel of the
   // stream (typically the append of the step's new tokens) is finishing; each waits for it
   // (griddepcontrol.wait) before reading anything
@@ -1342,12 +1447,19 @@ static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, decode_kernel<KF>, a);
   if (e != cudaSuccess) return e;
-  // the merge, as a programmatic dependent of the decode grid
+  // the merge, as a programmatic dependent of the decode grid: one warp per (unit, query head), or
+  // one CTA per (unit, query head) when the units are few and each holds many records (at most
+  // about consumer warps / units of them)
   const long long tasks = (long long)a.n_units * a.g;
+  const long long recs_per_unit = (long long)a.n_ctas * Geo<KF>::NCW / a.n_units + 2;
   cudaLaunchConfig_t mcfg = cfg;
-  mcfg.gridDim = dim3((unsigned)((tasks + MERGE_WARPS - 1) / MERGE_WARPS));
   mcfg.blockDim = dim3(MERGE_WARPS * 32);
   mcfg.dynamicSmemBytes = 0;
+  if (recs_per_unit > WIDE_MERGE_RECORDS) {
+    mcfg.gridDim = dim3((unsigned)tasks);
+    return cudaLaunchKernelEx(&mcfg, merge_wide_kernel, a);
+  }
+  mcfg.gridDim = dim3((unsigned)((tasks + MERGE_WARPS - 1) / MERGE_WARPS));
   return cudaLaunchKernelEx(&mcfg, merge_kernel, a);
 }
 
