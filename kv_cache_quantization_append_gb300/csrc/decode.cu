@@ -162,7 +162,10 @@ __device__ __forceinline__ uint32_t imad_u32(uint32_t a, uint32_t b, uint32_t c)
   asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
-// 32-bit shared-memory load at a shared-window address (data written before the loop that reads it)
+// 32-bit shared-memory load at a shared-window address, for data written before the loop that reads
+// it (the centroid table: written in the prologue, before a barrier).  Not volatile and without a
+// memory clobber, so the compiler may schedule it freely; the addresses used depend on codes read
+// from a stage after its barrier wait, which keeps each load after that wait.
 __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
   uint32_t v;
   asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
