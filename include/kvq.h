@@ -181,7 +181,9 @@ int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* 
  *              overlap on the GPU.
  * Splits the token axis over all SMs and runs a bulk-copy pipeline per SM (one launch); a second,
  * small launch on the same stream merges the partial softmax states.  Results do not depend on
- * timing (fixed merge order).
+ * timing (fixed merge order).  Calls may be captured in a CUDA graph once a call of the same or a
+ * larger batch has run on the device outside capture (the first call sets the kernel's
+ * shared-memory size, a host-side step that capture does not record).
  */
 size_t kv_decode_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t batch);
 int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* out,
