@@ -89,6 +89,34 @@ def test_sumsq128_tree():
     assert codec.sumsq128(e) == 9.0
 
 
+def test_sumsq128_tree_shape():
+    """The documented tree pairs (v0^2 + v1^2) + (v2^2 + v3^2) within a block and block i with block
+    i + 16, then i + 8, ...  Two squares of 2^-24 next to a 1 reach the exact (representable) sum
+    1 + 2^-23 only when the tree adds them to each other before adding them to the 1; a
+    left-to-right block sum or an adjacent-block pairing rounds each to even and returns 1."""
+    exact = np.float32(1 + 2.0 ** -23)
+    v = np.zeros(128, np.float32)
+    v[0], v[2], v[3] = 1.0, 2.0 ** -12, 2.0 ** -12          # same block, second pair
+    assert codec.sumsq128(v) == exact
+    v = np.zeros(128, np.float32)
+    v[0], v[4 * 1], v[4 * 17] = 1.0, 2.0 ** -12, 2.0 ** -12  # blocks 1 and 17 are siblings
+    assert codec.sumsq128(v) == exact
+
+
+def test_sumsq128_invariant_under_tree_symmetries():
+    """IEEE addition commutes, so swapping the operands of any node of the tree leaves the result
+    bit-identical: swaps within a pair, of the two pairs of a block, and block index b -> b xor m."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-8, 8, (64, 128)))).astype(np.float32)
+    ref = codec.sumsq128(x)
+    blk = x.reshape(64, 32, 4)
+    assert np.array_equal(codec.sumsq128(blk[:, :, [1, 0, 2, 3]].reshape(64, 128)), ref)
+    assert np.array_equal(codec.sumsq128(blk[:, :, [2, 3, 0, 1]].reshape(64, 128)), ref)
+    for m in (1, 2, 4, 8, 16, 31):
+        perm = np.arange(32) ^ m
+        assert np.array_equal(codec.sumsq128(blk[:, perm].reshape(64, 128)), ref)
+
+
 # ------------------------------------------------------------------ Q4G32
 def test_q4_on_grid_round_trip_is_lossless():
     """Inputs already on a grid z + s*c (fp16 z, power-of-two s, codes using 0 and 15)."""
@@ -139,6 +167,16 @@ def test_q4_scale_and_zero_formula_brute_force():
         assert z[gi] == np.float16(float(g.min()))
         want = np.float16(np.float32(np.float32(g.max()) - np.float32(g.min())) / np.float32(15))
         assert s[gi] == want
+
+
+def test_q4_ties_round_to_even():
+    """A group spanning exactly [0, 15] has scale 1 and zero 0, so (y - zero) / scale = y is exact and
+    values halfway between codes take the even code (IEEE round-half-even)."""
+    y = np.full(128, 7.0, np.float32)
+    y[:9] = [0, 15, 0.5, 1.5, 2.5, 3.5, 4.5, 13.5, 14.5]
+    c, s, z = codec.q4g32_encode(y)
+    assert s[0] == 1 and z[0] == 0
+    assert list(c[:9]) == [0, 15, 0, 2, 2, 4, 4, 14, 14]
 
 
 # ------------------------------------------------------------------ Lloyd-Max / TQ3
@@ -196,6 +234,34 @@ def test_tq3_codes_are_nearest_centroid_and_norms():
     assert np.array_equal(bits[far], t[far] >= 0)
 
 
+def test_tq3_codes_are_scale_invariant():
+    """u = y / |y| does not depend on the scale of y: a power-of-two scale (exact in float32) leaves
+    codes and signs unchanged and scales n exactly, down to norms far below any small epsilon."""
+    rng = np.random.default_rng(22)
+    proj = rng.standard_normal((128, 128)).astype(np.float32)
+    y = rng.standard_normal((50, 128)).astype(np.float32)
+    c0, b0, n0, g0 = codec.tq3_qjl_encode(y, proj)
+    for e in (-30, -12, 10):
+        c, b, n, g = codec.tq3_qjl_encode(y * np.float32(2.0 ** e), proj)
+        assert np.array_equal(c, c0) and np.array_equal(b, b0) and np.array_equal(g, g0)
+        if e == 10:
+            assert np.array_equal(n.astype(np.float32), n0.astype(np.float32) * np.float32(2.0 ** e))
+
+
+def test_tq3_zero_vector():
+    """y = 0: n = 0 and u = 0 (the guard max(n, eps) keeps the division finite); 0 is the middle
+    boundary of the symmetric codebook and a coordinate on a boundary takes the upper cell, so every
+    code is 4, the residual is -c4 in every coordinate and gamma = sqrt(128) * c4."""
+    rng = np.random.default_rng(23)
+    proj = rng.standard_normal((128, 128)).astype(np.float32)
+    c, b, n, g = codec.tq3_qjl_encode(np.zeros((1, 128), np.float32), proj)
+    cent, bnd = codec.tq3_codebook()
+    assert bnd[3] == 0 and n[0] == 0
+    assert np.all(c == 4)
+    assert g[0] == np.float16(math.sqrt(128) * float(cent[4]))
+    assert np.array_equal(b[0], proj.astype(np.float64).sum(1) * -float(cent[4]) >= 0)
+
+
 def test_qjl_estimator_is_unbiased():
     """E_S[sqrt(pi/2)/m * |r| * <S q, sign(S r)>] = <q, r> for Gaussian S (QJL)."""
     rng = np.random.default_rng(7)
@@ -220,6 +286,9 @@ def test_tq3_estimate_tracks_true_inner_product():
     true = y.astype(np.float64) @ q
     assert np.corrcoef(est, true)[0, 1] > 0.97
     assert abs(np.mean(est - true)) < 4 * np.std(est - true) / math.sqrt(len(true))
+    # unbiased means the estimate is on the scale of <q, y>: least-squares slope 1
+    slope = np.dot(est, true) / np.dot(true, true)
+    assert abs(slope - 1) < 0.05
 
 
 # ------------------------------------------------------------------ Sinkhorn invariants
@@ -232,6 +301,35 @@ def test_sinkhorn_recovers_planted_column_scales():
     sig = codec.sinkhorn_sigma(x).astype(np.float64)
     ratio = sig / cscale
     assert np.std(ratio) / np.mean(ratio) < 0.03
+
+
+def test_sinkhorn_recovers_column_scales_under_planted_row_scales():
+    """X = diag(r) A diag(c) with balanced A: alternating row and column normalisation (Sinkhorn)
+    removes the row factors, so sigma is proportional to c even when r spans four decades; column
+    normalisation alone would weight each column by a few dominant rows."""
+    rng = np.random.default_rng(24)
+    a = rng.standard_normal((1024, 128))
+    a /= np.sqrt((a ** 2).mean(0))
+    r = np.exp(rng.uniform(np.log(0.01), np.log(100), (1024, 1)))
+    cscale = np.exp(rng.uniform(np.log(0.2), np.log(5), 128))
+    sig = codec.sinkhorn_sigma((r * a * cscale).astype(np.float32)).astype(np.float64)
+    ratio = sig / cscale
+    assert np.std(ratio) / np.mean(ratio) < 0.03
+
+
+def test_sinkhorn_zero_rows_and_zero_block():
+    """Degenerate blocks: an all-zero token contributes nothing and keeps sigma finite; an all-zero
+    block has no scale to balance and gives sigma = 1."""
+    rng = np.random.default_rng(25)
+    a = rng.standard_normal((1024, 128))
+    a /= np.sqrt((a ** 2).mean(0))
+    cscale = np.exp(rng.uniform(np.log(0.2), np.log(5), 128))
+    x = (a * cscale).astype(np.float32)
+    x[::7] = 0
+    sig = codec.sinkhorn_sigma(x).astype(np.float64)
+    ratio = sig / cscale
+    assert np.all(np.isfinite(sig)) and np.std(ratio) / np.mean(ratio) < 0.03
+    assert np.all(codec.sinkhorn_sigma(np.zeros((64, 128), np.float32)) == 1)
 
 
 def test_sinkhorn_balanced_input_gives_unit_sigma():
@@ -272,32 +370,52 @@ def test_window_covering_context_is_plain_attention(L):
     assert np.allclose(out[0], ref, rtol=0, atol=1e-12)
 
 
-def _brute_force_unit(cache, q, L):
-    """Token-by-token loop with Python floats: dequantise, rotate q, exp, normalise."""
+def _brute_force_unit(cache, q, L, k_raw, v_raw):
+    """Token-by-token loop with Python floats for sequence 0, kv-head 0 of layer 0.
+
+    Quantised tokens are dequantised from the stored records (Q4G32: zero + scale * code, times
+    sigma when balanced; TQ3+QJL: n * (<q~, c[code]> + sqrt(pi/2)/128 * gamma * <S q~, 2b - 1>)) and
+    scored against the rotated query; window tokens are scored from the raw inputs ``k_raw``,
+    ``v_raw`` [L][128], not from the ring, so that the ring's slot bookkeeping is checked too.
+    """
     cfg = cache.cfg
     s = cache.signs.astype(np.float64)
     W = cfg.window
     Lq = max(0, L - W) if W > 0 else L
+    sk = [float(x) for x in cache.sigma_k[0, 0]] if cfg.sinkhorn else [1.0] * 128
+    sv = [float(x) for x in cache.sigma_v[0, 0]] if cfg.sinkhorn else [1.0] * 128
+    cent = [float(x) for x in codec.tq3_codebook()[0]]
     outs = []
     for qh in q:
         qt = codec.hadamard_butterfly(qh.astype(np.float64) * s) * float(codec.C_WHT)
         ws, vals = [], []
         for t in range(L):
             if t < Lq:
-                code = cache.k["code"][0, 0, 0, t]
-                kv = [float(cache.k["zero"][0, 0, 0, t, j // 32]) +
-                      float(np.float32(cache.k["scale"][0, 0, 0, t, j // 32]) * np.float32(code[j]))
-                      for j in range(128)]
-                lg = sum(qt[j] * kv[j] for j in range(128)) / math.sqrt(128)
+                if cfg.k_format == attention.TQ3_QJL:
+                    code = cache.k["code"][0, 0, 0, t]
+                    bits = cache.k["bits"][0, 0, 0, t]
+                    dot_c = sum(qt[j] * cent[code[j]] for j in range(128))
+                    dot_s = 0.0
+                    for i in range(128):
+                        sq_i = sum(float(cache.proj[i, j]) * qt[j] for j in range(128))
+                        dot_s += sq_i * (1.0 if bits[i] else -1.0)
+                    est = float(cache.k["norm"][0, 0, 0, t]) * (
+                        dot_c + math.sqrt(math.pi / 2) / 128 * float(cache.k["gamma"][0, 0, 0, t]) * dot_s)
+                    lg = est / math.sqrt(128)
+                else:
+                    code = cache.k["code"][0, 0, 0, t]
+                    kv = [sk[j] * (float(cache.k["zero"][0, 0, 0, t, j // 32]) +
+                                   float(np.float32(cache.k["scale"][0, 0, 0, t, j // 32]) * np.float32(code[j])))
+                          for j in range(128)]
+                    lg = sum(qt[j] * kv[j] for j in range(128)) / math.sqrt(128)
                 vc = cache.v["code"][0, 0, 0, t]
-                vr = np.array([float(cache.v["zero"][0, 0, 0, t, j // 32]) +
-                               float(np.float32(cache.v["scale"][0, 0, 0, t, j // 32]) * np.float32(vc[j]))
+                vr = np.array([sv[j] * (float(cache.v["zero"][0, 0, 0, t, j // 32]) +
+                                        float(np.float32(cache.v["scale"][0, 0, 0, t, j // 32]) * np.float32(vc[j])))
                                for j in range(128)])
                 vals.append(s * (codec.hadamard_butterfly(vr) * float(codec.C_WHT)))
             else:
-                kw = cache.ring_k[0, 0, 0, t % W].astype(np.float64)
-                lg = sum(float(qh[j]) * kw[j] for j in range(128)) / math.sqrt(128)
-                vals.append(cache.ring_v[0, 0, 0, t % W].astype(np.float64))
+                lg = sum(float(qh[j]) * float(k_raw[t, j]) for j in range(128)) / math.sqrt(128)
+                vals.append(v_raw[t].astype(np.float64))
             ws.append(lg)
         m = max(ws)
         e = [math.exp(w - m) for w in ws]
@@ -306,7 +424,7 @@ def _brute_force_unit(cache, q, L):
     return np.array(outs)
 
 
-@pytest.mark.parametrize("window,L", [(4, 9), (0, 6), (2, 2), (8, 3)])
+@pytest.mark.parametrize("window,L", [(4, 9), (0, 6), (2, 2), (8, 3), (4, 13)])
 def test_decode_matches_brute_force_on_tiny_inputs(window, L):
     rng = np.random.default_rng(13)
     c = _cache(window, 16, seed=5)
@@ -315,7 +433,87 @@ def test_decode_matches_brute_force_on_tiny_inputs(window, L):
     c.append(0, k, v, np.array([0]))
     q = rng.standard_normal((1, 2, 128)).astype(np.float32)
     out = c.decode(0, q, np.array([L]))
-    assert np.allclose(out[0], _brute_force_unit(c, q[0], L), rtol=0, atol=1e-10)
+    assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
+
+
+@pytest.mark.parametrize("window,L", [(4, 9), (0, 5)])
+def test_decode_tq_keys_matches_brute_force(window, L):
+    rng = np.random.default_rng(17)
+    proj = rng.standard_normal((128, 128)).astype(np.float32)
+    c = _cache(window, 16, kfmt=attention.TQ3_QJL, seed=2, proj=proj)
+    k = (rng.standard_normal((1, 1, L, 128)) * 2).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
+
+
+def _planted_column_block(rng, n, cscale, signs):
+    """Raw vectors whose ROTATED coordinates have column RMS ``cscale`` (unit-RMS Gaussian core)."""
+    a = rng.standard_normal((n, 128))
+    a /= np.sqrt((a ** 2).mean(0))
+    return codec.unrotate((a * cscale).astype(np.float32), signs)
+
+
+def test_decode_balanced_matches_brute_force():
+    rng = np.random.default_rng(18)
+    c = _cache(4, 16, sink=True, seed=1)
+    ck = np.exp(rng.uniform(np.log(0.1), np.log(10), 128))
+    cv = np.exp(rng.uniform(np.log(0.1), np.log(10), 128))
+    c.calibrate(0, _planted_column_block(rng, 256, ck, c.signs)[None],
+                _planted_column_block(rng, 256, cv, c.signs)[None])
+    assert not np.all(c.sigma_k == 1) and not np.all(c.sigma_v == 1)
+    L = 11
+    k = _planted_column_block(rng, L, ck, c.signs)[None, None]
+    v = _planted_column_block(rng, L, cv, c.signs)[None, None]
+    c.append(0, k, v, np.array([0]))
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
+
+
+def test_balanced_records_reconstruct_the_rotated_input():
+    """[KV] TLDR: the balanced value y / sigma is what is quantised, so sigma * dequant(code) is y
+    to within half a quantisation step of the balanced group (times sigma) plus fp16 rounding."""
+    rng = np.random.default_rng(19)
+    c = _cache(0, 64, sink=True, seed=4)
+    ck = np.exp(rng.uniform(np.log(0.05), np.log(20), 128))
+    cv = np.exp(rng.uniform(np.log(0.05), np.log(20), 128))
+    c.calibrate(0, _planted_column_block(rng, 512, ck, c.signs)[None],
+                _planted_column_block(rng, 512, cv, c.signs)[None])
+    for sg16, cs in ((c.sigma_k, ck), (c.sigma_v, cv)):    # each from its own block
+        ratio = sg16[0, 0].astype(np.float64) / cs
+        assert np.std(ratio) / np.mean(ratio) < 0.03
+    k = _planted_column_block(rng, 64, ck, c.signs)[None, None]
+    v = _planted_column_block(rng, 64, cv, c.signs)[None, None]
+    c.append(0, k, v, np.array([0]))
+    for rec, sg16, x in ((c.k, c.sigma_k, k), (c.v, c.sigma_v, v)):
+        sig = sg16[0, 0].astype(np.float64)
+        y = codec.rotate(x[0, 0], c.signs).astype(np.float64)
+        deq = codec.q4g32_decode(rec["code"][0, 0, 0], rec["scale"][0, 0, 0], rec["zero"][0, 0, 0])
+        sg = np.repeat(rec["scale"][0, 0, 0].astype(np.float64), 32, axis=-1)
+        zg = np.repeat(rec["zero"][0, 0, 0].astype(np.float64), 32, axis=-1)
+        bound = sig * (0.5 * sg + 2.0 ** -10 * (np.abs(zg) + 15 * sg)) + 2.0 ** -20 * np.abs(y) + 1e-6
+        assert np.all(np.abs(sig * deq - y) <= bound)
+
+
+def test_gqa_query_head_i_reads_kv_head_i_div_g():
+    """Grouped-query attention (Llama convention): query head i attends with kv-head i // g; each
+    sequence attends to its own first seq_lens[b] tokens."""
+    rng = np.random.default_rng(20)
+    B, H, Hq, T = 2, 2, 6, 60
+    c = _cache(128, 64, B=B, H=H, Hq=Hq)
+    k = rng.standard_normal((B, H, T, 128)).astype(np.float32)
+    v = rng.standard_normal((B, H, T, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0, 0]))
+    q = rng.standard_normal((B, Hq, 128)).astype(np.float32)
+    lens = np.array([T, 37])
+    out = c.decode(0, q, lens)
+    for b in range(B):
+        for i in range(Hq):
+            ref = attention.plain_attention64(q[b, i:i + 1], k[b, i // 3, :lens[b]], v[b, i // 3, :lens[b]])
+            assert np.allclose(out[b, i], ref[0], rtol=0, atol=1e-12)
 
 
 def test_bulk_append_equals_token_by_token():
@@ -330,6 +528,34 @@ def test_bulk_append_equals_token_by_token():
     for name in ("code", "scale", "zero"):
         assert np.array_equal(a.k[name], b.k[name]) and np.array_equal(a.v[name], b.v[name])
     assert np.array_equal(a.ring_k, b.ring_k) and np.array_equal(a.ring_v, b.ring_v)
+
+
+def test_append_skips_sequences_with_negative_position():
+    """pos[b] < 0 leaves sequence b untouched (records and ring), the others are written."""
+    rng = np.random.default_rng(26)
+    c = _cache(8, 32, B=3, H=1, Hq=2)
+    k = rng.standard_normal((3, 1, 5, 128)).astype(np.float32)
+    c.append(0, k, k, np.array([-1, 2, -1]))
+    for rec in (c.k, c.v):
+        for name in ("code", "scale", "zero"):
+            assert not rec[name][0, 0].any() and not rec[name][0, 2].any()
+            assert rec[name][0, 1, 0, 2:7].any()
+    assert not c.ring_k[0, 0].any() and not c.ring_k[0, 2].any() and c.ring_k[0, 1].any()
+
+
+def test_large_logits_stay_finite():
+    """The softmax is taken relative to the running maximum, so logits of order 10^4 neither
+    overflow nor lose the result (scipy's softmax as the reference)."""
+    rng = np.random.default_rng(27)
+    L = 40
+    c = _cache(128, 64)
+    k = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = (rng.standard_normal((1, 2, 128)) * 1000).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    ref = attention.plain_attention64(q[0], k[0, 0], v[0, 0])
+    assert np.all(np.isfinite(out)) and np.allclose(out[0], ref, rtol=0, atol=1e-12)
 
 
 def test_empty_sequence_gives_zero_output():
