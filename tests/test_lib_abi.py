@@ -81,3 +81,65 @@ def test_llama_3b_32k_quantised_store_is_6_4x_smaller_than_fp32(kvq):
     b = lib.kv_cache_bytes(flat)
     fp32 = attention.fp32_kv_bytes(28, 8, 32768)
     assert abs(fp32 / b - 6.4) < 0.01
+
+
+# ------------------------------------------------------------------ host-side argument checks
+# Only inputs that the library rejects before its first CUDA call: no device is touched, and the
+# fake device addresses below are never dereferenced.
+KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_ALIGN = 0, 1, 2, 3
+KVQ_ERR_CAPACITY, KVQ_ERR_CUDA, KVQ_ERR_NOT_INIT = 4, 5, 6
+FAKE_DEV = 0x7F0000000000          # 16-byte aligned, never dereferenced
+
+
+def test_strerror_names_every_status_code(kvq):
+    msgs = [lib.kv_strerror(c) for c in range(7)]
+    assert len(set(msgs)) == 7 and not any("unknown" in m for m in msgs)
+    assert "align" in msgs[KVQ_ERR_ALIGN] and "initialised" in msgs[KVQ_ERR_NOT_INIT]
+
+
+def test_cache_init_rejects_bad_arguments_before_any_device_work(kvq):
+    import ctypes
+
+    cfg = lib.make_config(2, 8, 24, 1, 1024)
+    need = lib.kv_cache_bytes(cfg)
+    cache = lib.kvq_cache()
+    init = kvq.kv_cache_init
+    P = ctypes.c_void_p
+    assert init(None, ctypes.byref(cfg), P(FAKE_DEV), need, None, None, None) == KVQ_ERR_INVALID_ARG
+    assert init(ctypes.byref(cache), None, P(FAKE_DEV), need, None, None, None) == KVQ_ERR_INVALID_ARG
+    assert init(ctypes.byref(cache), ctypes.byref(cfg), None, need, None, None, None) == KVQ_ERR_INVALID_ARG
+    bad = lib.make_config(2, 8, 24, 1, 1024, window=102)
+    assert init(ctypes.byref(cache), ctypes.byref(bad), P(FAKE_DEV), need, None, None, None) == KVQ_ERR_UNSUPPORTED
+    assert init(ctypes.byref(cache), ctypes.byref(cfg), P(FAKE_DEV), need - 1, None, None, None) == KVQ_ERR_CAPACITY
+    assert init(ctypes.byref(cache), ctypes.byref(cfg), P(FAKE_DEV + 8), need, None, None, None) == KVQ_ERR_ALIGN
+    assert init(ctypes.byref(cache), ctypes.byref(cfg), P(FAKE_DEV), need, P(FAKE_DEV + 4), None,
+                None) == KVQ_ERR_ALIGN
+    tq = lib.make_config(2, 8, 24, 1, 1024, k_format=lib.KVQ_TQ3_QJL)
+    assert init(ctypes.byref(cache), ctypes.byref(tq), P(FAKE_DEV), lib.kv_cache_bytes(tq), None, None,
+                None) == KVQ_ERR_INVALID_ARG          # TurboQuant keys need the projection matrix
+    assert cache.magic == 0                          # nothing was initialised
+
+
+def test_uninitialised_cache_is_refused_by_every_entry_point(kvq):
+    import ctypes
+
+    cache = lib.kvq_cache()                           # zeroed: never passed through kv_cache_init
+    cache.cfg = lib.make_config(2, 8, 24, 1, 1024)
+    c = ctypes.byref(cache)
+    P = ctypes.c_void_p
+    d = P(FAKE_DEV)
+    flags = ctypes.c_uint32(0)
+    assert kvq.kv_calibrate(c, 0, d, d, 64, d, 1 << 20, None) == KVQ_ERR_NOT_INIT
+    assert kvq.kv_quant_append(c, 0, d, d, d, 1, 1, None) == KVQ_ERR_NOT_INIT
+    assert kvq.kv_decode_attention(c, 0, d, d, d, 1, d, 1 << 20, None) == KVQ_ERR_NOT_INIT
+    assert kvq.kv_decode_attention_noalloc(c, 0, d, d, d, 1, None) == KVQ_ERR_NOT_INIT
+    assert kvq.kv_status(c, ctypes.byref(flags), None) == KVQ_ERR_NOT_INIT
+    assert kvq.kv_calibrate_scratch_bytes(c, 0, 64) == 0
+    assert kvq.kv_decode_scratch_bytes(c, 0, 1) == 0
+    # and a NULL cache
+    assert kvq.kv_quant_append(None, 0, d, d, d, 1, 1, None) == KVQ_ERR_INVALID_ARG
+    assert kvq.kv_decode_attention_noalloc(None, 0, d, d, d, 1, None) == KVQ_ERR_INVALID_ARG
+
+
+def test_cache_bytes_null_config(kvq):
+    assert kvq.kv_cache_bytes(None) == 0
