@@ -14,7 +14,8 @@ what the method computes, written from the source pages:
   ("TLDR" paragraph).
 * [TQ] "LLM memory saving: weights vs KV-cache quantization (2026)" (conanssam.com) -- random
   rotation, per-coordinate optimal scalar quantiser, 1-bit QJL sketch of the residual for an
-  unbiased inner product ("method comparison" table, "key idea" row).
+  unbiased inner product ("method comparison" table, "key idea" row); K kept at 8 bits while V
+  is cut to low bits as the safe asymmetric setting ("when to use what" and "rules" lists).
 
 Codec arithmetic is IEEE float32 in a fixed operation order with no fused multiply-add (every
 numpy ufunc call below rounds once), because the codes it decides must match the GPU bit for bit.

@@ -21,8 +21,10 @@ from . import codec
 
 F32 = np.float32
 Q4G32 = "q4g32"
+Q8G32 = "q8g32"
 TQ3_QJL = "tq3_qjl"
 REC_BYTES = {Q4G32: 64 + 8 + 8,          # 128 nibbles, 4 fp16 scales, 4 fp16 zeros
+             Q8G32: 128 + 8,             # 128 signed bytes, 4 fp16 scales
              TQ3_QJL: 48 + 16 + 2 + 2}   # 128 x 3-bit codes, 128 sign bits, fp16 norm, fp16 gamma
 
 
@@ -75,6 +77,9 @@ class OracleCache:
                           bits=np.zeros((L, B, H, P, codec.D), bool),
                           norm=np.zeros((L, B, H, P), np.float16),
                           gamma=np.zeros((L, B, H, P), np.float16))
+        elif cfg.k_format == Q8G32:
+            self.k = dict(code=np.zeros((L, B, H, P, codec.D), np.int8),
+                          scale=np.zeros((L, B, H, P, 4), np.float16))
         else:
             self.k = dict(code=np.zeros((L, B, H, P, codec.D), np.uint8),
                           scale=np.zeros((L, B, H, P, 4), np.float16),
@@ -97,11 +102,14 @@ class OracleCache:
             self.sigma_v[layer, h] = codec.sinkhorn_sigma(codec.rotate(v_calib[h], self.signs))
 
     # ---------------------------------------------------------------- append
-    def _encode_q4(self, x: np.ndarray, sigma: np.ndarray | None):
+    def _balanced(self, x: np.ndarray, sigma: np.ndarray | None):
         y = codec.rotate(x, self.signs)
         if sigma is not None:
             y = y / sigma.astype(F32)          # balanced value y / sigma (float32 division)
-        return codec.q4g32_encode(y)
+        return y
+
+    def _encode_q4(self, x: np.ndarray, sigma: np.ndarray | None):
+        return codec.q4g32_encode(self._balanced(x, sigma))
 
     def append(self, layer: int, k: np.ndarray, v: np.ndarray, pos: np.ndarray):
         """Append T tokens per sequence: k, v [B][H][T][128] float32; pos [B] first position."""
@@ -123,6 +131,10 @@ class OracleCache:
                     self.k["bits"][layer, b, h, sl] = bits
                     self.k["norm"][layer, b, h, sl] = n
                     self.k["gamma"][layer, b, h, sl] = g
+                elif cfg.k_format == Q8G32:
+                    c, s = codec.q8g32_encode(self._balanced(k[b, h], sk))
+                    self.k["code"][layer, b, h, sl] = c
+                    self.k["scale"][layer, b, h, sl] = s
                 else:
                     c, s, z = self._encode_q4(k[b, h], sk)
                     self.k["code"][layer, b, h, sl] = c
@@ -172,8 +184,12 @@ class OracleCache:
                 lq = np.stack([codec.tq3_qjl_dot64(qt[i], kk["code"], kk["bits"], kk["norm"],
                                                    kk["gamma"], self.proj) for i in range(g)])
             else:
-                kd = codec.q4g32_decode(self.k["code"][layer, b, h, :Lq], self.k["scale"][layer, b, h, :Lq],
-                                        self.k["zero"][layer, b, h, :Lq]).astype(np.float64)
+                if cfg.k_format == Q8G32:
+                    kd = codec.q8g32_decode(self.k["code"][layer, b, h, :Lq],
+                                            self.k["scale"][layer, b, h, :Lq]).astype(np.float64)
+                else:
+                    kd = codec.q4g32_decode(self.k["code"][layer, b, h, :Lq], self.k["scale"][layer, b, h, :Lq],
+                                            self.k["zero"][layer, b, h, :Lq]).astype(np.float64)
                 if cfg.sinkhorn:
                     kd = kd * self.sigma_k[layer, h].astype(np.float64)
                 lq = qt @ kd.T                                                    # [g][Lq]

@@ -154,6 +154,35 @@ def q4g32_decode(code: np.ndarray, scale: np.ndarray, zero: np.ndarray) -> np.nd
 
 
 # --------------------------------------------------------------------------------------------
+# 8-bit symmetric group quantiser (Q8G32) for keys kept at 8 bits
+# --------------------------------------------------------------------------------------------
+def q8g32_encode(y: np.ndarray):
+    """8-bit codes with one fp16 scale per group of 32 consecutive channels, no zero point.
+
+    [TQ] "when to use what" and "rules" lists: keep K at Q8 and cut only V to low bits.  The page
+    names the llama.cpp cache type without defining it; reading: its 8-bit block format (32 values,
+    one fp16 scale d = max|y| / 127, signed codes).  Per group: d = f16(f32(max |y|) / 127);
+    code = clamp(rint(y / f32(d)), -127, 127) with round-half-even against the STORED scale, or 0
+    when d == 0.  Returns (codes int8 [...,128], d f16 [...,4]).
+    """
+    y = np.asarray(y, dtype=F32)
+    g = y.reshape(y.shape[:-1] + (N_GROUPS, GROUP))
+    amax = np.abs(g).max(axis=-1)
+    d = (amax / F32(127.0)).astype(F16)
+    df = d.astype(F32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = g / df
+    code = np.where(df > 0, np.clip(np.rint(t), -127, 127), 0).astype(np.int8)
+    return code.reshape(y.shape), d
+
+
+def q8g32_decode(code: np.ndarray, d: np.ndarray) -> np.ndarray:
+    """Dequantised value f32(d * code) (one rounding; exact, since |code| < 2^8 and d is fp16)."""
+    c = np.asarray(code).reshape(code.shape[:-1] + (N_GROUPS, GROUP)).astype(F32)
+    return (d.astype(F32)[..., None] * c).reshape(code.shape)
+
+
+# --------------------------------------------------------------------------------------------
 # Lloyd-Max scalar quantiser for a Gaussian and the 3-bit TurboQuant key codec
 # --------------------------------------------------------------------------------------------
 def lloyd_max_gaussian(levels: int = 8, tol: float = 1e-15, max_iter: int = 200000):

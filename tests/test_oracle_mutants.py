@@ -42,6 +42,17 @@ MUTANTS = [
     ("codec.py", "out = zero.astype(F32)[..., None] + scale.astype(F32)[..., None] * c",
                  "out = (zero.astype(F32)[..., None] / scale.astype(F32)[..., None] + c)"
                  " * scale.astype(F32)[..., None]"),
+    # Q8G32 keys
+    ("codec.py", "d = (amax / F32(127.0)).astype(F16)", "d = (amax / F32(128.0)).astype(F16)"),
+    ("codec.py", "amax = np.abs(g).max(axis=-1)", "amax = g.max(axis=-1)"),
+    ("codec.py", "code = np.where(df > 0, np.clip(np.rint(t), -127, 127), 0)",
+                 "code = np.where(df > 0, np.clip(np.trunc(t), -127, 127), 0)"),
+    ("codec.py", "return (d.astype(F32)[..., None] * c).reshape(code.shape)",
+                 "return (d.astype(F32)[..., None] * (c + F32(0.5))).reshape(code.shape)"),
+    ("attention.py", "c, s = codec.q8g32_encode(self._balanced(k[b, h], sk))",
+                     "c, s = codec.q8g32_encode(codec.rotate(k[b, h], self.signs))"),
+    ("attention.py", "kd = codec.q8g32_decode(self.k[\"code\"][layer, b, h, :Lq],",
+                     "kd = -codec.q8g32_decode(self.k[\"code\"][layer, b, h, :Lq],"),
     # Lloyd-Max codebook and TQ3 + QJL keys
     ("codec.py", "b = 0.5 * (c[:-1] + c[1:])\n        edges", "b = 0.45 * (c[:-1] + c[1:])\n        edges"),
     ("codec.py", "cent = (c64 / np.sqrt(128.0)).astype(F16)", "cent = (c64 / np.sqrt(127.0)).astype(F16)"),

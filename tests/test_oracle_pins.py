@@ -179,6 +179,77 @@ def test_q4_ties_round_to_even():
     assert list(c[:9]) == [0, 15, 0, 2, 2, 4, 4, 14, 14]
 
 
+# ------------------------------------------------------------------ Q8G32 (8-bit keys)
+def test_q8_on_grid_round_trip_is_lossless():
+    """Inputs d * c with a power-of-two d and integer c in [-127, 127], one |c| = 127 per group."""
+    rng = np.random.default_rng(30)
+    for _ in range(20):
+        d = np.float32(2.0 ** rng.integers(-12, 2))
+        codes = rng.integers(-127, 128, (4, 32))
+        codes[:, 0] = 127 * rng.choice([-1, 1], 4)
+        y = (d * codes.astype(np.float32)).reshape(128)
+        c, dc = codec.q8g32_encode(y)
+        assert np.array_equal(c, codes.reshape(128).astype(np.int8))
+        assert np.all(dc.astype(np.float32) == d)
+        assert np.array_equal(codec.q8g32_decode(c, dc), y)
+
+
+def test_q8_codes_are_nearest_grid_points():
+    """Brute force over the 255 levels d * c; error at most half a step plus the fp16 rounding of d
+    (which can push max |y| / d just past 127, where the code clips)."""
+    rng = np.random.default_rng(31)
+    y = (rng.standard_normal((200, 128)) * rng.uniform(0.01, 50, (200, 1))).astype(np.float32)
+    c, d = codec.q8g32_encode(y)
+    dg = np.repeat(d.astype(np.float64), 32, axis=-1)
+    grid = dg[..., None] * np.arange(-127, 128)
+    dist = np.abs(y.astype(np.float64)[..., None] - grid)
+    best = dist.argmin(-1) - 127
+    sd = np.sort(dist, -1)
+    tie = sd[..., 1] - sd[..., 0] < 1e-6 * dg
+    assert np.array_equal(c[~tie].astype(np.int64), best[~tie])
+    amax = np.repeat(np.abs(y.reshape(200, 4, 32)).max(-1).astype(np.float64), 32, axis=-1)
+    err = np.abs(codec.q8g32_decode(c, d).astype(np.float64) - y)
+    assert np.all(err <= 0.5 * dg + 2.0 ** -11 * amax * 1.01)
+
+
+def test_q8_zero_group_sign_symmetry_and_ties():
+    z = np.zeros(128, np.float32)
+    c, d = codec.q8g32_encode(z)
+    assert np.all(c == 0) and np.all(d == 0)
+    rng = np.random.default_rng(32)
+    y = rng.standard_normal((50, 128)).astype(np.float32)
+    c1, d1 = codec.q8g32_encode(y)
+    c2, d2 = codec.q8g32_encode(-y)
+    assert np.array_equal(c2, -c1) and np.array_equal(d2, d1)
+    # a group with max |y| = 127 has d = 1: halves go to the even code (IEEE round-half-even)
+    y = np.zeros(128, np.float32)
+    y[:8] = [127, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 126.5]
+    c, d = codec.q8g32_encode(y)
+    assert d[0] == 1 and list(c[:8]) == [127, 0, 2, 2, 0, -2, -2, 126]
+
+
+def test_q8_key_record_is_8_5_bits():
+    """An 8-bit block format of 32 values with one fp16 scale stores 34 bytes per 32 values."""
+    assert attention.REC_BYTES[attention.Q8G32] * 8 / 128 == 8.5
+    cfg = attention.OracleConfig(1, 1, 1, 1, 1, k_format=attention.Q8G32)
+    assert attention.payload_bytes_per_token_head(cfg) == 136 + 80
+
+
+def test_q8_keys_score_far_closer_than_q4_keys():
+    """[TQ] "rules": K at Q8 is the safe setting.  On outlier-bearing keys the Q8 logit error is at
+    least ten times below the Q4 one (step 2 max|y| / 254 against (max - min) / 15)."""
+    rng = np.random.default_rng(33)
+    k = rng.standard_normal((1000, 128)).astype(np.float32)
+    k[:, :3] *= 8
+    s = codec.wht_signs(0)
+    y = codec.rotate(k, s)
+    q = rng.standard_normal(128)
+    true = y.astype(np.float64) @ q
+    e8 = np.abs(codec.q8g32_decode(*codec.q8g32_encode(y)).astype(np.float64) @ q - true).mean()
+    e4 = np.abs(codec.q4g32_decode(*codec.q4g32_encode(y)).astype(np.float64) @ q - true).mean()
+    assert e8 * 10 < e4
+
+
 # ------------------------------------------------------------------ Lloyd-Max / TQ3
 def test_lloyd_max_matches_textbook_table():
     rows = _golden_rows("lloyd_max_gaussian_8.txt")
@@ -402,6 +473,11 @@ def _brute_force_unit(cache, q, L, k_raw, v_raw):
                     est = float(cache.k["norm"][0, 0, 0, t]) * (
                         dot_c + math.sqrt(math.pi / 2) / 128 * float(cache.k["gamma"][0, 0, 0, t]) * dot_s)
                     lg = est / math.sqrt(128)
+                elif cfg.k_format == attention.Q8G32:
+                    code = cache.k["code"][0, 0, 0, t]
+                    kv = [sk[j] * float(np.float32(cache.k["scale"][0, 0, 0, t, j // 32]) * np.float32(code[j]))
+                          for j in range(128)]
+                    lg = sum(qt[j] * kv[j] for j in range(128)) / math.sqrt(128)
                 else:
                     code = cache.k["code"][0, 0, 0, t]
                     kv = [sk[j] * (float(cache.k["zero"][0, 0, 0, t, j // 32]) +
@@ -449,6 +525,21 @@ def test_decode_tq_keys_matches_brute_force(window, L):
     assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
 
 
+@pytest.mark.parametrize("window,L,sink", [(4, 9, False), (0, 5, False), (4, 10, True)])
+def test_decode_q8_keys_matches_brute_force(window, L, sink):
+    rng = np.random.default_rng(34)
+    c = _cache(window, 16, kfmt=attention.Q8G32, seed=6, sink=sink)
+    if sink:
+        blk = (rng.standard_normal((1, 256, 128)) * np.exp(rng.uniform(-2, 2, 128))).astype(np.float32)
+        c.calibrate(0, blk, blk * np.float32(0.5))
+    k = (rng.standard_normal((1, 1, L, 128)) * 2).astype(np.float32)
+    v = rng.standard_normal((1, 1, L, 128)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = rng.standard_normal((1, 2, 128)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))
+    assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
+
+
 def _planted_column_block(rng, n, cscale, signs):
     """Raw vectors whose ROTATED coordinates have column RMS ``cscale`` (unit-RMS Gaussian core)."""
     a = rng.standard_normal((n, 128))
@@ -473,11 +564,12 @@ def test_decode_balanced_matches_brute_force():
     assert np.allclose(out[0], _brute_force_unit(c, q[0], L, k[0, 0], v[0, 0]), rtol=0, atol=1e-10)
 
 
-def test_balanced_records_reconstruct_the_rotated_input():
+@pytest.mark.parametrize("kfmt", [attention.Q4G32, attention.Q8G32])
+def test_balanced_records_reconstruct_the_rotated_input(kfmt):
     """[KV] TLDR: the balanced value y / sigma is what is quantised, so sigma * dequant(code) is y
     to within half a quantisation step of the balanced group (times sigma) plus fp16 rounding."""
     rng = np.random.default_rng(19)
-    c = _cache(0, 64, sink=True, seed=4)
+    c = _cache(0, 64, sink=True, seed=4, kfmt=kfmt)
     ck = np.exp(rng.uniform(np.log(0.05), np.log(20), 128))
     cv = np.exp(rng.uniform(np.log(0.05), np.log(20), 128))
     c.calibrate(0, _planted_column_block(rng, 512, ck, c.signs)[None],
@@ -491,10 +583,15 @@ def test_balanced_records_reconstruct_the_rotated_input():
     for rec, sg16, x in ((c.k, c.sigma_k, k), (c.v, c.sigma_v, v)):
         sig = sg16[0, 0].astype(np.float64)
         y = codec.rotate(x[0, 0], c.signs).astype(np.float64)
-        deq = codec.q4g32_decode(rec["code"][0, 0, 0], rec["scale"][0, 0, 0], rec["zero"][0, 0, 0])
         sg = np.repeat(rec["scale"][0, 0, 0].astype(np.float64), 32, axis=-1)
-        zg = np.repeat(rec["zero"][0, 0, 0].astype(np.float64), 32, axis=-1)
-        bound = sig * (0.5 * sg + 2.0 ** -10 * (np.abs(zg) + 15 * sg)) + 2.0 ** -20 * np.abs(y) + 1e-6
+        if "zero" in rec:
+            deq = codec.q4g32_decode(rec["code"][0, 0, 0], rec["scale"][0, 0, 0], rec["zero"][0, 0, 0])
+            zg = np.repeat(rec["zero"][0, 0, 0].astype(np.float64), 32, axis=-1)
+            step = 0.5 * sg + 2.0 ** -10 * (np.abs(zg) + 15 * sg)
+        else:
+            deq = codec.q8g32_decode(rec["code"][0, 0, 0], rec["scale"][0, 0, 0])
+            step = 0.5 * sg + 2.0 ** -11 * 127 * sg * 1.01
+        bound = sig * step + 2.0 ** -20 * np.abs(y) + 1e-6
         assert np.all(np.abs(sig * deq - y) <= bound)
 
 
