@@ -162,6 +162,10 @@ int kv_calibrate(kvq_cache* cache, int32_t layer, const void* k_calib, const voi
  *   k, v       device, cfg.in_dtype, [L?][batch][n_kv_heads][n_tokens][128], contiguous
  *   pos        device int32 [batch]; pos[b] < 0 leaves sequence b untouched (lets a caller
  *              append ragged chunks to a subset of the batch)
+ * Value range: scales, zeros, norms and sigma are stored as fp16, so each vector must be finite
+ * with Euclidean norm below 65504 (after division by sigma when balanced; the rotation keeps the
+ * norm).  Outside that range the stored metadata is infinite or NaN and the codes are undefined;
+ * nothing is flagged.
  */
 int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* v,
                     const int32_t* pos, int32_t batch, int32_t n_tokens, void* stream);
