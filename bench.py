@@ -438,40 +438,176 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------------ CPU oracle
-def cpu_baseline(w, layers, lens, budget_s=12.0, max_units=3):
-    """Time the oracle's decode on a few (layer, kv-head) units of this workload (their encode is
-    not timed), repeating until ``budget_s`` of decode time, and scale to one full step."""
-    from oracle import attention
+ORACLE_CPU_WORK_S = 24.0      # CPU-seconds of oracle decode per baseline sample (all workers)
 
+
+def _oracle_units(w, layers, lens, n):
+    """``n`` (layer, sequence) units spread over the workload: their seeded K/V, q and length."""
     H, Hq = w["n_kv_heads"], w["n_q_heads"]
     g = Hq // H
-    proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
-    picks = [(l, int(b)) for l, b in zip(range(max_units), np.linspace(0, len(lens) - 1, max_units).astype(int))]
+    seqs = np.linspace(0, len(lens) - 1, n).round().astype(int)
     units = []
-    for layer, b in picks:
+    for i in range(n):
+        layer, b = i % layers, int(seqs[i])
         L = int(lens[b])
-        ocfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=g, max_batch=1, max_seq_len=L,
-                                      window=w["window"], k_format=w["k_format"], sinkhorn=w["sinkhorn"],
-                                      seed=w["wht_seed"])
-        ora = attention.OracleCache(ocfg, proj)
         k, v = synth.kv_tokens(w, layer, 1, 1, 0, L, device="cpu")
-        ora.append(0, k.float().numpy(), v.float().numpy(), np.array([0]))
         q = synth.queries(w, layer, 1, g, device="cpu").float().numpy()
-        units.append((ora, q, L))
+        units.append((L, k.float().numpy(), v.float().numpy(), q))
+    return units
+
+
+def _oracle_cache(w, unit, proj):
+    from oracle import attention
+
+    L, k, v, q = unit
+    ocfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=q.shape[1], max_batch=1,
+                                  max_seq_len=L, window=w["window"], k_format=w["k_format"],
+                                  sinkhorn=w["sinkhorn"], seed=w["wht_seed"])
+    ora = attention.OracleCache(ocfg, proj)
+    ora.append(0, k, v, np.array([0]))      # encode: not timed
+    return ora
+
+
+def _time_decode(ora, q, L, budget_s):
+    """Repeat the oracle's decode of one unit until ``budget_s`` seconds of it have run."""
     spent, tokens, n = 0.0, 0, 0
-    while spent < budget_s or n < len(units):
-        ora, q, L = units[n % len(units)]
+    while spent < budget_s or n < 1:
         t = time.perf_counter()
         ora.decode(0, q, np.array([L]))
         spent += time.perf_counter() - t
         tokens += L
         n += 1
-    per_token_head = spent / tokens                      # seconds per (token, kv-head) attended
-    step_s = per_token_head * float(lens.sum()) * H * w["n_layers"]  # the whole model's step
-    return {"value": float(lens.sum()) / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"numpy oracle decode of {len(units)} (layer, kv-head) units ({n} timed calls, "
-                      f"{spent:.1f} s), scaled by tokens to the {w['n_layers'] * len(lens) * H} units of one "
-                      f"step; their encode not timed; one thread"}
+    return tokens, spent, n
+
+
+def _oracle_worker(conn, w, unit, proj):
+    """Spawned process, one BLAS thread: encode one unit, then time its decode once per budget
+    received on ``conn`` and send back (tokens, seconds, calls); ``None`` ends the process."""
+    try:
+        ora = _oracle_cache(w, unit, proj)
+        L, _, _, q = unit
+        ora.decode(0, q, np.array([L]))     # warm-up call
+        conn.send("ready")
+        while True:
+            budget = conn.recv()
+            if budget is None:
+                break
+            conn.send(_time_decode(ora, q, L, budget))
+    except Exception as e:                  # reported to the parent, which then gives up the pool
+        conn.send(("error", repr(e)))
+    finally:
+        conn.close()
+
+
+class OracleTimer:
+    """One spawned worker process per host core, each holding one oracle unit of the workload.
+
+    ``step(budget)`` has every worker time its unit's decode for ``budget`` seconds at the same
+    time, so the sum of the workers' rates is the oracle's throughput on all cores.
+    """
+
+    def __init__(self, w, layers, lens, procs: int, timeout_s: float = 900.0):
+        import multiprocessing as mp
+
+        self.w, self.procs, self.timeout = w, procs, timeout_s
+        proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
+        units = _oracle_units(w, layers, lens, procs)
+        ctx = mp.get_context("spawn")       # never fork a process that holds a CUDA context
+        self.conns, self.workers = [], []
+        for u in units:
+            a, b = ctx.Pipe()
+            pr = ctx.Process(target=_oracle_worker, args=(b, w, u, proj), daemon=True)
+            pr.start()
+            b.close()
+            self.conns.append(a)
+            self.workers.append(pr)
+        for c in self.conns:
+            self._recv(c, "ready")
+
+    def _recv(self, c, want=None):
+        if not c.poll(self.timeout):
+            raise RuntimeError("oracle worker timed out")
+        m = c.recv()
+        if isinstance(m, tuple) and m and m[0] == "error":
+            raise RuntimeError(f"oracle worker failed: {m[1]}")
+        if want is not None and m != want:
+            raise RuntimeError(f"oracle worker sent {m!r}")
+        return m
+
+    def step(self, budget_s: float):
+        for c in self.conns:
+            c.send(budget_s)
+        return [self._recv(c) for c in self.conns]
+
+    def close(self):
+        for c in self.conns:
+            try:
+                c.send(None)
+            except (BrokenPipeError, OSError):
+                pass
+        for pr in self.workers:
+            pr.join(timeout=30)
+            if pr.is_alive():
+                pr.terminate()
+                pr.join(timeout=30)
+
+
+def _baseline_record(w, layers, lens, results, procs, budget_s, all_cores: bool):
+    """cpu_baseline object from per-unit (tokens, seconds, calls).  Rates add across workers that
+    ran at the same time; units timed one after another in one thread give tokens / seconds.  One
+    step attends every cached token once per (layer, kv-head), over the ``layers`` the GPU step
+    covers."""
+    H = w["n_kv_heads"]
+    if all_cores:
+        rates = [t / s for t, s, _ in results]          # token-heads per second, per worker
+        rate, per_core_rate = sum(rates), sum(rates) / len(rates)
+    else:
+        rate = per_core_rate = sum(t for t, _, _ in results) / sum(s for _, s, _ in results)
+    step_token_heads = float(lens.sum()) * H * layers
+    value = float(lens.sum()) / (step_token_heads / rate)
+    per_core = float(lens.sum()) / (step_token_heads / per_core_rate)
+    calls = sum(n for _, _, n in results)
+    how = (f"{procs} spawned processes, one BLAS thread each, each timing its own (layer, sequence, "
+           f"kv-head) unit concurrently for {budget_s:.2f} s" if all_cores else
+           "one thread in this process (the worker pool was not available)")
+    return {"value": value, "unit": "tokens/s", "cores": procs if all_cores else 1, "kind": "oracle",
+            "per_core_value": per_core,
+            "sample": f"numpy oracle decode of {len(results)} units ({calls} timed calls) of the "
+                      f"{layers * len(lens) * H} in one step, scaled by tokens attended to the "
+                      f"whole step; their encode not timed; {how}"}
+
+
+def host_cores() -> int:
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_baseline(w, layers, lens, timer: OracleTimer | None = None, budget_s: float | None = None,
+                 pool: bool = True):
+    """The oracle's decode throughput on this host's cores (one worker per core); if the worker
+    pool cannot be used (or ``pool`` is false), one thread in this process on three units."""
+    own = timer is None
+    try:
+        if not pool:
+            raise RuntimeError("worker pool not requested")
+        if own:
+            timer = OracleTimer(w, layers, lens, host_cores())
+        budget = budget_s if budget_s is not None else max(1.0, ORACLE_CPU_WORK_S / timer.procs)
+        return _baseline_record(w, layers, lens, timer.step(budget), timer.procs, budget, True)
+    except Exception as e:  # noqa: BLE001 -- fall back to a one-thread sample and say so
+        if pool:
+            print(f"bench: oracle worker pool unavailable ({e}); timing one thread instead", file=sys.stderr)
+        proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
+        units = _oracle_units(w, layers, lens, 3)
+        caches = [_oracle_cache(w, u, proj) for u in units]
+        budget = budget_s if budget_s is not None else 12.0
+        res = [_time_decode(c, u[3], u[0], budget / len(units)) for c, u in zip(caches, units)]
+        return _baseline_record(w, layers, lens, res, 1, budget, False)
+    finally:
+        if own and timer is not None:
+            timer.close()
 
 
 def run_reference(args):
@@ -479,12 +615,22 @@ def run_reference(args):
     if rank != 0:
         return None
     w, layers, lens = workload_cfg(args.workload)
-    budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))     # wall seconds per step
     vals = []
-    for i in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, layers, lens, budget_s=budget)
-        if i >= args.warmup:
-            vals.append(cb["value"])
+    timer = None
+    try:
+        timer = OracleTimer(w, layers, lens, host_cores())
+    except Exception as e:  # noqa: BLE001
+        print(f"bench: oracle worker pool unavailable ({e}); timing one thread instead", file=sys.stderr)
+        timer = None
+    try:
+        for i in range(args.warmup + args.steps):
+            cb = cpu_baseline(w, layers, lens, timer=timer, budget_s=budget, pool=timer is not None)
+            if i >= args.warmup:
+                vals.append(cb["value"])
+    finally:
+        if timer is not None:
+            timer.close()
     value = statistics.mean(vals)
     step_s = float(lens.sum()) / value
     cb["value"] = value
