@@ -506,7 +506,7 @@ class OracleTimer:
     time, so the sum of the workers' rates is the oracle's throughput on all cores.
     """
 
-    def __init__(self, w, layers, lens, procs: int, timeout_s: float = 900.0):
+    def __init__(self, w, layers, lens, procs: int, timeout_s: float = 300.0):
         import multiprocessing as mp
 
         self.w, self.procs, self.timeout = w, procs, timeout_s
