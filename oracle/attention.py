@@ -216,6 +216,30 @@ class OracleCache:
         return out
 
 
+def prefill(cache: "OracleCache", layer: int, k: np.ndarray, v: np.ndarray, q: np.ndarray,
+            pos: np.ndarray) -> np.ndarray:
+    """Chunked prefill over the compressed cache: T new tokens per sequence with their queries.
+
+    [QC] v3.2 note: a batched prefill writes exactly what T single-token steps write.  Reading for
+    the attention of the chunk: also exactly what T single-token steps compute, so query t of
+    sequence b attends causally to positions [0, pos[b] + t] with the window of that step (the
+    newest ``window`` of those positions raw, the rest through their quantised records).  Written as
+    that definition: append token t, then decode at L = pos[b] + t + 1.
+
+    k, v [B][H][T][128]; q [B][Hq][T][128]; pos [B] (pos[b] < 0: sequence b takes no part, its
+    outputs are zero).  Returns out [B][Hq][T][128] float64.
+    """
+    B, _, T, _ = k.shape
+    out = np.zeros((B, cache.cfg.n_q_heads, T, codec.D), np.float64)
+    active = np.asarray(pos) >= 0
+    for t in range(T):
+        p = np.where(active, np.asarray(pos) + t, -1)
+        cache.append(layer, k[:, :, t:t + 1], v[:, :, t:t + 1], p)
+        lens = np.where(active, p + 1, 0)
+        out[:, :, t] = cache.decode(layer, q[:, :, t], lens)
+    return out
+
+
 def plain_attention64(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
     """Textbook softmax(q k^T / sqrt(d)) v in float64 via scipy's softmax; q [g][d], k, v [L][d]."""
     from scipy.special import softmax

@@ -93,6 +93,11 @@ MUTANTS = [
                      "logits.append((qt @ kw.T) * inv_sqrt_d if Lq > 0 else (q64 @ kw.T) * inv_sqrt_d)"),
     ("attention.py", "m = lg.max(axis=1, keepdims=True)", "m = lg.max(axis=1, keepdims=True) * 0 + 50"),
     ("attention.py", "out += codec.unrotate64(p[:, :Lq] @ vd, self.signs)", "out += p[:, :Lq] @ vd"),
+    # chunked prefill
+    ("attention.py", "lens = np.where(active, p + 1, 0)", "lens = np.where(active, p, 0)"),
+    ("attention.py", "p = np.where(active, np.asarray(pos) + t, -1)", "p = np.where(active, np.asarray(pos), -1)"),
+    ("attention.py", "out[:, :, t] = cache.decode(layer, q[:, :, t], lens)",
+                     "out[:, :, t] = cache.decode(layer, q[:, :, 0], lens)"),
 ]
 
 # Child interpreter: build the ``oracle`` package from its sources with one replacement applied,

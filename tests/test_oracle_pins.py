@@ -716,3 +716,70 @@ def test_tq_record_is_4_25_bits_and_compresses_over_4_5x():
     assert attention.REC_BYTES[attention.TQ3_QJL] * 8 / 128 == 4.25
     assert 16 / 3.5 >= 4.5
     assert 32 / 4.25 > 4.5
+
+
+# ------------------------------------------------------------------ chunked prefill (T queries)
+def _prefill_case(window, p0, T, B=1, H=1, Hq=2, seed=40):
+    rng = np.random.default_rng(seed)
+    cap = p0 + T + 4
+    c = _cache(window, cap, B=B, H=H, Hq=Hq, seed=3)
+    kp = rng.standard_normal((B, H, p0, 128)).astype(np.float32)
+    vp = rng.standard_normal((B, H, p0, 128)).astype(np.float32)
+    if p0:
+        c.append(0, kp, vp, np.zeros(B, int))
+    k = rng.standard_normal((B, H, T, 128)).astype(np.float32)
+    v = rng.standard_normal((B, H, T, 128)).astype(np.float32)
+    q = rng.standard_normal((B, Hq, T, 128)).astype(np.float32)
+    return c, np.concatenate([kp, k], axis=2), np.concatenate([vp, v], axis=2), k, v, q
+
+
+@pytest.mark.parametrize("p0", [0, 20])
+def test_prefill_with_covering_window_is_causal_attention(p0):
+    """Window >= context: query t is exactly softmax attention over raw positions 0 .. p0 + t."""
+    c, kall, vall, k, v, q = _prefill_case(128, p0, 40, B=2, H=2, Hq=6)
+    out = attention.prefill(c, 0, k, v, q, np.array([p0, p0]))
+    for b in range(2):
+        for i in range(6):
+            for t in range(40):
+                L = p0 + t + 1
+                ref = attention.plain_attention64(q[b, i:i + 1, t], kall[b, i // 3, :L], vall[b, i // 3, :L])
+                assert np.allclose(out[b, i, t], ref[0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("window,p0,T", [(0, 3, 6), (4, 3, 10), (8, 0, 12)])
+def test_prefill_matches_brute_force_with_sliding_window(window, p0, T):
+    """Query t sees positions [0, L - W) through their records and [L - W, L) raw, L = p0 + t + 1;
+    the brute force reads the raw window from the inputs, not from the ring."""
+    c, kall, vall, k, v, q = _prefill_case(window, p0, T)
+    out = attention.prefill(c, 0, k, v, q, np.array([p0]))
+    for t in range(T):
+        L = p0 + t + 1
+        ref = _brute_force_unit(c, q[0, :, t], L, kall[0, 0], vall[0, 0])
+        assert np.allclose(out[0, :, t], ref, rtol=0, atol=1e-10)
+
+
+def test_prefill_is_causal_and_leaves_the_bulk_append_state():
+    """Changing the chunk's tokens after t leaves query t's output unchanged; the cache afterwards
+    holds exactly what one bulk append of the chunk writes ([QC] v3.2 note)."""
+    c1, _, _, k, v, q = _prefill_case(4, 5, 9)
+    c2, _, _, _, _, _ = _prefill_case(4, 5, 9)
+    c3, _, _, _, _, _ = _prefill_case(4, 5, 9)
+    out1 = attention.prefill(c1, 0, k, v, q, np.array([5]))
+    k2, v2, q2 = k.copy(), v.copy(), q.copy()
+    k2[:, :, 6:] += 1.0
+    v2[:, :, 6:] -= 2.0
+    q2[:, :, 6:] *= 3.0
+    out2 = attention.prefill(c2, 0, k2, v2, q2, np.array([5]))
+    assert np.array_equal(out1[:, :, :6], out2[:, :, :6])
+    assert not np.allclose(out1[:, :, 6:], out2[:, :, 6:])
+    c3.append(0, k, v, np.array([5]))
+    for name in ("code", "scale", "zero"):
+        assert np.array_equal(c1.k[name], c3.k[name]) and np.array_equal(c1.v[name], c3.v[name])
+    assert np.array_equal(c1.ring_k, c3.ring_k) and np.array_equal(c1.ring_v, c3.ring_v)
+
+
+def test_prefill_skips_inactive_sequences():
+    c, _, _, k, v, q = _prefill_case(8, 0, 5, B=2)
+    out = attention.prefill(c, 0, k, v, q, np.array([-1, 0]))
+    assert not out[0].any() and out[1].any()
+    assert not c.k["code"][0, 0].any()
