@@ -20,10 +20,12 @@
  *     inputs, outputs, scratch, the block table).  No entry point allocates or frees memory.
  *   - Device pointers must be 16-byte aligned (KVQ_ERR_ALIGN otherwise).
  *   - Work is enqueued asynchronously on ``stream`` (a cudaStream_t; NULL = legacy default
- *     stream).  Entry points return after launching; none synchronises except kv_status.
+ *     stream).  Entry points return after launching; none synchronises except kv_cache_init
+ *     (its header copy) and kv_status.
  *   - Invalid arguments return a KVQ_ERR_* code and launch nothing.  Inconsistencies only the
- *     device can see (a block-table entry out of range, a position past capacity, a pipeline wait
- *     that gave up) set bits in the cache's device status word, read with kv_status.
+ *     device can see (a block-table entry out of range, a position past capacity, a sequence
+ *     length out of range, a pipeline wait that gave up) set bits in the cache's device status
+ *     word, read with kv_status.
  *   - head_dim is 128; n_q_heads is a multiple of n_kv_heads with a GQA group of 1..4 query heads
  *     per kv-head; page_tokens is 64; window is 0 or a multiple of 4 up to 1024.
  */
@@ -136,6 +138,12 @@ size_t kv_cache_bytes(const kvq_config* cfg);
  *   qjl_proj_host    host float [128][128] row-major i.i.d. N(0,1) projection S of the QJL sketch;
  *                    required when k_format == KVQ_TQ3_QJL, ignored otherwise.
  * Synchronises ``stream`` before returning (the header copies are complete on return).
+ * Saving and restoring: the buffer holds the whole state (header with signs, codebook, projection
+ * and Sinkhorn scales; the identity block table; rings; pages), none of it tied to its address.
+ * To restore a saved copy, call kv_cache_init with the same config on a buffer of the same size
+ * (or reuse the struct of the original buffer), then copy the saved bytes over the whole buffer;
+ * a caller-supplied block table is the caller's to save.  Re-initialising a live buffer resets
+ * its Sinkhorn scales to 1.
  */
 int kv_cache_init(kvq_cache* cache, const kvq_config* cfg, void* dev_mem, size_t bytes,
                   const int32_t* block_table, const float* qjl_proj_host, void* stream);
