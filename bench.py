@@ -577,11 +577,16 @@ def _baseline_record(w, layers, lens, results, procs, budget_s, all_cores: bool)
                       f"whole step; their encode not timed; {how}"}
 
 
+ORACLE_MAX_WORKERS = 64       # bounds the pool's start-up time and memory on very large hosts
+
+
 def host_cores() -> int:
+    """Oracle workers to start: the cores this process may run on, at most ORACLE_MAX_WORKERS."""
     try:
-        return max(1, len(os.sched_getaffinity(0)))
+        n = len(os.sched_getaffinity(0))
     except AttributeError:
-        return max(1, os.cpu_count() or 1)
+        n = os.cpu_count() or 1
+    return max(1, min(ORACLE_MAX_WORKERS, n))
 
 
 def cpu_baseline(w, layers, lens, timer: OracleTimer | None = None, budget_s: float | None = None,
