@@ -783,3 +783,13 @@ def test_prefill_skips_inactive_sequences():
     out = attention.prefill(c, 0, k, v, q, np.array([-1, 0]))
     assert not out[0].any() and out[1].any()
     assert not c.k["code"][0, 0].any()
+
+
+def test_q4_key_codes_are_8x_fewer_bytes_than_fp32_keys():
+    """[TQ] "inference cost" row: logits up to 8x faster at 4-bit than at 32-bit keys, i.e. the
+    bytes a bandwidth-bound logit pass reads per key: 128 nibbles against 128 floats; with the
+    group scales and zeros the Q4G32 record is 6.4x smaller."""
+    fp32_key = 128 * 4
+    codes = 128 // 2
+    assert fp32_key / codes == 8
+    assert fp32_key / attention.REC_BYTES[attention.Q4G32] == 6.4
