@@ -143,3 +143,59 @@ def test_uninitialised_cache_is_refused_by_every_entry_point(kvq):
 
 def test_cache_bytes_null_config(kvq):
     assert kvq.kv_cache_bytes(None) == 0
+
+
+# ------------------------------------------------------------------ the header from plain C
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "kvq.h"
+
+int main(void) {
+  kvq_config c;
+  kvq_cache cache;
+  size_t good, bad;
+  int rc;
+  memset(&c, 0, sizeof c);
+  c.n_layers = 28; c.n_kv_heads = 8; c.n_q_heads = 24; c.head_dim = 128; c.max_batch = 1;
+  c.max_seq_len = 32768; c.window = 128; c.page_tokens = 64; c.n_pages = 0;
+  c.k_format = KVQ_Q4G32; c.v_format = KVQ_Q4G32; c.sinkhorn = 0; c.group = 32;
+  c.in_dtype = KVQ_IN_BF16; c.seed = 0;
+  good = kv_cache_bytes(&c);
+  c.head_dim = 64;
+  bad = kv_cache_bytes(&c);
+  memset(&cache, 0, sizeof cache);
+  rc = kv_quant_append(&cache, 0, NULL, NULL, NULL, 1, 1, NULL);
+  printf("%zu %zu %d %s\n", good, bad, rc, kv_strerror(rc));
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(kvq):
+    """include/kvq.h compiles as strict C99 and as C++; a C program links against libkvq.so and
+    calls it (size query, refusal of an uninitialised cache) with no GPU."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    out_dir = os.path.dirname(lib.LIB_PATH)
+    src = os.path.join(out_dir, "abi_check.c")
+    exe = os.path.join(out_dir, "abi_check")
+    with open(src, "w") as f:
+        f.write(C_PROGRAM)
+    inc = os.path.join(ROOT, "include")
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", inc, src,
+                    "-L", out_dir, "-lkvq", f"-Wl,-rpath,{out_dir}", "-o", exe], check=True)
+    gxx = shutil.which("g++")
+    if gxx is not None:
+        subprocess.run([gxx, "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++",
+                        os.path.join(inc, "kvq.h")], check=True)
+    res = subprocess.run([exe], capture_output=True, text=True, check=True)
+    good, bad, rc, msg = res.stdout.strip().split(" ", 3)
+    cfg = lib.make_config(28, 8, 24, 1, 32768, window=128)
+    assert int(good) == lib.kv_cache_bytes(cfg) > 0
+    assert int(bad) == 0
+    assert int(rc) == 6 and msg == "cache not initialised"
