@@ -172,8 +172,11 @@ int kv_calibrate(kvq_cache* cache, int32_t layer, const void* k_calib, const voi
  *              append ragged chunks to a subset of the batch)
  * Value range: scales, zeros, norms and sigma are stored as fp16, so each vector must be finite
  * with Euclidean norm below 65504 (after division by sigma when balanced; the rotation keeps the
- * norm).  Outside that range the stored metadata is infinite or NaN and the codes are undefined;
- * nothing is flagged.
+ * norm).  TQ3 keys must also be zero or have some rotated element above 2^-75 in magnitude: when
+ * every square underflows float32 the norm is 0, the 1/max(norm, FLT_MIN) guard scales the vector
+ * by 2^126 and the stored residual norm is infinite (the key's logits are then NaN).  Outside
+ * these ranges the stored metadata is infinite or NaN and the codes are undefined; nothing is
+ * flagged.
  */
 int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* v,
                     const int32_t* pos, int32_t batch, int32_t n_tokens, void* stream);
