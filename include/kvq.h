@@ -155,6 +155,9 @@ int kv_cache_init(kvq_cache* cache, const kvq_config* cfg, void* dev_mem, size_t
  * layer.  Inputs (device, cfg.in_dtype): k_calib, v_calib [L?][n_kv_heads][n_tokens][128] with the
  * leading layer axis present when layer == -1.  n_tokens in 1..4096.  ``scratch`` (device, at
  * least kv_calibrate_scratch_bytes) holds the float working copies.  Needs cfg.sinkhorn == 1.
+ * sigma is relative (an overall factor is free) and stored as fp16: a channel whose scale falls
+ * below fp16's smallest subnormal relative to the others (column RMS ratios beyond ~10^7) stores
+ * sigma = 0, and values later appended in that channel are divided by zero.
  */
 size_t kv_calibrate_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t n_tokens);
 int kv_calibrate(kvq_cache* cache, int32_t layer, const void* k_calib, const void* v_calib,

@@ -103,3 +103,19 @@ def test_tq3_key_below_the_norm_guard():
     y[0, 0] = 2.0 ** -74                                 # one square survives: a normal key again
     code, bits, n, gamma = codec.tq3_qjl_encode(y, proj)
     assert np.isfinite(float(gamma[0])) and float(gamma[0]) < 3.0
+
+
+def test_sinkhorn_scale_outside_fp16():
+    """sigma is stored as fp16: channel scales spread by 10^4 are recovered in ratio, while a channel
+    10^8 below the others rounds to sigma = 0 (the calibration precondition in the header)."""
+    x = np.random.default_rng(0).standard_normal((256, 128)).astype(np.float32)
+    y = x.copy()
+    y[:, 5] *= np.float32(1e4)
+    s = codec.sinkhorn_sigma(y).astype(np.float64)
+    others = np.delete(s, 5)
+    assert 0.8e4 < s[5] / np.median(others) < 1.25e4
+    y = x.copy()
+    y[:, 5] *= np.float32(1e-8)
+    with np.errstate(all="ignore"):
+        s = codec.sinkhorn_sigma(y)
+    assert float(s[5]) == 0.0 and np.all(np.delete(s, 5) > 0)
