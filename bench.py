@@ -439,6 +439,7 @@ def run_gpu(args):
 
 # ------------------------------------------------------------------ CPU oracle
 ORACLE_CPU_WORK_S = 24.0      # CPU-seconds of oracle decode per baseline sample (all workers)
+REFERENCE_WALL_S = 60.0       # wall seconds of timed oracle work in a whole --impl reference run
 
 
 def _oracle_units(w, layers, lens, n):
@@ -620,7 +621,7 @@ def run_reference(args):
     if rank != 0:
         return None
     w, layers, lens = workload_cfg(args.workload)
-    budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))     # wall seconds per step
+    budget = max(0.5, REFERENCE_WALL_S / max(1, args.steps + args.warmup))   # wall seconds per step
     vals = []
     timer = None
     try:

@@ -61,3 +61,29 @@ def test_one_thread_fallback():
     w, layers, lens = bench.workload_cfg("tiny")
     cb = bench.cpu_baseline(w, layers, lens, budget_s=0.3, pool=False)
     assert cb["cores"] == 1 and cb["value"] > 0 and "one thread" in cb["sample"]
+
+
+def test_reference_arm_json_line(monkeypatch):
+    """--impl reference: rank 0 prints the contract's line, timed on the oracle; other ranks none."""
+    import argparse
+
+    monkeypatch.setattr(bench, "REFERENCE_WALL_S", 1.0)
+    monkeypatch.setattr(bench, "host_cores", lambda: 2)
+    args = argparse.Namespace(steps=1, warmup=3, workload="tiny", impl="reference", gpus=1)
+    monkeypatch.setenv("RANK", "1")
+    assert bench.run_reference(args) is None
+    monkeypatch.setenv("RANK", "0")
+    res = bench.run_reference(args)
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in res, key
+    assert res["impl"] == "reference" and res["steps"] == 1 and res["warmup"] == 3
+    assert res["value"] > 0 and res["higher_is_better"] is True and res["vs_baseline"] is None
+    assert res["config"]["workload"] == "tiny"
+    cb = res["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == res["value"] and cb["sample"]
+    e2e = res["e2e"]
+    assert e2e["value"] == res["value"] and e2e["unit"] == res["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert res["ms_per_step"] == pytest.approx(512 / res["value"] * 1e3)
