@@ -119,3 +119,36 @@ def test_sinkhorn_scale_outside_fp16():
     with np.errstate(all="ignore"):
         s = codec.sinkhorn_sigma(y)
     assert float(s[5]) == 0.0 and np.all(np.delete(s, 5) > 0)
+
+
+@settings(max_examples=40, deadline=None, derandomize=True)
+@given(st.integers(0, 2), st.integers(1, 40), st.sampled_from([0, 4, 8]), st.integers(0, 2 ** 31 - 1))
+def test_decode_output_is_a_convex_combination_of_values(kind, L, window, seed):
+    """Softmax weights are non-negative and sum to 1, and the inverse rotation is linear, so every
+    output coordinate lies between the smallest and largest value any attended token contributes
+    (dequantised and un-rotated, or raw in the window)."""
+    from oracle import attention
+
+    kfmt = (attention.Q4G32, attention.Q8G32, attention.TQ3_QJL)[kind]
+    rng = np.random.default_rng(seed)
+    proj = rng.standard_normal((128, 128)).astype(np.float32) if kfmt == attention.TQ3_QJL else None
+    cfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=2, max_batch=1, max_seq_len=48,
+                                 window=window, k_format=kfmt, seed=seed % 7)
+    c = attention.OracleCache(cfg, proj)
+    k = (rng.standard_normal((1, 1, L, 128)) * rng.uniform(0.1, 5)).astype(np.float32)
+    v = (rng.standard_normal((1, 1, L, 128)) * rng.uniform(0.1, 5)).astype(np.float32)
+    c.append(0, k, v, np.array([0]))
+    q = (rng.standard_normal((1, 2, 128)) * rng.uniform(0.1, 3)).astype(np.float32)
+    out = c.decode(0, q, np.array([L]))[0]
+    Lq = max(0, L - window) if window > 0 else L
+    vals = []
+    if Lq:
+        vd = codec.q4g32_decode(c.v["code"][0, 0, 0, :Lq], c.v["scale"][0, 0, 0, :Lq],
+                                c.v["zero"][0, 0, 0, :Lq]).astype(np.float64)
+        vals.append(codec.unrotate64(vd, c.signs))
+    if L > Lq:
+        vals.append(v[0, 0, Lq:L].astype(np.float64))
+    vals = np.concatenate(vals)
+    lo, hi = vals.min(0), vals.max(0)
+    tol = 1e-9 * np.abs(vals).max()
+    assert np.all(out >= lo - tol) and np.all(out <= hi + tol)
