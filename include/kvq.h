@@ -16,8 +16,11 @@
  *
  * Conventions for every entry point
  *   - All functions are host functions.  Pointers documented as "device" must point to memory of
- *     the CUDA device that was current at kv_cache_init; the caller owns every buffer (the cache,
- *     inputs, outputs, scratch, the block table).  No entry point allocates or frees memory.
+ *     the CUDA device that was current at kv_cache_init, and that device must be current when an
+ *     entry point that launches work is called (KVQ_ERR_INVALID_ARG otherwise).  The caller owns
+ *     every buffer (the cache, inputs, outputs, scratch, the block table) with one exception:
+ *     kv_decode_attention_noalloc takes its scratch from a fixed array of the library's own device
+ *     memory.  No entry point allocates or frees memory.
  *   - Device pointers must be 16-byte aligned (KVQ_ERR_ALIGN otherwise).
  *   - Work is enqueued asynchronously on ``stream`` (a cudaStream_t; NULL = legacy default
  *     stream).  Entry points return after launching; none synchronises except kv_cache_init
@@ -125,13 +128,28 @@ typedef struct kvq_cache {
  *     bit i (= (S r)_i >= 0) at bit i of the 16-byte stream.
  */
 
-/* Closed-form size of the cache buffer for ``cfg``; 0 if the config is invalid or unsupported. */
+/*
+ * Closed-form size of the cache buffer for ``cfg``; 0 if the config is invalid or unsupported.
+ * [QC] PPL / KV-memory table and the "6.4x KV compression" figure: a Q4G32 record is 4-bit codes
+ * plus an fp16 scale and zero per 32 values, 80 B per 128-value vector against 512 B in FP32
+ * (6.4x); the "4-bit + progressive" row adds the 128-token FP32 window on top of the 4-bit store
+ * (2.33 vs 2.30 GB for Llama-3.2-3B at 32K), which is the ring counted here.  [TQ] "method
+ * comparison" table, compression >= 4.5x: a TQ3_QJL key record is 68 B (3-bit codes, 128 sign bits,
+ * fp16 norm and residual norm).  Total = header + 2 rings of n_layers * max_batch * n_kv_heads *
+ * window * 512 B + n_layers * n_pages * n_kv_heads pages of 64 tokens x (K record + 80 B), each
+ * region rounded up to 256 B.
+ */
 size_t kv_cache_bytes(const kvq_config* cfg);
 
 /*
  * Lay out a cache in the caller's device buffer ``dev_mem`` (``bytes`` >= kv_cache_bytes(cfg)),
  * write the header (signs from cfg->seed, codebook, QJL projection, unit Sinkhorn scales,
  * identity block table) and clear the status word.  Page and ring contents are not cleared.
+ * The header holds what the pages' codecs fix once per cache: the random +-1 signs of the
+ * randomised Walsh-Hadamard rotation ([KV] TLDR; [TQ] "key idea" row, random rotation), the
+ * per-coordinate optimal (Lloyd-Max) 3-bit codebook and the Gaussian projection of the 1-bit QJL
+ * residual sketch ([TQ] "key idea" row), and the Sinkhorn scales of [KV] TLDR (1 until
+ * kv_calibrate).  The window size follows [QC] "how it works" (the 128 most recent tokens in FP32).
  *   block_table      device int32 [max_batch][max_pages_per_seq] mapping (sequence, logical page)
  *                    to a physical page in [0, n_pages); NULL = contiguous identity table.  The
  *                    caller keeps it alive and may rewrite it between calls.
@@ -189,6 +207,11 @@ int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* 
  * positions [0, L - window) through the quantised pages (logits in rotated space), positions
  * [L - window, L) through the FP32 ring, one softmax with scale 1/sqrt(128), L = seq_lens[b]
  * (tokens already appended, the current one included).  An empty sequence (L = 0) gives zeros.
+ * Sources: [QC] "how it works" (attention over the 4-bit store plus the FP32 window of the most
+ * recent 128 tokens; the PPL / KV-memory table's "4-bit + progressive" row is this read path);
+ * [TQ] "method comparison" table, "inference cost" row (attention logits computed directly on the
+ * low-bit keys, no dense FP16 copy) and "key idea" row (the QJL residual term makes the inner
+ * product estimate unbiased); [KV] TLDR (the Sinkhorn scales are folded into q and the output).
  *   layer      0..n_layers-1, or -1 for all layers (q, out then carry a leading layer axis)
  *   q          device, cfg.in_dtype, [L?][batch][n_q_heads][128]; query head j uses kv-head
  *              j / (n_q_heads / n_kv_heads)
@@ -218,7 +241,9 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
  *   - Calls needing more scratch than that (kv_decode_scratch_bytes > KVQ_NOALLOC_SCRATCH_MAX)
  *     return KVQ_ERR_CAPACITY and launch nothing.
  *   - The first call on a device looks up the array's device address (once per device, with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The address is kept for
+ *     the life of the process: after a cudaDeviceReset (or any teardown of the device's primary
+ *     context) this entry point must not be called again on that device.
  *   - Every call shares the one array: calls that overlap on the GPU (other streams, other host
  *     threads) race on it and must be serialised by the caller.
  *   - Calls no cudaMalloc, cudaFree or other allocating routine.

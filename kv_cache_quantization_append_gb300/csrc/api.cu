@@ -157,6 +157,14 @@ static int layers_of_call(const kvq_cache* c, int32_t layer, int* l0, int* nl) {
   return KVQ_OK;
 }
 
+// The cache's pointers belong to the device that was current at kv_cache_init; a launch with
+// another device current would hand that device foreign addresses, so such calls are refused.
+static int check_device(const kvq_cache* c) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
+  return dev == c->device ? KVQ_OK : KVQ_ERR_INVALID_ARG;
+}
+
 int decode_ctas(int device) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
@@ -240,6 +248,7 @@ int kv_calibrate(kvq_cache* cache, int32_t layer, const void* k_calib, const voi
   int l0, nl;
   if ((rc = layers_of_call(cache, layer, &l0, &nl)) != KVQ_OK) return rc;
   if (scratch_bytes < kv_calibrate_scratch_bytes(cache, layer, n_tokens)) return KVQ_ERR_CAPACITY;
+  if ((rc = check_device(cache)) != KVQ_OK) return rc;
   CalibArgs a;
   a.p = dev_ptrs(*cache, L);
   a.kc = k_calib;
@@ -263,6 +272,7 @@ int kv_quant_append(kvq_cache* cache, int32_t layer, const void* k, const void* 
   if (!aligned16(k) || !aligned16(v) || !aligned16(pos)) return KVQ_ERR_ALIGN;
   int l0, nl;
   if ((rc = layers_of_call(cache, layer, &l0, &nl)) != KVQ_OK) return rc;
+  if ((rc = check_device(cache)) != KVQ_OK) return rc;
   AppendArgs a;
   a.p = dev_ptrs(*cache, L);
   a.L = L;
@@ -305,6 +315,7 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   if (!aligned16(q) || !aligned16(out) || !aligned16(seq_lens) || !aligned16(scratch)) return KVQ_ERR_ALIGN;
   int l0, nl;
   if ((rc = layers_of_call(cache, layer, &l0, &nl)) != KVQ_OK) return rc;
+  if ((rc = check_device(cache)) != KVQ_OK) return rc;
   const int ctas = decode_ctas(cache->device);
   if (ctas <= 0) return KVQ_ERR_CUDA;
   const int n_units = nl * batch * cache->cfg.n_kv_heads;

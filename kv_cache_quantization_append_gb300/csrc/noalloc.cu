@@ -39,12 +39,15 @@ int scratch_address(int device, void** out) {
 
 int decode_attention_noalloc(kvq_cache* cache, int32_t layer, const void* q, float* out,
                              const int32_t* seq_lens, int32_t batch, void* stream) {
-  const size_t need = kv_decode_scratch_bytes(cache, layer, batch);
-  if (need == 0) return KVQ_ERR_INVALID_ARG;
-  if (need > NOALLOC_SCRATCH_BYTES) return KVQ_ERR_CAPACITY;
+  // argument errors first, so that a zero scratch size below can only mean a failed CUDA query
+  if (layer < -1 || layer >= cache->cfg.n_layers) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > cache->cfg.max_batch) return KVQ_ERR_INVALID_ARG;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   if (dev != cache->device) return KVQ_ERR_INVALID_ARG;
+  const size_t need = kv_decode_scratch_bytes(cache, layer, batch);
+  if (need == 0) return KVQ_ERR_CUDA;
+  if (need > NOALLOC_SCRATCH_BYTES) return KVQ_ERR_CAPACITY;
   void* scratch = nullptr;
   const int rc = scratch_address(dev, &scratch);
   if (rc != KVQ_OK) return rc;

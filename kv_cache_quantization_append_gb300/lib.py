@@ -114,6 +114,44 @@ def _check_in_dtype(cache: kvq_cache, *tensors: torch.Tensor):
             raise KVQError(f"input dtype {t.dtype} does not match the cache's in_dtype ({want})")
 
 
+def _layers_in_call(cache: kvq_cache, layer: int) -> int:
+    return cache.cfg.n_layers if layer == -1 else 1
+
+
+def _check_shape(name: str, t: torch.Tensor, want: tuple):
+    """The library reads and writes whole rows of these shapes from the bare pointer; a tensor of
+    another size would be read or written past its end, which the C ABI cannot see."""
+    if tuple(t.shape) != tuple(want):
+        raise KVQError(f"{name} has shape {tuple(t.shape)}, expected {tuple(want)}")
+
+
+def _check_decode_shapes(cache: kvq_cache, layer: int, q: torch.Tensor, out: torch.Tensor,
+                         seq_lens: torch.Tensor) -> int:
+    """q and out [L?][B][Hq][128] (the layer axis present iff layer == -1), seq_lens [B]; returns B."""
+    if q.dim() not in (3, 4) or q.dim() != (4 if layer == -1 else 3):
+        raise KVQError(f"q must be {'[L][B][Hq][128]' if layer == -1 else '[B][Hq][128]'}, got {tuple(q.shape)}")
+    B = q.shape[-3]
+    lead = (_layers_in_call(cache, layer),) if layer == -1 else ()
+    _check_shape("q", q, lead + (B, cache.cfg.n_q_heads, 128))
+    _check_shape("out", out, tuple(q.shape))
+    _check_shape("seq_lens", seq_lens, (B,))
+    return B
+
+
+def _check_append_shapes(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch.Tensor,
+                         pos: torch.Tensor) -> tuple:
+    """k and v [L?][B][Hkv][T][128] (the layer axis present iff layer == -1), pos [B]; returns (B, T)."""
+    if k.dim() != (5 if layer == -1 else 4):
+        raise KVQError(f"k must be {'[L][B][Hkv][T][128]' if layer == -1 else '[B][Hkv][T][128]'}, "
+                       f"got {tuple(k.shape)}")
+    B, T = k.shape[-4], k.shape[-2]
+    lead = (_layers_in_call(cache, layer),) if layer == -1 else ()
+    _check_shape("k", k, lead + (B, cache.cfg.n_kv_heads, T, 128))
+    _check_shape("v", v, tuple(k.shape))
+    _check_shape("pos", pos, (B,))
+    return B, T
+
+
 def make_config(n_layers, n_kv_heads, n_q_heads, max_batch, max_seq_len, window=128, n_pages=0,
                 k_format=KVQ_Q4G32, v_format=KVQ_Q4G32, sinkhorn=False, in_dtype=KVQ_IN_BF16,
                 seed=0) -> kvq_config:
@@ -146,6 +184,9 @@ def kv_calibrate(cache: kvq_cache, layer: int, k_calib: torch.Tensor, v_calib: t
                  scratch: torch.Tensor, stream=None):
     _check_in_dtype(cache, k_calib, v_calib)
     n_tokens = k_calib.shape[-2]
+    lead = (_layers_in_call(cache, layer),) if layer == -1 else ()
+    _check_shape("k_calib", k_calib, lead + (cache.cfg.n_kv_heads, n_tokens, 128))
+    _check_shape("v_calib", v_calib, tuple(k_calib.shape))
     _check(load().kv_calibrate(ctypes.byref(cache), layer, _ptr(k_calib), _ptr(v_calib), n_tokens,
                                _ptr(scratch), scratch.numel() * scratch.element_size(),
                                _stream(stream)))
@@ -157,7 +198,7 @@ def kv_quant_append(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch.Tens
     if pos.dtype != torch.int32:
         raise KVQError("pos must be int32")
     _check_in_dtype(cache, k, v)
-    B, T = k.shape[-4], k.shape[-2]
+    B, T = _check_append_shapes(cache, layer, k, v, pos)
     _check(load().kv_quant_append(ctypes.byref(cache), layer, _ptr(k), _ptr(v), _ptr(pos), B, T,
                                   _stream(stream)))
 
@@ -173,7 +214,7 @@ def kv_decode_attention(cache: kvq_cache, layer: int, q: torch.Tensor, out: torc
     if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
         raise KVQError("seq_lens must be int32 and out float32")
     _check_in_dtype(cache, q)
-    B = q.shape[-3]
+    B = _check_decode_shapes(cache, layer, q, out, seq_lens)
     _check(load().kv_decode_attention(ctypes.byref(cache), layer, _ptr(q), _ptr(out), _ptr(seq_lens),
                                       B, _ptr(scratch), scratch.numel() * scratch.element_size(),
                                       _stream(stream)))
@@ -186,7 +227,7 @@ def kv_decode_attention_noalloc(cache: kvq_cache, layer: int, q: torch.Tensor, o
     if seq_lens.dtype != torch.int32 or out.dtype != torch.float32:
         raise KVQError("seq_lens must be int32 and out float32")
     _check_in_dtype(cache, q)
-    B = q.shape[-3]
+    B = _check_decode_shapes(cache, layer, q, out, seq_lens)
     _check(load().kv_decode_attention_noalloc(ctypes.byref(cache), layer, _ptr(q), _ptr(out),
                                               _ptr(seq_lens), B, _stream(stream)))
 

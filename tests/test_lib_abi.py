@@ -199,3 +199,55 @@ def test_header_is_plain_c_and_links(kvq):
     assert int(good) == lib.kv_cache_bytes(cfg) > 0
     assert int(bad) == 0
     assert int(rc) == 6 and msg == "cache not initialised"
+
+
+# ------------------------------------------------------------------ the binding's shape checks
+# The library reads q, k, v and writes out through bare pointers; a tensor of the wrong size would
+# be read or written past its end, which the C ABI cannot see.  The binding refuses such tensors
+# before any library call (so these checks run on CPU tensors, with no device touched).
+def _fake_cache(layers=2, hkv=2, hq=6, batch=3):
+    cache = lib.kvq_cache()
+    cache.cfg = lib.make_config(layers, hkv, hq, batch, 256)
+    return cache
+
+
+def test_decode_binding_refuses_mismatched_shapes():
+    import torch
+
+    c = _fake_cache()
+    bf = torch.bfloat16
+    sl = torch.zeros(3, dtype=torch.int32)
+    cases = [
+        (-1, torch.zeros(3, 6, 128, dtype=bf), torch.zeros(3, 6, 128)),          # no layer axis
+        (-1, torch.zeros(1, 3, 6, 128, dtype=bf), torch.zeros(1, 3, 6, 128)),    # one layer of two
+        (0, torch.zeros(2, 3, 6, 128, dtype=bf), torch.zeros(2, 3, 6, 128)),     # layer axis on a layer call
+        (0, torch.zeros(3, 4, 128, dtype=bf), torch.zeros(3, 4, 128)),           # wrong head count
+        (0, torch.zeros(3, 6, 128, dtype=bf), torch.zeros(2, 6, 128)),           # out smaller than q
+        (0, torch.zeros(3, 6, 64, dtype=bf), torch.zeros(3, 6, 64)),             # head_dim 64
+    ]
+    for layer, q, out in cases:
+        for fn in (lambda: lib.kv_decode_attention(c, layer, q, out, sl, torch.zeros(16, dtype=torch.uint8)),
+                   lambda: lib.kv_decode_attention_noalloc(c, layer, q, out, sl)):
+            with pytest.raises(lib.KVQError, match="shape|must be"):
+                fn()
+    q = torch.zeros(3, 6, 128, dtype=bf)
+    with pytest.raises(lib.KVQError, match="seq_lens"):
+        lib.kv_decode_attention_noalloc(c, 0, q, torch.zeros(3, 6, 128), torch.zeros(2, dtype=torch.int32))
+
+
+def test_append_binding_refuses_mismatched_shapes():
+    import torch
+
+    c = _fake_cache()
+    bf = torch.bfloat16
+    pos = torch.zeros(3, dtype=torch.int32)
+    cases = [
+        (-1, torch.zeros(3, 2, 5, 128, dtype=bf), torch.zeros(3, 2, 5, 128, dtype=bf), pos),
+        (-1, torch.zeros(1, 3, 2, 5, 128, dtype=bf), torch.zeros(1, 3, 2, 5, 128, dtype=bf), pos),
+        (0, torch.zeros(3, 1, 5, 128, dtype=bf), torch.zeros(3, 1, 5, 128, dtype=bf), pos),
+        (0, torch.zeros(3, 2, 5, 128, dtype=bf), torch.zeros(3, 2, 4, 128, dtype=bf), pos),
+        (0, torch.zeros(3, 2, 5, 128, dtype=bf), torch.zeros(3, 2, 5, 128, dtype=bf), pos[:2]),
+    ]
+    for layer, k, v, p in cases:
+        with pytest.raises(lib.KVQError, match="shape|must be"):
+            lib.kv_quant_append(c, layer, k, v, p)

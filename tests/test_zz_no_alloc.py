@@ -30,23 +30,25 @@ def _cache_and_inputs():
 
 
 def test_noalloc_matches_scratch_entry_point_on_consecutive_calls():
+    """Both entry points launch the same deterministic kernels with the same split of the work (the
+    scratch only holds partial records, merged in a fixed order), so the outputs are bit-identical;
+    the tolerance of the other tests (2e-3 of max |out|) would hide a dependence on stale contents."""
     torch.cuda.set_device(0)
     cache, q, seq = _cache_and_inputs()
     ref = cache.decode(-1, q, seq).clone()
     torch.cuda.synchronize()
-    scale = ref.abs().max().item()
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         lib.kv_decode_attention_noalloc(cache.handle, -1, q, out, seq)
         torch.cuda.synchronize()
         assert cache.status() == 0
-        err = (out - ref).abs().max().item()
-        assert err <= 2e-3 * scale, f"call {call}: max abs err {err:.3e} vs {scale:.3e}"
+        assert torch.equal(out.view(torch.int32), ref.view(torch.int32)), f"call {call} differs"
     # a per-layer call reuses the same array with a different layout of record ranges and records
-    one = torch.empty(q.shape[1:], dtype=torch.float32, device="cuda")
+    ref1 = cache.decode(1, q[1].contiguous(), seq).clone()
+    one = torch.full_like(ref1, float("nan"))
     lib.kv_decode_attention_noalloc(cache.handle, 1, q[1].contiguous(), one, seq)
     torch.cuda.synchronize()
-    assert (one - ref[1]).abs().max().item() <= 2e-3 * scale
+    assert torch.equal(one.view(torch.int32), ref1.view(torch.int32))
 
 
 def test_noalloc_refuses_calls_beyond_its_array():

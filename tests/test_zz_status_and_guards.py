@@ -141,3 +141,31 @@ def test_bad_block_table_entry_is_flagged_and_skipped(gpu_lib):
         assert gpu.status() == 1
     off = layout.regions(gpu.cfg, gpu.buffer.numel())["off_pages"]
     assert torch.equal(before[off:], gpu.buffer[off:])  # no page byte changed (the ring may)
+
+
+def test_calls_with_another_device_current_are_refused(gpu_lib):
+    """The cache's pointers belong to the device current at kv_cache_init; a handle that names
+    another device (as if that device were current now) is refused before anything launches."""
+    import ctypes
+
+    w = synth.WORKLOADS["qwen3-4b-kvarn-128k"]
+    gpu, _, _ = harness.make_pair(1, 1, 2, 1, 256, window=128, sinkhorn=True)
+    other = lib.kvq_cache.from_buffer_copy(gpu.handle)
+    other.device = gpu.handle.device + 1
+    k, v = synth.kv_tokens(w, 0, 1, 1, 0, 8, device="cuda")
+    q = synth.queries(w, 0, 1, 2, device="cuda")
+    out = torch.zeros(1, 2, 128, dtype=torch.float32, device="cuda")
+    sl = torch.tensor([8], dtype=torch.int32, device="cuda")
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scratch = gpu.scratch(0, 1)
+    before = gpu.buffer.clone()
+    for call in (lambda: lib.kv_quant_append(other, 0, k, v, pos),
+                 lambda: lib.kv_decode_attention(other, 0, q, out, sl, scratch),
+                 lambda: lib.kv_decode_attention_noalloc(other, 0, q, out, sl),
+                 lambda: lib.kv_calibrate(other, 0, k[0].contiguous(), v[0].contiguous(),
+                                          torch.empty(1 << 20, dtype=torch.uint8, device="cuda"))):
+        with pytest.raises(lib.KVQError, match="code 1"):
+            call()
+    torch.cuda.synchronize()
+    assert torch.equal(before, gpu.buffer) and torch.count_nonzero(out).item() == 0
+    assert ctypes.sizeof(other) == ctypes.sizeof(gpu.handle)
