@@ -2,15 +2,20 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
-Default workload: Llama-3.2-3B-shaped decode at 32K context (28 layers, 24 query / 8 kv heads,
-batch 1, Q4G32 with a 128-token FP32 window).  One step = append the newest token of every layer
-(one launch over all layers) + decode attention over every layer (one streaming launch over all
-layers, then a small launch that merges the partial softmax states).
-The cache (1.2 GB for the default workload) is larger than L2, so every step streams it from HBM.
+Default workload: the largest single-GPU configuration, a Llama-3.1-8B-shaped TurboQuant cache
+(32 layers, 32 query / 8 kv heads, 8 sequences of 32768 tokens, 3-bit Lloyd-Max keys with a 1-bit
+QJL residual sketch, 4-bit group-32 values, 128-token FP32 window; 10.2 GB streamed per step).
+One step = append the newest token of every layer (one launch over all layers) + decode attention
+over every layer (one streaming launch over all layers, then a small launch that merges the
+partial softmax states).  Every cache is larger than L2, so every step streams it from HBM.
 
 Prints one JSON line.  ``value`` = cached tokens attended per second, device-timed with CUDA events
 over K steps on resident inputs; ``e2e`` = the same through the public API with the step's inputs
-copied from pinned host memory and the output copied back inside the timed region.
+copied from pinned host memory and the output copied back inside the timed region.  ``roofline``
+is the decode call alone, timed over at least one second of back-to-back calls.  ``workloads``
+carries the same decode roofline, the per-layer call form and the bulk (prefill-sized) append for
+the other large configurations (Llama-3.2-3B at 32K, Qwen3-4B KVarN at 128K, the ragged 27B-class
+batch), each built and measured after the headline one.
 With --impl reference the CPU oracle is timed instead (a bounded sample of each step).
 """
 
@@ -37,6 +42,10 @@ sys.path.insert(0, ROOT)
 from kv_cache_quantization_append_gb300 import QuantKVCache, lib, synth  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
+# the largest configuration that fits one GPU (10.2 GB streamed per step) is the headline; the other
+# large configurations are measured after it in the same run
+HEADLINE_WORKLOAD = "llama3.1-8b-tq-b8-32k"
+OTHER_WORKLOADS = ("llama3.2-3b-32k", "qwen3-4b-kvarn-128k", "dense27b-ragged-b32")
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -122,19 +131,23 @@ class Clocks:
 
 
 # ------------------------------------------------------------------ workload set-up
-def workload_cfg(name: str):
+def workload_cfg(name: str, batch=None):
     w = synth.WORKLOADS[name]
     layers = w.get("alloc_layers", w["n_layers"])
     if "ctx_range" in w:
         lens = synth.ragged_lengths(*w["ctx_range"], n=w["batch"], seed=w["len_seed"])
     else:
         lens = np.full(w["batch"], w["ctx"], np.int32)
+    if batch is not None and batch < w["batch"]:
+        w = dict(w, batch=batch)
+        lens = lens[:batch]
     return w, layers, lens
 
 
-def build_cache(name: str, device="cuda"):
-    """Allocate and prefill the cache of a workload; returns (cache, lens, block_table)."""
-    w, layers, lens = workload_cfg(name)
+def build_cache(name: str, device="cuda", batch=None):
+    """Allocate and prefill the cache of a workload; returns (cache, w, layers, lens).  ``batch``
+    keeps only the first sequences of the workload (a smaller case for profiler captures)."""
+    w, layers, lens = workload_cfg(name, batch)
     B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
     cap = int(-(-(int(lens.max()) + 64) // 64) * 64)
     kf = lib.KVQ_TQ3_QJL if w["k_format"] == "tq3_qjl" else lib.KVQ_Q4G32
@@ -244,6 +257,147 @@ def weak_scaling_value(tokens_per_step_per_rank: float, world: int, ms_per_step_
 
 
 # ------------------------------------------------------------------ GPU arm
+DECODE_ROOFLINE_MIN_S = 1.0   # the decode-only pass runs at least this long, whatever --steps is
+BULK_APPEND_REPS = 10
+
+
+def step_inputs(w, layers, lens, dev, nbuf=8):
+    """Per-step inputs of a workload: ``nbuf`` rotating query sets [L][B][Hq][128], the newest token
+    of every layer and sequence [L][B][Hkv][1][128] (K and V), its positions and the lengths."""
+    B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
+    qs = [torch.stack([synth.queries(w, l, B, Hq, step=i, device=dev) for l in range(layers)]) for i in range(nbuf)]
+    kvs = [synth.kv_tokens(w, l, B, H, int(lens.max()) - 1, 1, device=dev) for l in range(layers)]
+    knew = torch.stack([k for k, _ in kvs]).contiguous()
+    vnew = torch.stack([v for _, v in kvs]).contiguous()
+    pos = torch.as_tensor((lens - 1).astype(np.int32), device=dev)
+    seq = torch.as_tensor(lens.astype(np.int32), device=dev)
+    return qs, knew, vnew, pos, seq
+
+
+def time_decode_only(cache, qs, seq, out, steps, warmup, stream, min_s=DECODE_ROOFLINE_MIN_S):
+    """Average duration of one all-layer decode call (the streaming launch and its merge launch),
+    from CUDA events around at least DECODE_ROOFLINE_MIN_S seconds of back-to-back calls (and at
+    least ``steps`` calls).  Returns (microseconds per call, calls timed)."""
+    nbuf = len(qs)
+    for i in range(warmup):
+        cache.decode(-1, qs[i % nbuf], seq, out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(3):
+        cache.decode(-1, qs[i % nbuf], seq, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_s = e0.elapsed_time(e1) / 3 / 1e3
+    n = max(steps, int(np.ceil(min_s / max(est_s, 1e-6))))
+    e0.record(stream)
+    for i in range(n):
+        cache.decode(-1, qs[i % nbuf], seq, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n * 1e3, n
+
+
+def time_per_layer_graph(cache, qs, seq, out, layers, steps, warmup, stream):
+    """The second form of the decode step: one decode call per layer (two launches each), the calls
+    of a step captured in one CUDA graph and replayed.  The first calls, outside the capture,
+    allocate the per-layer scratch and set the kernels' attributes.  Seconds per step."""
+    q0 = qs[0].contiguous()
+    ql = [q0[l] for l in range(layers)]
+    ol = [out[l] for l in range(layers)]
+    for l in range(layers):
+        cache.decode(l, ql[l], seq, ol[l])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for l in range(layers):
+            cache.decode(l, ql[l], seq, ol[l])
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    del graph
+    return g0.elapsed_time(g1) / steps / 1e3
+
+
+def time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src):
+    """Bulk (prefill-sized) append: the workload's prefill chunk written at the end of every sequence
+    where the workload names one (the cache has room for it), else a rewrite of positions
+    [0, 4096) of every layer from the same seeded inputs (identical page bytes; the window ring then
+    holds those positions, so nothing decodes after it)."""
+    B, H = w["batch"], w["n_kv_heads"]
+    Tc = int(w.get("prefill_chunk", 4096))
+    if w.get("prefill_chunk"):
+        kc, vc = synth.kv_tokens(w, 0, B, H, 0, Tc, device=dev)
+        kc = torch.stack([kc] * layers) if layers > 1 else kc
+        vc = torch.stack([vc] * layers) if layers > 1 else vc
+        pos_c = torch.as_tensor(lens.astype(np.int32), device=dev)
+    else:
+        kl = [synth.kv_tokens(w, l, B, H, 0, Tc, device=dev) for l in range(layers)]
+        kc = torch.stack([k for k, _ in kl]).contiguous()
+        vc = torch.stack([v for _, v in kl]).contiguous()
+        del kl
+        pos_c = torch.zeros(B, dtype=torch.int32, device=dev)
+    lay = -1 if layers > 1 else 0
+    for _ in range(3):
+        cache.append(lay, kc, vc, pos_c)
+    torch.cuda.synchronize()
+    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a0.record(stream)
+    for _ in range(BULK_APPEND_REPS):
+        cache.append(lay, kc, vc, pos_c)
+    a1.record(stream)
+    torch.cuda.synchronize()
+    if cache.status() != 0:
+        raise RuntimeError("device status set during the bulk append")
+    a_s = a0.elapsed_time(a1) / BULK_APPEND_REPS / 1e3
+    a_bytes = bulk_append_bytes(w, layers, Tc)
+    res = {"tokens_per_sequence": Tc, "us": a_s * 1e6, "algorithmic_bytes": a_bytes,
+           "achieved_gbs": a_bytes / a_s / 1e9, "tokens_per_s": layers * B * Tc / a_s,
+           "kernel": "append_bulk_kernel" + (" + append_kernel (TQ3 keys)" if w["k_format"] == "tq3_qjl" else "")}
+    res["roofline"] = {"bound": "hbm", "achieved": res["achieved_gbs"], "peak": peak, "unit": "GB/s",
+                       "frac": res["achieved_gbs"] / peak, "peak_source": peak_src}
+    return res
+
+
+def decode_roofline(name, w, layers, lens, dec_us, calls):
+    peak, peak_src = hbm_peak()
+    alg = algorithmic_bytes(w, layers, lens)
+    achieved = alg / (dec_us / 1e6) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "peak_source": peak_src, "traffic": measured_traffic(name), "algorithmic_bytes_per_launch": alg,
+            "kernel": "decode call: decode_kernel (all layers) + merge_kernel", "decode_us_avg": dec_us,
+            "calls_timed": calls}
+
+
+def measure_other_workload(name, args, dev, stream):
+    """Decode roofline, per-layer call form and bulk append of one more workload (built, measured
+    and freed here)."""
+    cache, w, layers, lens = build_cache(name, dev)
+    qs, _, _, _, seq = step_inputs(w, layers, lens, dev)
+    out = torch.empty(layers, w["batch"], w["n_q_heads"], 128, dtype=torch.float32, device=dev)
+    dec_us, calls = time_decode_only(cache, qs, seq, out, args.steps, args.warmup, stream, args.decode_min_s)
+    if cache.status() != 0:
+        raise RuntimeError(f"device status set during the decode timing of {name}")
+    res = {"config": bench_config(name, w, layers, lens, 1),
+           "roofline": decode_roofline(name, w, layers, lens, dec_us, calls),
+           "tokens_per_s_decode": float(lens.sum()) / (dec_us / 1e6)}
+    if layers > 1:
+        g_s = time_per_layer_graph(cache, qs, seq, out, layers, args.steps, args.warmup, stream)
+        res["decode_per_layer_graph"] = {"form": "per-layer decode calls captured in one CUDA graph",
+                                         "decode_us_per_step": g_s * 1e6, "launches_per_step": 2 * layers,
+                                         "vs_all_layer_call": g_s * 1e6 / dec_us}
+    peak, peak_src = hbm_peak()
+    res["bulk_append"] = time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src)
+    del cache, qs, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_gpu(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -254,29 +408,19 @@ def run_gpu(args):
         import torch.distributed as dist
 
         dist.init_process_group("nccl")
-    cache, w, layers, lens = build_cache(args.workload, dev)
-    B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
-    dt = torch.bfloat16 if w["in_dtype"] == "bf16" else torch.float32
-    nbuf = 8
-    qs = [torch.stack([synth.queries(w, l, B, Hq, step=i, device=dev) for l in range(layers)]) for i in range(nbuf)]
-    kvs = [synth.kv_tokens(w, l, B, H, int(lens.max()) - 1, 1, device=dev) for l in range(layers)]
-    knew = torch.stack([k for k, _ in kvs]).contiguous()    # [L][B][H][1][128]
-    vnew = torch.stack([v for _, v in kvs]).contiguous()
-    pos = torch.as_tensor((lens - 1).astype(np.int32), device=dev)
-    seq = torch.as_tensor(lens.astype(np.int32), device=dev)
+    cache, w, layers, lens = build_cache(args.workload, dev, batch=args.batch)
+    B, Hq = w["batch"], w["n_q_heads"]
+    qs, knew, vnew, pos, seq = step_inputs(w, layers, lens, dev)
+    nbuf = len(qs)
     out = torch.empty(layers, B, Hq, 128, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    for i in range(args.warmup):
         cache.append(-1, knew, vnew, pos)
         cache.decode(-1, qs[i % nbuf], seq, out)
-
-    for i in range(args.warmup):
-        step(i)
     torch.cuda.synchronize()
     # device-timed region: events around the whole loop of K steps (nothing between the append
     # and the decode of a step, so the decode's programmatic launch can overlap the append's end)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -288,49 +432,20 @@ def run_gpu(args):
             cache.decode(-1, qs[i % nbuf], seq, out)
         t1.record(stream)
         torch.cuda.synchronize()
-        # the decode kernel alone, for its roofline: the same steps again with events around
-        # every decode launch
-        for i in range(args.steps):
-            cache.append(-1, knew, vnew, pos)
-            ev[i][0].record(stream)
-            cache.decode(-1, qs[i % nbuf], seq, out)
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
+        # the decode call alone, for its roofline: back-to-back calls for at least a second
+        dec_us, dec_calls = time_decode_only(cache, qs, seq, out, args.steps, 0, stream, args.decode_min_s)
     total_ms = max_over_ranks(t0.elapsed_time(t1), dev)
-    dec_ms = [a.elapsed_time(b) for a, b in ev]
     if cache.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
-    # the second form of the decode step: one decode call per layer (two launches each), the calls of
-    # a step captured in one CUDA graph and replayed (the first calls, outside the capture, allocate
-    # the per-layer scratch and set the kernels' attributes)
     per_layer = None
     if layers > 1:
-        q0 = qs[0].contiguous()
-        ql = [q0[l] for l in range(layers)]
-        ol = [out[l] for l in range(layers)]
-        for l in range(layers):
-            cache.decode(l, ql[l], seq, ol[l])
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            for l in range(layers):
-                cache.decode(l, ql[l], seq, ol[l])
-        for _ in range(args.warmup):
-            graph.replay()
-        torch.cuda.synchronize()
-        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        g0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        g1.record(stream)
-        torch.cuda.synchronize()
+        g_s = max_over_ranks(time_per_layer_graph(cache, qs, seq, out, layers, args.steps, args.warmup, stream), dev)
         if cache.status() != 0:
             raise RuntimeError("device status set during the per-layer graph timing")
-        g_s = max_over_ranks(g0.elapsed_time(g1), dev) / args.steps / 1e3
         per_layer = {"form": "per-layer decode calls captured in one CUDA graph", "decode_us_per_step": g_s * 1e6,
-                     "launches_per_step": 2 * layers, "tokens_per_s": weak_scaling_value(float(lens.sum()), world, g_s * 1e3)}
-        del graph
+                     "launches_per_step": 2 * layers, "vs_all_layer_call": g_s * 1e6 / dec_us,
+                     "tokens_per_s": weak_scaling_value(float(lens.sum()), world, g_s * 1e3)}
 
     # end-to-end through the public API: host inputs in, host output out, every step
     q_h = [q.cpu().pin_memory() for q in qs]
@@ -354,50 +469,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
-    # bulk (prefill-sized) append, timed on its own after the decode measurements: the workload's
-    # prefill chunk written at the end of every sequence where the workload names one (the cache has
-    # room for it), else a rewrite of positions [0, 4096) of every layer from the same seeded inputs
-    # (identical page bytes; the window ring then holds those positions, and nothing decodes after)
-    Tc = int(w.get("prefill_chunk", 4096))
-    if w.get("prefill_chunk"):
-        kc, vc = synth.kv_tokens(w, 0, B, H, 0, Tc, device=dev)
-        kc = torch.stack([kc] * layers) if layers > 1 else kc
-        vc = torch.stack([vc] * layers) if layers > 1 else vc
-        pos_c = torch.as_tensor(lens.astype(np.int32), device=dev)
-    else:
-        kl = [synth.kv_tokens(w, l, B, H, 0, Tc, device=dev) for l in range(layers)]
-        kc = torch.stack([k for k, _ in kl]).contiguous()
-        vc = torch.stack([v for _, v in kl]).contiguous()
-        del kl
-        pos_c = torch.zeros(B, dtype=torch.int32, device=dev)
-    lay = -1 if layers > 1 else 0
-    for _ in range(3):
-        cache.append(lay, kc, vc, pos_c)
-    torch.cuda.synchronize()
-    a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 10
-    a0.record(stream)
-    for _ in range(reps):
-        cache.append(lay, kc, vc, pos_c)
-    a1.record(stream)
-    torch.cuda.synchronize()
-    if cache.status() != 0:
-        raise RuntimeError("device status set during the bulk append")
-    a_s = a0.elapsed_time(a1) / reps / 1e3
-    a_bytes = bulk_append_bytes(w, layers, Tc)
-    append_res = {"tokens_per_sequence": Tc, "us": a_s * 1e6, "algorithmic_bytes": a_bytes,
-                  "achieved_gbs": a_bytes / a_s / 1e9, "tokens_per_s": layers * B * Tc / a_s,
-                  "kernel": "append_bulk_kernel" + (" + append_kernel (TQ3 keys)" if w["k_format"] == "tq3_qjl" else "")}
-    del kc, vc
+    h2d_bytes = int(q_h[0].numel() * q_h[0].element_size() + 2 * knew.numel() * knew.element_size())
+    d2h_bytes = int(out_h.numel() * 4)
+    peak, peak_src = hbm_peak()
+    append_res = time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src)
+    del cache, qs, out, q_h, q_d, k_d, v_d
+    torch.cuda.empty_cache()
 
     tokens_per_rank = float(lens.sum())  # sequence lengths summed; every layer attends them
     ms_step = total_ms / args.steps
     value = weak_scaling_value(tokens_per_rank, world, ms_step)
-    alg = algorithmic_bytes(w, layers, lens)
-    dec_avg_s = statistics.mean(dec_ms) / 1e3
-    peak, peak_src = hbm_peak()
-    achieved = alg / dec_avg_s / 1e9
-    traffic = measured_traffic(args.workload)
+    roof = decode_roofline(args.workload, w, layers, lens, dec_us, dec_calls)
     result = None
     if rank == 0:
         result = {
@@ -407,18 +489,14 @@ def run_gpu(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "q4/fp16-mma,f32-accum" if w["k_format"] == "q4g32" else "tq3+qjl/q4,f32-accum",
             "data": "synthetic (seeded N(0,1) with outlier channels, shapes of the workload; no weights)",
             "config": bench_config(args.workload, w, layers, lens, world),
-            "hbm_gbs": achieved,
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_src,
-                         "traffic": traffic, "algorithmic_bytes_per_launch": alg,
-                         "kernel": "decode call: decode_kernel (all layers) + merge_kernel",
-                         "decode_us_avg": dec_avg_s * 1e6},
+            "hbm_gbs": roof["achieved"],
+            "roofline": roof,
             "e2e": {"value": weak_scaling_value(tokens_per_rank, world, e2e_ms / args.steps), "unit": "tokens/s",
-                    "h2d_bytes_per_step": int(qs[0].numel() * qs[0].element_size() + 2 * knew.numel() * knew.element_size()),
-                    "d2h_bytes_per_step": int(out.numel() * 4), "ms_per_step": e2e_ms / args.steps},
+                    "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_ms / args.steps},
             "gpu_launches": 3 * args.steps,
             "decode_per_layer_graph": per_layer,
             "clocks": clk.summary(),
+            "bulk_append": append_res,
         }
         if layers < w["n_layers"]:
             # only `layers` of the model's layers are allocated and timed; the whole-model step
@@ -429,12 +507,14 @@ def run_gpu(args):
             result["us_per_step"] = ms_step * f * 1e3
             result["ms_per_step_timed_layers"] = ms_step
             result["e2e"]["value"] /= f
-        peak_a = peak
-        append_res["roofline"] = {"bound": "hbm", "achieved": append_res["achieved_gbs"], "peak": peak_a,
-                                  "unit": "GB/s", "frac": append_res["achieved_gbs"] / peak_a,
-                                  "peak_source": peak_src}
-        result["bulk_append"] = append_res
-    return result, cache, w, layers, lens
+    others = [n for n in (args.also or []) if n != args.workload]
+    if others and world == 1 and args.batch is None:
+        with Clocks(local) as clk2:
+            res_o = {n: measure_other_workload(n, args, dev, stream) for n in others}
+        if result is not None:
+            result["workloads"] = res_o
+            result["workloads_clocks"] = clk2.summary()
+    return result, w, layers, lens
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -575,7 +655,8 @@ def _baseline_record(w, layers, lens, results, procs, budget_s, all_cores: bool)
             "per_core_value": per_core,
             "sample": f"numpy oracle decode of {len(results)} units ({calls} timed calls) of the "
                       f"{layers * len(lens) * H} in one step, scaled by tokens attended to the "
-                      f"whole step; their encode not timed; {how}"}
+                      f"whole step; not timed: the oracle's encode of each unit and the step's append of "
+                      f"one token per layer (about 1/32000 of a step's tokens at these lengths); {how}"}
 
 
 ORACLE_MAX_WORKERS = 64       # bounds the pool's start-up time and memory on very large hosts
@@ -654,7 +735,14 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="llama3.2-3b-32k", choices=list(synth.WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE_WORKLOAD, choices=list(synth.WORKLOADS))
+    ap.add_argument("--also", nargs="*", default=list(OTHER_WORKLOADS), choices=list(synth.WORKLOADS),
+                    help="workloads measured after the headline one (decode roofline, per-layer form, "
+                         "bulk append); none with --also alone")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="keep only the first B sequences of the workload (smaller profiler captures)")
+    ap.add_argument("--decode-min-s", type=float, default=DECODE_ROOFLINE_MIN_S,
+                    help="seconds of back-to-back decode calls timed for the roofline (0: --steps calls)")
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -665,7 +753,7 @@ def main():
         if res is not None:
             print(json.dumps(res))
         return
-    res, cache, w, layers, lens = run_gpu(args)
+    res, w, layers, lens = run_gpu(args)
     if res is not None:
         if not args.no_cpu_baseline and res["n_gpus"] == 1:
             res["cpu_baseline"] = cpu_baseline(w, layers, lens)
