@@ -110,8 +110,7 @@ typedef struct kvq_cache {
  *   pages      [n_layers][n_pages][n_kv_heads][page_bytes]; one page = 64 tokens of one
  *              (layer, kv-head) stored as two 32-token halves (tokens 0-31, 32-63), each half
  *              contiguous with regions in order (t = token index within the half):
- *     K main   Q4G32: 64 B per token at 64t;  TQ3_QJL: 48 B codes at 48t, then 16 B sign bits at
- *              1536 + 16t
+ *     K main   Q4G32 and TQ3_QJL: 64 B per token at 64t
  *     V main   64 B per token at 2048 + 64t
  *     K meta   at 4096: Q4G32 per token fp16 {scale[4], zero[4]} (512 B); TQ3_QJL fp16 norm[32],
  *              gamma[32] (128 B)
@@ -124,8 +123,9 @@ typedef struct kvq_cache {
  *     for r = 0..7, G = 0..3 the 4 bytes at 128p + 16*((r + 2*(p mod 4)) mod 8) + 4G are
  *     [token 2p byte0, token 2p+1 byte0, token 2p byte1, token 2p+1 byte1], where byte0 holds
  *     channels 32G + 4r (low nibble) and 32G + 4r + 1, byte1 channels 32G + 4r + 2 and + 3.
- *   TQ3 record: code of channel j at bits 3j .. 3j+2 of the 48-byte little-endian stream; sign
- *     bit i (= (S r)_i >= 0) at bit i of the 16-byte stream.
+ *   TQ3_QJL K record (64 B per token): byte j holds the 3-bit codes of channels 2j (bits 0-2) and
+ *     2j + 1 (bits 3-5) and the QJL sign bits (1 = (S r)_i >= 0) of projections i = 2j (bit 6) and
+ *     2j + 1 (bit 7).
  */
 
 /*

@@ -125,12 +125,14 @@ static void build_codebook(CodebookDev* cb) {
   }
   for (int k = 0; k < 7; ++k) cb->bnd[k] = (cf[k] + cf[k + 1]) / 2.0f;
   cb->bnd[7] = INFINITY;
-  for (int i = 0; i < 64; ++i) {
-    const __half lo = cb->cent[i & 7], hi = cb->cent[i >> 3];
+  for (int v = 0; v < 256; ++v) {
+    const __half lo = cb->cent[v & 7], hi = cb->cent[(v >> 3) & 7];
     uint16_t l, h;
     std::memcpy(&l, &lo, 2);
     std::memcpy(&h, &hi, 2);
-    cb->lut[i] = (uint32_t)l | ((uint32_t)h << 16);
+    const uint32_t s0 = (v >> 6) & 1 ? 0x3C00u : 0xBC00u;  // fp16 +1 / -1
+    const uint32_t s1 = (v >> 7) & 1 ? 0x3C00u : 0xBC00u;
+    cb->lut8[v] = make_uint2((uint32_t)l | ((uint32_t)h << 16), s0 | (s1 << 16));
   }
 }
 

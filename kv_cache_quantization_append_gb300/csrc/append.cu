@@ -76,8 +76,8 @@ __device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, int kv,
 constexpr int VPW = 4;  // vectors (consecutive tokens) per warp: their loads are issued together
 
 // encode one vector (lane holds channels 4*lane..+3 of the raw input) into its page and ring slot
-__device__ __forceinline__ void encode_vector(const AppendArgs& a, uint32_t (&sbits)[12], int lane, int kv,
-                                              int layer, int b, int h, int t, int p, float4 xin) {
+__device__ __forceinline__ void encode_vector(const AppendArgs& a, int lane, int kv, int layer, int b, int h,
+                                              int t, int p, float4 xin) {
   const int H = a.Hkv;
   // raw copy into the window ring for the last `window` tokens of this call
   if (a.W > 0 && t >= a.T - a.W) {
@@ -137,22 +137,15 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, uint32_t (&sb
         acc[3] = __fadd_rn(acc[3], __fmul_rn(s4.w, rj));
       }
     }
-    uint32_t word = 0;
+    // record byte 2*lane + e holds the codes of channels 4*lane + 2e, +1 (bits 0-2, 3-5) and the
+    // sign bits of projections 4*lane + 2e, +1 (bits 6, 7): this lane's halfword
+    uint32_t hw = 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) word |= (acc[e] >= 0.0f ? 1u : 0u) << (4 * (lane & 7) + e);
-#pragma unroll
-    for (int m = 1; m < 8; m <<= 1) word |= __shfl_xor_sync(FULL, word, m);
-    // 3-bit codes: channel j at bits 3j..3j+2 of a 384-bit stream; lane holds bits 12*lane..+11
-    if (lane < 12) sbits[lane] = 0u;
-    __syncwarp();
-    const int bit = 12 * lane, w0 = bit >> 5, sh = bit & 31;
-    atomicOr(&sbits[w0], c12 << sh);
-    if (sh > 20) atomicOr(&sbits[w0 + 1], c12 >> (32 - sh));
-    __syncwarp();
-    uint8_t* rec = pg + (size_t)tin * 48;
-    if (lane < 12) reinterpret_cast<uint32_t*>(rec)[lane] = sbits[lane];
-    uint32_t* sgn = reinterpret_cast<uint32_t*>(pg + 48 * HALF + (size_t)tin * 16);
-    if ((lane & 7) == 0) sgn[lane >> 3] = word;
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t code = (c12 >> (3 * e)) & 7u, bitv = acc[e] >= 0.0f ? 1u : 0u;
+      hw |= (code << (8 * (e >> 1) + 3 * (e & 1))) | (bitv << (8 * (e >> 1) + 6 + (e & 1)));
+    }
+    reinterpret_cast<uint16_t*>(pg + (size_t)tin * 64)[lane] = (uint16_t)hw;
     if (lane == 0) {
       __half* meta = reinterpret_cast<__half*>(pg + a.L.off_kmeta);
       meta[tin] = __float2half_rn(n);
@@ -188,7 +181,6 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, uint32_t (&sb
 }
 
 __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
-  __shared__ uint32_t sbits[WARPS][12];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   // a dependent decode launch may start its set-up now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;");
@@ -222,7 +214,7 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
     if (j < nv) x[j] = load4_in(kv ? a.v : a.k, (vec0 + j) * D + 4 * lane, a.in_bf16);
 #pragma unroll
   for (int j = 0; j < VPW; ++j)
-    if (j < nv) encode_vector(a, sbits[wl], lane, kv, layer, b, h, t0 + j, p0 + t0 + j, x[j]);
+    if (j < nv) encode_vector(a, lane, kv, layer, b, h, t0 + j, p0 + t0 + j, x[j]);
 }
 
 }  // namespace

@@ -35,7 +35,6 @@ namespace kvq {
 
 namespace {
 
-constexpr int STAGE_BYTES = 5120;            // max half-page (Q4/Q4) and window chunk (4 KB)
 constexpr int REC_FLOATS = 16 + 2 * MAX_GQA * D;
 constexpr int KIND_WINDOW = 0, KIND_QUANT = 1;
 constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wait after ~1 s
@@ -64,14 +63,18 @@ struct Geo {
 #endif
   static constexpr int NSLOT = TQ ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
   static constexpr int NSTAGE = NSLOT * NCW;
-  static constexpr int SM_STAGES = 0;
-  static constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE_BYTES;
+  // a stage holds one half-page (Q4/Q4 5120 B, TQ3/Q4 4736 B) or one window chunk (4096 B)
+  static constexpr int STAGE = TQ ? 4736 : 5120;
+  // TQ3 record-byte table: entry v (256 of them) at 256 v: lane j's copy of the centroid pair at
+  // +4 j, of the sign pair at +128 + 4 j
+  static constexpr int LUT_BYTES = TQ ? 256 * 256 : 0;
+  static constexpr int SM_LUT = 0;
+  static constexpr int SM_STAGES = SM_LUT + LUT_BYTES;
+  static constexpr int SM_BARS = SM_STAGES + NSTAGE * STAGE;
   static constexpr int SM_DESC = SM_BARS + 2 * NSTAGE * 8;
   static constexpr int SM_Q = SM_DESC + NSTAGE * 16;                         // [NCW][4][128] float
-  static constexpr int SM_SQ = SM_Q + NCW * MAX_GQA * D * 4;                 // [NCW][4][128] (TQ)
-  static constexpr int SM_QSUM = SM_SQ + (TQ ? NCW * MAX_GQA * D * 4 : 0);   // [NCW][4][4] float
-  static constexpr int SM_LUT = SM_QSUM + NCW * 16 * 4;                      // [64][32] u32 (TQ)
-  static constexpr int SM_P = SM_LUT + (TQ ? 64 * 32 * 4 : 0);               // [NCW][2][4][32] fp16
+  static constexpr int SM_QSUM = SM_Q + NCW * MAX_GQA * D * 4;               // [NCW][4][4] float
+  static constexpr int SM_P = SM_QSUM + NCW * 16 * 4;                        // [NCW][2][4][32] fp16
   static constexpr int SM_WML = SM_P + NCW * 2 * MAX_GQA * HALF * 2;         // [NCW][8] float
   static constexpr int SM_WPOS = SM_WML + NCW * 8 * 4;                       // [NCW+1] int4, i64
   static constexpr int SM_SEQ = SM_WPOS + (NCW + 1) * 24;                     // 6 int[batch+1]
@@ -149,6 +152,27 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// 32-bit shared-memory load at a shared-window address, for tables written before the loop that
+// reads them (behind a barrier).  Not volatile and without a memory clobber, so the compiler may
+// schedule it freely; the addresses used depend on record bytes read from a stage after its
+// barrier wait, which keeps each load after that wait.
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+// The same at a shared-window address given as a register plus a constant offset (the offset
+// goes into the load's immediate field: no add instruction).
+template <int OFF>
+__device__ __forceinline__ uint32_t lds_u32_at(uint32_t addr) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1+%2];" : "=r"(v) : "r"(addr), "n"(OFF));
+  return v;
+}
+// Shared-window address at which this kernel's dynamic shared memory starts when the kernel has no
+// static shared memory: the block's first 1 KB is reserved by the system on this architecture.
+// Checked at run time (a kernel that finds another base takes the path with explicit adds).
+constexpr uint32_t DYN_SMEM_WINDOW_BASE = 0x400;
 __device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
@@ -156,21 +180,6 @@ __device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__
 // byte and converted as an FP8 E4M3 value, which for bit patterns 0..15 (exponent field 0 or 1)
 // is exactly c * 2^-9.  lo0 = (n0, n2), lo1 = (n4, n6), hi0 = (n1, n3), hi1 = (n5, n7) where n_m is
 // the m-th nibble (low nibble of byte k is n_2k).
-// a * b + c as an integer multiply-add (the FMA pipe; kept as written, not turned into ALU shifts)
-__device__ __forceinline__ uint32_t imad_u32(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-// 32-bit shared-memory load at a shared-window address, for data written before the loop that reads
-// it (the centroid table: written in the prologue, before a barrier).  Not volatile and without a
-// memory clobber, so the compiler may schedule it freely; the addresses used depend on codes read
-// from a stage after its barrier wait, which keeps each load after that wait.
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
 __device__ __forceinline__ void cvt8(uint32_t w, uint32_t& lo0, uint32_t& lo1, uint32_t& hi0, uint32_t& hi1) {
   const uint32_t lo = w & 0x0F0F0F0Fu;
   // a plain shift: the multiply-high form of w >> 4 (integer pipe) measured 4-5 % slower here
@@ -264,11 +273,12 @@ template <int KF>
 struct Kernel {
   using GE = Geo<KF>;
   static constexpr int NCW = GE::NCW;
-  static constexpr int SM_Q = GE::SM_Q, SM_SQ = GE::SM_SQ, SM_QSUM = GE::SM_QSUM, SM_LUT = GE::SM_LUT;
+  static constexpr int SM_Q = GE::SM_Q, SM_QSUM = GE::SM_QSUM, SM_LUT = GE::SM_LUT;
   static constexpr int SM_P = GE::SM_P;
   const DecodeArgs& a;
   uint8_t* smem;
   int lane, warp;
+  bool lut_base_known;  // dynamic shared memory starts at DYN_SMEM_WINDOW_BASE (TQ3 table addressing)
   int B, H, W, g, Hq;
   long long S_layer, S;  // steps per layer, steps of the call
   long long C_layer, C;  // costs per layer, cost of the call
@@ -390,7 +400,6 @@ struct Kernel {
       return;
     }
     float* qs = reinterpret_cast<float*>(smem + SM_Q) + warp * MAX_GQA * D;
-    float* sqs = reinterpret_cast<float*>(smem + SM_SQ) + warp * MAX_GQA * D;
     float* qsum = reinterpret_cast<float*>(smem + SM_QSUM) + warp * 16;
     const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
 #pragma unroll
@@ -415,30 +424,11 @@ struct Kernel {
       if ((lane & 7) == 0) qsum[hh * 4 + (lane >> 3)] = s;
     }
     __syncwarp();
-    if (KF == KVQ_TQ3_QJL) {
-      // S q~ for each head: lane computes projections 4*lane .. 4*lane+3
-      const float4* st = reinterpret_cast<const float4*>(a.p.qjl_t) + lane;
-      for (int hh = 0; hh < g; ++hh) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-        for (int j = 0; j < D; ++j) {
-          const float qj = qs[hh * D + j];
-          const float4 s4 = st[j * (D / 4)];
-          acc.x += s4.x * qj;
-          acc.y += s4.y * qj;
-          acc.z += s4.z * qj;
-          acc.w += s4.w * qj;
-        }
-        *reinterpret_cast<float4*>(sqs + hh * D + 4 * lane) = acc;
-      }
-      __syncwarp();
-    }
     const int r = lane >> 2, i = lane & 3;
     const int head = r >> 1;
     const bool lo = r & 1;
     const bool hv = head < g;
     const float* qh = qs + head * D;
-    const float* sh = sqs + head * D;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       int d0, d1, d2, d3;
@@ -462,18 +452,43 @@ struct Kernel {
       const uint32_t v2 = hv ? split_pick(qh[d2] * us, lo) : 0u, v3 = hv ? split_pick(qh[d3] * us, lo) : 0u;
       st.qb[kk][0] = v0 | (v1 << 16);
       st.qb[kk][1] = v2 | (v3 << 16);
-      if (KF == KVQ_TQ3_QJL) {
-        // signs: k-step kk holds projections 32i + 2kk + {0, 16 | 1, 17}
-        const int p0 = 32 * i + 2 * kk;
-        const uint32_t s0 = hv ? split_pick(sh[p0], lo) : 0u, s1 = hv ? split_pick(sh[p0 + 16], lo) : 0u;
-        const uint32_t s2 = hv ? split_pick(sh[p0 + 1], lo) : 0u, s3 = hv ? split_pick(sh[p0 + 17], lo) : 0u;
-        st.sb[kk][0] = s0 | (s1 << 16);
-        st.sb[kk][1] = s2 | (s3 << 16);
-      }
     }
     // zero-point term as one more k-step: k = group G (0..3), column = head (hi | lo)
     st.zb = (hv && i < 2) ? split_pick(qsum[head * 4 + 2 * i], lo) | (split_pick(qsum[head * 4 + 2 * i + 1], lo) << 16)
                           : 0u;
+    if (KF == KVQ_TQ3_QJL) {
+      // S q~ for each head (lane computes projections 4*lane .. 4*lane+3 from q~), written over q~
+      // once every lane has read its q~ fragments; signs use the codes' k-step mapping: k-step kk
+      // holds projections 32i + 4kk + {0,1 | 2,3}
+      const float4* stp = reinterpret_cast<const float4*>(a.p.qjl_t) + lane;
+      float4 sq[MAX_GQA];
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh) sq[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (int j = 0; j < D; ++j) {
+        const float4 s4 = stp[j * (D / 4)];
+#pragma unroll
+        for (int hh = 0; hh < MAX_GQA; ++hh) {
+          const float qj = qs[hh * D + j];
+          sq[hh].x += s4.x * qj;
+          sq[hh].y += s4.y * qj;
+          sq[hh].z += s4.z * qj;
+          sq[hh].w += s4.w * qj;
+        }
+      }
+      __syncwarp();
+#pragma unroll
+      for (int hh = 0; hh < MAX_GQA; ++hh) *reinterpret_cast<float4*>(qs + hh * D + 4 * lane) = sq[hh];
+      __syncwarp();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int p0 = 32 * i + 4 * kk;
+        const uint32_t s0 = hv ? split_pick(qh[p0], lo) : 0u, s1 = hv ? split_pick(qh[p0 + 1], lo) : 0u;
+        const uint32_t s2 = hv ? split_pick(qh[p0 + 2], lo) : 0u, s3 = hv ? split_pick(qh[p0 + 3], lo) : 0u;
+        st.sb[kk][0] = s0 | (s1 << 16);
+        st.sb[kk][1] = s2 | (s3 << 16);
+      }
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j) st.acc[j][0] = st.acc[j][1] = st.acc[j][2] = st.acc[j][3] = 0.f;
     st.zacc[0] = st.zacc[1] = st.zacc[2] = st.zacc[3] = 0.f;
@@ -584,44 +599,70 @@ struct Kernel {
     const uint8_t* kmain = stage;
     const uint8_t* kmeta = stage + OFF_KMETA;
     if (KF == KVQ_TQ3_QJL) {
-      float cacc[4] = {0.f, 0.f, 0.f, 0.f}, sacc[4] = {0.f, 0.f, 0.f, 0.f};
-      // this lane's column of the centroid-pair table (entry j at byte 128 j): the entry address is
-      // formed by one integer multiply-add (FMA pipe) from the extracted 6-bit field
-      const uint32_t lutb = (uint32_t)__cvta_generic_to_shared(smem + SM_LUT) + 4u * lane;
-      const uint32_t* ca = reinterpret_cast<const uint32_t*>(kmain + ta * 48 + 12 * i);
-      const uint32_t* cbp = reinterpret_cast<const uint32_t*>(kmain + tb * 48 + 12 * i);
-      const uint32_t wa[4] = {ca[0], ca[1], ca[2], 0u};
-      const uint32_t wb[4] = {cbp[0], cbp[1], cbp[2], 0u};
+      // record byte 16i + 2kk + e of a token = its A operands of k-step kk, slot e (k = 2i, 2i+1 for
+      // e = 0, 2i + 8, 2i + 9 for e = 1): two 3-bit codes and two QJL sign bits.  One byte_perm
+      // puts the byte above this lane's table offset; the entry's centroid pair and +-1 sign pair
+      // are read as two 4-byte loads, so that each lands directly in its mma operand register (an
+      // 8-byte load would pair a centroid and a sign register, and the operands would need moves).
+      // even and odd k-steps accumulate separately: four independent mma chains instead of two
+      float cacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const uint4 ka = *reinterpret_cast<const uint4*>(kmain + ta * 64 + 16 * i);
+      const uint4 kb = *reinterpret_cast<const uint4*>(kmain + tb * 64 + 16 * i);
+      const uint32_t lane4 = 4u * lane;
+      constexpr int LUT_WIN = (int)DYN_SMEM_WINDOW_BASE + SM_LUT;
+      if (lut_base_known) {
+        // the table's shared-window address is the constant LUT_WIN: one byte_perm per byte
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t pa[2], pb[2];
+        for (int kk = 0; kk < 8; ++kk) {
+          const int wi = kk >> 1;
+          const uint32_t wa = wi == 0 ? ka.x : wi == 1 ? ka.y : wi == 2 ? ka.z : ka.w;
+          const uint32_t wb = wi == 0 ? kb.x : wi == 1 ? kb.y : wi == 2 ? kb.z : kb.w;
+          uint32_t ca[2], cb[2], sa[2], sb[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int bit = 6 * (2 * kk + e), wi = bit >> 5, sh = bit & 31;
-          pa[e] = lds_u32(imad_u32(__funnelshift_r(wa[wi], wa[wi + 1], sh) & 63u, 128u, lutb));
-          pb[e] = lds_u32(imad_u32(__funnelshift_r(wb[wi], wb[wi + 1], sh) & 63u, 128u, lutb));
+          for (int e = 0; e < 2; ++e) {
+            // result bytes: [lane4, record byte 2(kk & 1) + e, 0, 0] = 256 v + 4 lane: the lane's
+            // copy of entry v's centroid pair; its sign pair is 128 bytes further
+            const uint32_t sel = 0x5504u | ((uint32_t)(2 * (kk & 1) + e) << 4);
+            const uint32_t pa = __byte_perm(wa, lane4, sel), pb = __byte_perm(wb, lane4, sel);
+            ca[e] = lds_u32_at<LUT_WIN>(pa);
+            sa[e] = lds_u32_at<LUT_WIN + 128>(pa);
+            cb[e] = lds_u32_at<LUT_WIN>(pb);
+            sb[e] = lds_u32_at<LUT_WIN + 128>(pb);
+          }
+          mma16816(cacc[kk & 1], ca[0], cb[0], ca[1], cb[1], st.qb[kk][0], st.qb[kk][1]);
+          mma16816(sacc[kk & 1], sa[0], sb[0], sa[1], sb[1], st.sb[kk][0], st.sb[kk][1]);
         }
-        mma16816(cacc, pa[0], pb[0], pa[1], pb[1], st.qb[kk][0], st.qb[kk][1]);
-      }
-      const uint32_t sa = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * HALF + ta * 16 + 4 * i);
-      const uint32_t sbw = ~*reinterpret_cast<const uint32_t*>(kmain + 48 * HALF + tb * 16 + 4 * i);
+      } else {
+        const uint32_t lut = smem_addr(smem + SM_LUT);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        // half2 index k' = 2kk + eps holds bits (k', k'+16) as +-1.0
-        const int k0 = 2 * kk, k1 = 2 * kk + 1;
-        // the bit moves to the fp16 sign by a multiply-add that also adds 1.0 (0x3C00) to both halves:
-        // one and on the ALU pipe, one integer mad on the FMA pipe
-        const uint32_t a0 = imad_u32(sa & (0x00010001u << k0), 1u << (15 - k0), 0x3C003C00u);
-        const uint32_t a1 = imad_u32(sbw & (0x00010001u << k0), 1u << (15 - k0), 0x3C003C00u);
-        const uint32_t a2 = imad_u32(sa & (0x00010001u << k1), 1u << (15 - k1), 0x3C003C00u);
-        const uint32_t a3 = imad_u32(sbw & (0x00010001u << k1), 1u << (15 - k1), 0x3C003C00u);
-        mma16816(sacc, a0, a1, a2, a3, st.sb[kk][0], st.sb[kk][1]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const int wi = kk >> 1;
+          const uint32_t wa = wi == 0 ? ka.x : wi == 1 ? ka.y : wi == 2 ? ka.z : ka.w;
+          const uint32_t wb = wi == 0 ? kb.x : wi == 1 ? kb.y : wi == 2 ? kb.z : kb.w;
+          uint32_t ca[2], cb[2], sa[2], sb[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t sel = 0x5504u | ((uint32_t)(2 * (kk & 1) + e) << 4);
+            const uint32_t pa = lut + __byte_perm(wa, lane4, sel), pb = lut + __byte_perm(wb, lane4, sel);
+            ca[e] = lds_u32(pa);
+            sa[e] = lds_u32(pa + 128);
+            cb[e] = lds_u32(pb);
+            sb[e] = lds_u32(pb + 128);
+          }
+          mma16816(cacc[kk & 1], ca[0], cb[0], ca[1], cb[1], st.qb[kk][0], st.qb[kk][1]);
+          mma16816(sacc[kk & 1], sa[0], sb[0], sa[1], sb[1], st.sb[kk][0], st.sb[kk][1]);
+        }
       }
       const __half* nrm = reinterpret_cast<const __half*>(kmeta);
       const float na = __half2float(nrm[ta]), nb = __half2float(nrm[tb]);
       const float ga = __half2float(nrm[HALF + ta]), gb = __half2float(nrm[HALF + tb]);
-      la = na * ((cacc[0] + cacc[1]) + QJL_CONST * ga * (sacc[0] + sacc[1]));
-      lb = nb * ((cacc[2] + cacc[3]) + QJL_CONST * gb * (sacc[2] + sacc[3]));
+      const float ca0 = (cacc[0][0] + cacc[1][0]) + (cacc[0][1] + cacc[1][1]);
+      const float cb0 = (cacc[0][2] + cacc[1][2]) + (cacc[0][3] + cacc[1][3]);
+      const float sa0 = (sacc[0][0] + sacc[1][0]) + (sacc[0][1] + sacc[1][1]);
+      const float sb0 = (sacc[0][2] + sacc[1][2]) + (sacc[0][3] + sacc[1][3]);
+      la = na * (ca0 + QJL_CONST * ga * sa0);
+      lb = nb * (cb0 + QJL_CONST * gb * sb0);
     } else {
       const uint4 ka = *reinterpret_cast<const uint4*>(kmain + ta * 64 + 16 * i);
       const uint4 kb = *reinterpret_cast<const uint4*>(kmain + tb * 64 + 16 * i);
@@ -1138,6 +1179,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   const int tid = threadIdx.x;
   K.warp = tid >> 5;
   K.lane = tid & 31;
+  K.lut_base_known = smem_addr(smem) == DYN_SMEM_WINDOW_BASE;
   K.B = a.batch;
   K.H = a.Hkv;
   K.W = a.W;
@@ -1154,6 +1196,10 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   uint64_t* empty = full + NSTAGE;
   int4* desc = reinterpret_cast<int4*>(smem + GE::SM_DESC);
 
+  // the TQ3 decode table (2 KB in the cache header) is read once per CTA into the first stage, and
+  // expanded to its per-lane copies after the barrier below (the stages are idle until then)
+  if (KF == KVQ_TQ3_QJL && tid < 256)
+    reinterpret_cast<uint2*>(smem + GE::SM_STAGES)[tid] = a.p.cb->lut8[tid];
   // ---- per-sequence step counts: window chunks first, then quantised half-pages
   for (int b = tid; b < B; b += NTHREADS) {
     int L = a.seq_lens[b];
@@ -1207,8 +1253,10 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (KF == KVQ_TQ3_QJL) {
+    // entry v: 32 lane copies of its centroid pair, then 32 lane copies of its sign pair
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(smem + GE::SM_STAGES);
     uint32_t* lut = reinterpret_cast<uint32_t*>(smem + GE::SM_LUT);
-    for (int idx = tid; idx < 64 * 32; idx += NTHREADS) lut[idx] = a.p.cb->lut[idx >> 5];
+    for (int idx = tid; idx < 256 * 64; idx += NTHREADS) lut[idx] = src[2 * (idx >> 6) + ((idx >> 5) & 1)];
   }
   __syncthreads();
   K.sq.S = sS;
@@ -1278,7 +1326,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
         const int layer = a.layer0 + ps.ll;
         const int L = sL[ps.b];
         const int nwin = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
-        uint8_t* dst = smem + GE::SM_STAGES + slot * STAGE_BYTES;
+        uint8_t* dst = smem + GE::SM_STAGES + slot * GE::STAGE;
         if (ps.local < nwin) {
           const int s0 = ps.local * WCHUNK;
           const int ntok = min(WCHUNK, min(L, W) - s0);
@@ -1387,7 +1435,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       if (kind == KIND_WINDOW) hasw = true;
       else hasq = true;
     }
-    uint8_t* stage = smem + GE::SM_STAGES + slot * STAGE_BYTES;
+    uint8_t* stage = smem + GE::SM_STAGES + slot * GE::STAGE;
     if (d.z > 0) {
       if (d.y == KIND_WINDOW) K.window_step(stage, d.z, ws, st);
       else K.quant_step(stage, d.z, st);

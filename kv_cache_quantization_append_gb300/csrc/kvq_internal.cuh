@@ -42,7 +42,10 @@ struct Layout {
 struct CodebookDev {
   __half cent[8];        // TQ3 centroids (ascending)
   float bnd[8];          // 7 boundaries (midpoints), [7] unused
-  uint32_t lut[64];      // half2 (cent[i & 7], cent[i >> 3]) for a pair of 3-bit codes
+  // decode table of one TQ3 record byte v (two 3-bit codes in bits 0-5, two QJL sign bits in
+  // bits 6-7): .x = half2 (cent[v & 7], cent[(v >> 3) & 7]), .y = half2 of the signs as +-1
+  // (bit set = +1, the sign of a non-negative projection)
+  uint2 lut8[256];
 };
 
 bool compute_layout(const kvq_config& c, Layout* L);

@@ -73,9 +73,12 @@ def _q4v_codes(half_v: np.ndarray, t: np.ndarray) -> np.ndarray:
     return out
 
 
-def _tq3_codes(rec: np.ndarray) -> np.ndarray:
-    bits = np.unpackbits(rec, axis=1, bitorder="little")[:, :384].reshape(-1, 128, 3)
-    return (bits[..., 0] | (bits[..., 1] << 1) | (bits[..., 2] << 2)).astype(np.uint8)
+def _tq3_fields(rec: np.ndarray):
+    """TQ3 key record [T][64]: byte j holds the 3-bit codes of channels 2j (bits 0-2) and 2j + 1
+    (bits 3-5) and the QJL sign bits of projections 2j (bit 6) and 2j + 1 (bit 7)."""
+    codes = np.stack([rec & 7, (rec >> 3) & 7], axis=-1).reshape(-1, 128).astype(np.uint8)
+    bits = np.stack([(rec >> 6) & 1, rec >> 7], axis=-1).reshape(-1, 128).astype(bool)
+    return codes, bits
 
 
 def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
@@ -93,9 +96,7 @@ def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
     kmeta0 = base + 128 * H
     vmeta0 = kmeta0 + R["kmeta"] * H
     if cfg.k_format == 3:
-        out["k_code"] = _tq3_codes(_gather(buf, base + t * 48, 48))
-        sg = _gather(buf, base + 48 * H + t * 16, 16)
-        out["k_bits"] = np.unpackbits(sg, axis=1, bitorder="little").astype(bool)
+        out["k_code"], out["k_bits"] = _tq3_fields(_gather(buf, base + t * 64, 64))
         out["k_norm"] = _gather(buf, kmeta0 + t * 2, 2).view(np.float16)[:, 0]
         out["k_gamma"] = _gather(buf, kmeta0 + 2 * H + t * 2, 2).view(np.float16)[:, 0]
     else:
