@@ -45,7 +45,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the largest configuration that fits one GPU (10.2 GB streamed per step) is the headline; the other
 # large configurations are measured after it in the same run
 HEADLINE_WORKLOAD = "llama3.1-8b-tq-b8-32k"
-OTHER_WORKLOADS = ("llama3.2-3b-32k", "qwen3-4b-kvarn-128k", "dense27b-ragged-b32")
+OTHER_WORKLOADS = ("llama3.2-3b-32k", "qwen3-4b-kvarn-128k", "dense27b-ragged-b32", "llama3.2-3b-32k-k8v4")
+# bytes of one key record (a 128-value vector) per key format; a Q4G32 value record is 80 B
+K_RECORD_BYTES = {"q4g32": 80, "tq3_qjl": 68, "q8g32": 136}
+DTYPE_NAMES = {"q4g32": "q4/fp16-mma,f32-accum", "tq3_qjl": "tq3+qjl/q4,f32-accum", "q8g32": "q8/q4,fp16-mma,f32-accum"}
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -150,7 +153,7 @@ def build_cache(name: str, device="cuda", batch=None):
     w, layers, lens = workload_cfg(name, batch)
     B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
     cap = int(-(-(int(lens.max()) + 64) // 64) * 64)
-    kf = lib.KVQ_TQ3_QJL if w["k_format"] == "tq3_qjl" else lib.KVQ_Q4G32
+    kf = lib.K_FORMATS[w["k_format"]]
     bt = None
     n_pages = 0
     if w.get("page_tokens"):
@@ -202,7 +205,7 @@ def bulk_append_bytes(w, layers, T) -> int:
     (K 80 B or 68 B for TQ3 keys, V 80 B per token and kv-head) and the FP32 window copy of the
     last min(window, T) tokens (512 B each of K and V)."""
     inb = 2 if w["in_dtype"] == "bf16" else 4
-    rec = (68 if w["k_format"] == "tq3_qjl" else 80) + 80
+    rec = K_RECORD_BYTES[w["k_format"]] + 80
     per_seq_head = T * (2 * 128 * inb + rec) + min(w["window"], T) * 1024
     return layers * w["batch"] * w["n_kv_heads"] * per_seq_head
 
@@ -226,7 +229,7 @@ def algorithmic_bytes(w, layers, lens) -> int:
     """Bytes the decode step must move: packed records of the quantised tokens, the FP32 window,
     q and out (per launch over all layers)."""
     W = w["window"]
-    rec = (68 if w["k_format"] == "tq3_qjl" else 80) + 80
+    rec = K_RECORD_BYTES[w["k_format"]] + 80
     H, Hq = w["n_kv_heads"], w["n_q_heads"]
     per_layer = 0
     for L in lens:
@@ -486,7 +489,7 @@ def run_gpu(args):
             "metric": "quantized-KV decode attention: cached tokens/s (decode of all layers + append of one token per layer)",
             "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "q4/fp16-mma,f32-accum" if w["k_format"] == "q4g32" else "tq3+qjl/q4,f32-accum",
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[w["k_format"]],
             "data": "synthetic (seeded N(0,1) with outlier channels, shapes of the workload; no weights)",
             "config": bench_config(args.workload, w, layers, lens, world),
             "hbm_gbs": roof["achieved"],

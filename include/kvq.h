@@ -66,6 +66,7 @@ enum {
   KVQ_Q4G32 = 1,     /* 4-bit asymmetric codes, groups of 32 channels, fp16 scale and zero (K, V) */
   KVQ_TQ3_QJL = 3,   /* keys only: 3-bit Lloyd-Max codes of the unit vector, fp16 norm, 128 QJL
                         residual sign bits and fp16 residual norm */
+  KVQ_Q8G32 = 4,     /* keys only: 8-bit symmetric codes, groups of 32 channels, fp16 scale */
 };
 enum { KVQ_IN_F32 = 0, KVQ_IN_BF16 = 1 };
 
@@ -79,9 +80,9 @@ typedef struct kvq_config {
   int32_t window;        /* most recent tokens also kept in FP32; 0 = flat 4-bit ([QC]: 128) */
   int32_t page_tokens;   /* 64 */
   int32_t n_pages;       /* physical pages per layer; 0 = max_batch * ceil(max_seq_len / 64) */
-  int32_t k_format;      /* KVQ_Q4G32 or KVQ_TQ3_QJL */
+  int32_t k_format;      /* KVQ_Q4G32, KVQ_TQ3_QJL or KVQ_Q8G32 */
   int32_t v_format;      /* KVQ_Q4G32 */
-  int32_t sinkhorn;      /* 1 = per-channel balancing scales (Q4G32 K and V only) */
+  int32_t sinkhorn;      /* 1 = per-channel balancing scales (not with KVQ_TQ3_QJL keys) */
   int32_t group;         /* 32 */
   int32_t in_dtype;      /* KVQ_IN_F32 or KVQ_IN_BF16: dtype of k, v, q and calibration inputs */
   uint64_t seed;         /* seed of the rotation's random signs (SplitMix64 stream) */
@@ -110,12 +111,13 @@ typedef struct kvq_cache {
  *   pages      [n_layers][n_pages][n_kv_heads][page_bytes]; one page = 64 tokens of one
  *              (layer, kv-head) stored as two 32-token halves (tokens 0-31, 32-63), each half
  *              contiguous with regions in order (t = token index within the half):
- *     K main   Q4G32 and TQ3_QJL: 64 B per token at 64t
- *     V main   64 B per token at 2048 + 64t
- *     K meta   at 4096: Q4G32 per token fp16 {scale[4], zero[4]} (512 B); TQ3_QJL fp16 norm[32],
- *              gamma[32] (128 B)
+ *     K main   Q4G32 and TQ3_QJL: 64 B per token at 64t; Q8G32: 128 B per token at 128t
+ *     V main   64 B per token at K + 64t, K = 2048 (Q4G32, TQ3_QJL) or 4096 (Q8G32)
+ *     K meta   after V main: Q4G32 per token fp16 {scale[4], zero[4]} (512 B); TQ3_QJL fp16
+ *              norm[32], gamma[32] (128 B); Q8G32 per token fp16 scale[4] (256 B)
  *     V meta   after K meta: fp16 scale[4][32] then fp16 zero[4][32] (group-major, 512 B)
- *   Half sizes: Q4G32 K + Q4G32 V = 5120 B, TQ3_QJL K + Q4G32 V = 4736 B.
+ *   Half sizes: Q4G32 K + Q4G32 V = 5120 B, TQ3_QJL K + Q4G32 V = 4736 B, Q8G32 K + Q4G32 V =
+ *   6912 B.
  *   Q4G32 K record (64 B per token): 32-bit word (i, G), i, G = 0..3, at byte 16i + 4G holds channels
  *     32G + 8i .. 32G + 8i + 7 of the rotated (and balanced) vector; byte k of the word holds
  *     channel 32G + 8i + 2k in its low nibble and the next channel in its high nibble.
@@ -123,6 +125,10 @@ typedef struct kvq_cache {
  *     for r = 0..7, G = 0..3 the 4 bytes at 128p + 16*((r + 2*(p mod 4)) mod 8) + 4G are
  *     [token 2p byte0, token 2p+1 byte0, token 2p byte1, token 2p+1 byte1], where byte0 holds
  *     channels 32G + 4r (low nibble) and 32G + 4r + 1, byte1 channels 32G + 4r + 2 and + 3.
+ *   Q8G32 K record (128 B per token t): codes are stored as unsigned bytes u = c + 128 (c in
+ *     -127..127); sixteen-byte chunk m = 2i + h (i = 0..3, h = 0..1) sits at 16 * (m XOR (t mod 2))
+ *     and its 32-bit word w holds, for k = 16 (4h + w), the channels k + 2i, k + 2i + 1, k + 2i + 8,
+ *     k + 2i + 9 in bytes 0..3.  Scale d of group G (channels 32G .. 32G + 31) at K meta + 8t + 2G.
  *   TQ3_QJL K record (64 B per token): byte j holds the 3-bit codes of channels 2j (bits 0-2) and
  *     2j + 1 (bits 3-5) and the QJL sign bits (1 = (S r)_i >= 0) of projections i = 2j (bit 6) and
  *     2j + 1 (bit 7).
@@ -135,7 +141,8 @@ typedef struct kvq_cache {
  * (6.4x); the "4-bit + progressive" row adds the 128-token FP32 window on top of the 4-bit store
  * (2.33 vs 2.30 GB for Llama-3.2-3B at 32K), which is the ring counted here.  [TQ] "method
  * comparison" table, compression >= 4.5x: a TQ3_QJL key record is 68 B (3-bit codes, 128 sign bits,
- * fp16 norm and residual norm).  Total = header + 2 rings of n_layers * max_batch * n_kv_heads *
+ * fp16 norm and residual norm).  [TQ] "when to use what" and "rules" lists (keep K at Q8, cut only
+ * V): a Q8G32 key record is 136 B (8-bit codes and four fp16 scales).  Total = header + 2 rings of n_layers * max_batch * n_kv_heads *
  * window * 512 B + n_layers * n_pages * n_kv_heads pages of 64 tokens x (K record + 80 B), each
  * region rounded up to 256 B.
  */

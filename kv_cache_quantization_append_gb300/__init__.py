@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import lib
-from .lib import (KVQ_IN_BF16, KVQ_IN_F32, KVQ_Q4G32, KVQ_TQ3_QJL, kv_cache_bytes, kv_cache_init,  # noqa: F401
+from .lib import (KVQ_IN_BF16, KVQ_IN_F32, KVQ_Q4G32, KVQ_Q8G32, KVQ_TQ3_QJL, kv_cache_bytes,  # noqa: F401
+                  kv_cache_init,
                   kv_calibrate, kv_calibrate_scratch_bytes, kv_decode_attention,
                   kv_decode_scratch_bytes, kv_quant_append, kv_status, kv_strerror, make_config)
 

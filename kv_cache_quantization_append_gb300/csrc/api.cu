@@ -19,10 +19,10 @@ static bool config_ok(const kvq_config& c) {
   if (g < 1 || g > MAX_GQA) return false;
   if (c.max_batch < 1 || c.max_batch > MAX_BATCH || c.max_seq_len < 1) return false;
   if (c.window < 0 || c.window > MAX_WINDOW || c.window % WCHUNK != 0) return false;
-  if (c.k_format != KVQ_Q4G32 && c.k_format != KVQ_TQ3_QJL) return false;
+  if (c.k_format != KVQ_Q4G32 && c.k_format != KVQ_TQ3_QJL && c.k_format != KVQ_Q8G32) return false;
   if (c.v_format != KVQ_Q4G32) return false;
   if (c.sinkhorn != 0 && c.sinkhorn != 1) return false;
-  if (c.sinkhorn && c.k_format != KVQ_Q4G32) return false;
+  if (c.sinkhorn && c.k_format == KVQ_TQ3_QJL) return false;
   if (c.in_dtype != KVQ_IN_F32 && c.in_dtype != KVQ_IN_BF16) return false;
   if (c.n_pages < 0) return false;
   return true;
@@ -35,9 +35,11 @@ bool compute_layout(const kvq_config& c, Layout* L) {
   const long long contiguous = (long long)c.max_batch * l.max_pages_per_seq;
   if (contiguous > INT32_MAX) return false;
   l.n_pages = c.n_pages > 0 ? c.n_pages : (int)contiguous;
-  l.kmeta_bytes = (c.k_format == KVQ_TQ3_QJL) ? 4 : 16;
-  l.off_vmain = 64 * HALF;
-  l.off_kmeta = 128 * HALF;
+  // per token: K main 64 B (Q4G32, TQ3_QJL) or 128 B (Q8G32); K meta 16 B (Q4G32 scale and zero),
+  // 4 B (TQ3_QJL norm and residual norm) or 8 B (Q8G32 scales)
+  l.kmeta_bytes = c.k_format == KVQ_TQ3_QJL ? 4 : c.k_format == KVQ_Q8G32 ? 8 : 16;
+  l.off_vmain = (c.k_format == KVQ_Q8G32 ? 128 : 64) * HALF;
+  l.off_kmeta = l.off_vmain + 64 * HALF;
   l.off_vmeta = l.off_kmeta + l.kmeta_bytes * HALF;
   l.half_bytes = l.off_vmeta + 16 * HALF;
   l.page_bytes = 2 * l.half_bytes;

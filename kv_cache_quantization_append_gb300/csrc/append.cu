@@ -73,6 +73,30 @@ __device__ __forceinline__ void q4_encode(const float (&y)[4], int lane, int kv,
   }
 }
 
+// Q8G32 key: per group of 32 channels (lanes 8G .. 8G+7) d = fp16(max |y| / 127) and codes
+// clamp(rint(y / d), -127, 127) with round-half-even (IEEE division by the stored scale), 0 when
+// d == 0; stored as u = c + 128.  Record of token t (128 B): chunk m = 2i + h at 16 (m ^ (t & 1)),
+// word w of the chunk = channels k + 2i, k + 2i + 1, k + 2i + 8, k + 2i + 9 with k = 16 (4h + w).
+__device__ __forceinline__ void q8_encode_key(const float (&y)[4], int lane, int tin, uint8_t* kmain,
+                                              uint8_t* kmeta) {
+  float amax = fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3])));
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, m));
+  const __half d16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+  const float d = __half2float(d16);
+  uint8_t* rec = kmain + (size_t)tin * 128;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    int c = 0;
+    if (d > 0.0f) c = min(max(__float2int_rn(__fdiv_rn(y[e], d)), -127), 127);
+    const int ch = 4 * lane + e, kk = ch >> 4, within = ch & 15;
+    const int i = (within & 7) >> 1, byte = (within & 1) + ((within >> 3) << 1);
+    const int m = 2 * i + (kk >> 2), w = kk & 3;
+    rec[16 * (m ^ (tin & 1)) + 4 * w + byte] = (uint8_t)(c + 128);
+  }
+  if ((lane & 7) == 0) reinterpret_cast<__half*>(kmeta + (size_t)tin * 8)[lane >> 3] = d16;
+}
+
 constexpr int VPW = 4;  // vectors (consecutive tokens) per warp: their loads are issued together
 
 // encode one vector (lane holds channels 4*lane..+3 of the raw input) into its page and ring slot
@@ -154,11 +178,15 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, int lane, int
     return;
   }
 
-  // ---- Q4G32 (optionally Sinkhorn-balanced: y / sigma per channel)
+  // ---- Q4G32 or Q8G32 (optionally Sinkhorn-balanced: y / sigma per channel)
   if (a.sinkhorn) {
     const __half* sig = (kv ? a.p.sigv : a.p.sigk) + ((size_t)layer * H + h) * D + 4 * lane;
 #pragma unroll
     for (int e = 0; e < 4; ++e) y[e] = __fdiv_rn(y[e], __half2float(sig[e]));
+  }
+  if (kv == 0 && a.k_format == KVQ_Q8G32) {
+    q8_encode_key(y, lane, tin, pg, pg + a.L.off_kmeta);
+    return;
   }
   __half s16, z16;
   q4_encode(y, lane, kv, tin, pg + (kv ? a.L.off_vmain : 0), s16, z16);

@@ -1,4 +1,5 @@
-// Bulk append kernel for Q4G32 vectors: four lanes per new token, eight tokens per warp.
+// Bulk append kernel for Q4G32 vectors and Q8G32 keys: four lanes per new token, eight tokens per
+// warp.
 //
 // Same codec as the per-vector append kernel ([QC] "how it works": 4-bit groups, FP32 window;
 // [KV] TLDR: Walsh-Hadamard rotation, then Sinkhorn balancing, then 4-bit), same operations in
@@ -32,6 +33,7 @@ constexpr int BW = 8;     // warps per CTA
 constexpr int TPW = 8;    // tokens per warp
 constexpr float RINT_MAGIC = 12582912.0f;                 // 1.5 * 2^23
 constexpr float FAST_Q_LIMIT = 0.5f - 7.62939453125e-6f;  // 0.5 - 2^-17
+constexpr float FAST_Q8_LIMIT = 0.5f - 3.0517578125e-5f;  // 0.5 - 2^-15
 
 __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_constant__ AppendArgs a) {
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
@@ -150,6 +152,80 @@ __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_co
       x[2 * j] = __fdiv_rn(x[2 * j], s.x);
       x[2 * j + 1] = __fdiv_rn(x[2 * j + 1], s.y);
     }
+  }
+
+  if (kv == 0 && a.k_format == KVQ_Q8G32) {
+    // ---- Q8G32 key for the lane's group: d = fp16(max |y| / 127), codes clamp(rint(y / d), -127,
+    // 127) against the stored d (0 when d == 0), stored as u = c + 128.  The quotient is formed as
+    // y * RN(1/d), within 1.9e-5 of the IEEE quotient for |y / d| <= 127.5; where it lies within
+    // 2^-15 of a half-integer the lane redoes its group with the IEEE division.
+    float am[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) am[e] = fabsf(x[e]);
+#pragma unroll
+    for (int e = 4; e < 32; ++e) am[e & 3] = fmaxf(am[e & 3], fabsf(x[e]));
+    const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+    const __half d16 = __float2half_rn(__fdiv_rn(amax, 127.0f));
+    const float d = __half2float(d16);
+    uint32_t u8[8];  // byte-packed codes: u8[j] holds local channels 4j .. 4j+3
+    if (d > 0.0f) {
+      const float inv = __frcp_rn(d);
+      float dmax8 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          float q0 = x[4 * j + e], q1 = x[4 * j + e + 1];
+          mul2(q0, q1, inv, inv);
+          float t0 = q0, t1 = q1;
+          add2(t0, t1, RINT_MAGIC, RINT_MAGIC);
+          float r0 = t0, r1 = t1;
+          sub2(r0, r1, RINT_MAGIC, RINT_MAGIC);
+          float d0 = q0, d1 = q1;
+          sub2(d0, d1, r0, r1);
+          dmax8 = fmaxf(dmax8, fmaxf(fabsf(d0), fabsf(d1)));
+          const int c0 = min(max((int)(__float_as_uint(t0) - __float_as_uint(RINT_MAGIC)), -127), 127);
+          const int c1 = min(max((int)(__float_as_uint(t1) - __float_as_uint(RINT_MAGIC)), -127), 127);
+          word |= ((uint32_t)(c0 + 128) << (8 * e)) | ((uint32_t)(c1 + 128) << (8 * e + 8));
+        }
+        u8[j] = word;
+      }
+      if (dmax8 > FAST_Q8_LIMIT && valid) {
+        // rare: the group's codes from the IEEE quotient
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t word = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = min(max(__float2int_rn(__fdiv_rn(x[4 * j + e], d)), -127), 127);
+            word |= (uint32_t)(c + 128) << (8 * e);
+          }
+          u8[j] = word;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) u8[j] = 0x80808080u;
+    }
+    if (valid) {
+      // k-step kk = 2G + s (s = 0, 1) covers local channels 16 s .. 16 s + 15; word (i, kk) = local
+      // channels 16 s + 2i, +1, +8, +9: bytes of u8[4 s + (i >> 1)] and u8[4 s + 2 + (i >> 1)]
+      uint8_t* rec = pg + (size_t)tin * 128;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t wd[2];
+#pragma unroll
+        for (int sdx = 0; sdx < 2; ++sdx) {
+          const uint32_t lo = u8[4 * sdx + (i >> 1)], hi = u8[4 * sdx + 2 + (i >> 1)];
+          wd[sdx] = __byte_perm(lo, hi, (i & 1) ? 0x7632u : 0x5410u);
+        }
+        const int m = 2 * i + (G >> 1);
+        *reinterpret_cast<uint2*>(rec + 16 * (m ^ (tin & 1)) + 8 * (G & 1)) = make_uint2(wd[0], wd[1]);
+      }
+      reinterpret_cast<__half*>(pg + a.L.off_kmeta + (size_t)tin * 8)[G] = d16;
+    }
+    return;
   }
 
   // ---- Q4G32 for the lane's group: exact min/max, fp16 scale (max-min)/15 and zero min, codes

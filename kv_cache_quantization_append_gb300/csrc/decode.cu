@@ -44,27 +44,34 @@ constexpr long long WIDE_MERGE_RECORDS = 48;  // above this many records per uni
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
-// latency; measured faster than 11 warps with 3 stages at 168 registers); TQ3 keys, whose fragments
-// need more registers: 11 consumer warps.  Build flags KVQ_Q4_CONSUMER_WARPS, KVQ_Q4_SLOTS and
-// KVQ_TQ_CONSUMER_WARPS override the counts.
+// latency; measured faster than 11 warps with 3 stages at 168 registers); TQ3 and Q8 keys, whose
+// fragments need more registers: 11 consumer warps (12 warps in all: three per SM sub-partition, so
+// 168 registers a thread; 13-16 warps leave 128 and spill, measured slower for both).  Build flags
+// KVQ_Q4_CONSUMER_WARPS, KVQ_Q4_SLOTS, KVQ_TQ_CONSUMER_WARPS and KVQ_Q8_CONSUMER_WARPS override the
+// counts.
 template <int KF>
 struct Geo {
   static constexpr bool TQ = KF == KVQ_TQ3_QJL;
+  static constexpr bool Q8 = KF == KVQ_Q8G32;
 #ifndef KVQ_TQ_CONSUMER_WARPS
 #define KVQ_TQ_CONSUMER_WARPS 11
 #endif
 #ifndef KVQ_Q4_CONSUMER_WARPS
 #define KVQ_Q4_CONSUMER_WARPS 15
 #endif
-  static constexpr int NCW = TQ ? KVQ_TQ_CONSUMER_WARPS : KVQ_Q4_CONSUMER_WARPS;  // consumer warps
+#ifndef KVQ_Q8_CONSUMER_WARPS
+#define KVQ_Q8_CONSUMER_WARPS 11
+#endif
+  static constexpr int NCW = TQ ? KVQ_TQ_CONSUMER_WARPS : Q8 ? KVQ_Q8_CONSUMER_WARPS : KVQ_Q4_CONSUMER_WARPS;
   static constexpr int NTHREADS = (NCW + 1) * 32;      // + 1 producer warp
 #ifndef KVQ_Q4_SLOTS
 #define KVQ_Q4_SLOTS 2
 #endif
-  static constexpr int NSLOT = TQ ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
+  static constexpr int NSLOT = (TQ || Q8) ? 2 : KVQ_Q4_SLOTS;   // stages owned by each consumer warp
   static constexpr int NSTAGE = NSLOT * NCW;
-  // a stage holds one half-page (Q4/Q4 5120 B, TQ3/Q4 4736 B) or one window chunk (4096 B)
-  static constexpr int STAGE = TQ ? 4736 : 5120;
+  // a stage holds one half-page (Q4/Q4 5120 B, TQ3/Q4 4736 B, Q8/Q4 6912 B) or one window chunk
+  // (4096 B)
+  static constexpr int STAGE = TQ ? 4736 : Q8 ? 6912 : 5120;
   // TQ3 record-byte table: entry v (256 of them) at 256 v: lane j's copy of the centroid pair at
   // +4 j, of the sign pair at +128 + 4 j
   static constexpr int LUT_BYTES = TQ ? 256 * 256 : 0;
@@ -438,6 +445,12 @@ struct Kernel {
         d1 = d0 + 1;
         d2 = d0 + 2;
         d3 = d0 + 3;
+      } else if (KF == KVQ_Q8G32) {
+        // Q8: k-step kk holds channels 16kk + {2i, 2i+1 | 2i+8, 2i+9}
+        d0 = 16 * kk + 2 * i;
+        d1 = d0 + 1;
+        d2 = d0 + 8;
+        d3 = d0 + 9;
       } else {
         // Q4: k-step (G, e) = (kk >> 1, kk & 1) holds channels 32G + 8i + 4e + {0,2 | 1,3}; the codes
         // arrive scaled by 2^-9, so q~ is scaled by 2^9 (exact)
@@ -447,7 +460,7 @@ struct Kernel {
         d2 = d0 + 1;
         d3 = d0 + 3;
       }
-      const float us = (KF == KVQ_TQ3_QJL) ? 1.f : CODE_UNSCALE;
+      const float us = (KF == KVQ_Q4G32) ? CODE_UNSCALE : 1.f;
       const uint32_t v0 = hv ? split_pick(qh[d0] * us, lo) : 0u, v1 = hv ? split_pick(qh[d1] * us, lo) : 0u;
       const uint32_t v2 = hv ? split_pick(qh[d2] * us, lo) : 0u, v3 = hv ? split_pick(qh[d3] * us, lo) : 0u;
       st.qb[kk][0] = v0 | (v1 << 16);
@@ -587,9 +600,9 @@ struct Kernel {
   // ---------------------------------------------------------------- quantised half-page
   // regions of a 32-token half-page (bytes): K main at 0, V main at 64*HALF, K meta at 128*HALF,
   // V meta after K meta
-  static constexpr int OFF_VMAIN = 64 * HALF;
-  static constexpr int OFF_KMETA = 128 * HALF;
-  static constexpr int OFF_VMETA = OFF_KMETA + (KF == KVQ_TQ3_QJL ? 4 : 16) * HALF;
+  static constexpr int OFF_VMAIN = (KF == KVQ_Q8G32 ? 128 : 64) * HALF;
+  static constexpr int OFF_KMETA = OFF_VMAIN + 64 * HALF;
+  static constexpr int OFF_VMETA = OFF_KMETA + (KF == KVQ_TQ3_QJL ? 4 : KF == KVQ_Q8G32 ? 8 : 16) * HALF;
 
   // logits of tokens ta = 16mt + r and tb = ta + 8 for head i (this thread's column pair)
   __device__ __forceinline__ void tile_logits(const uint8_t* stage, int mt, const QuantState& st, float& la,
@@ -598,7 +611,46 @@ struct Kernel {
     const int ta = 16 * mt + r, tb = ta + 8;
     const uint8_t* kmain = stage;
     const uint8_t* kmeta = stage + OFF_KMETA;
-    if (KF == KVQ_TQ3_QJL) {
+    if (KF == KVQ_Q8G32) {
+      // Q8 keys: a token's 16-byte chunks 2i (k-steps 0-3) and 2i + 1 (4-7), swizzled by the token's
+      // parity (ta and tb have the parity of r); word kk & 3 of a chunk holds the stored bytes
+      // u = c + 128 of this lane's A operands, and a byte permute with 0x64 high bytes makes each
+      // pair the exact fp16 values 1024 + u = 1152 + c.  Per group G: acc_G = q~_G . (1152 + c);
+      // the offset leaves through the zero-point mma: logit = sum_G d_G acc_G - 1152 sum_G d_G qsum_G.
+      const int sw = r & 1;
+      const uint4 a0 = *reinterpret_cast<const uint4*>(kmain + ta * 128 + 16 * ((2 * i) ^ sw));
+      const uint4 a1 = *reinterpret_cast<const uint4*>(kmain + ta * 128 + 16 * ((2 * i + 1) ^ sw));
+      const uint4 b0 = *reinterpret_cast<const uint4*>(kmain + tb * 128 + 16 * ((2 * i) ^ sw));
+      const uint4 b1 = *reinterpret_cast<const uint4*>(kmain + tb * 128 + 16 * ((2 * i + 1) ^ sw));
+      constexpr uint32_t HI = 0x64646464u;
+      float acc[4][4];
+#pragma unroll
+      for (int G = 0; G < 4; ++G) {
+        acc[G][0] = acc[G][1] = acc[G][2] = acc[G][3] = 0.f;
+#pragma unroll
+        for (int sdx = 0; sdx < 2; ++sdx) {
+          const int kk = 2 * G + sdx, w = kk & 3;
+          const uint4 ca = kk < 4 ? a0 : a1, cb = kk < 4 ? b0 : b1;
+          const uint32_t wa = w == 0 ? ca.x : w == 1 ? ca.y : w == 2 ? ca.z : ca.w;
+          const uint32_t wb = w == 0 ? cb.x : w == 1 ? cb.y : w == 2 ? cb.z : cb.w;
+          mma16816(acc[G], __byte_perm(wa, HI, 0x4140u), __byte_perm(wb, HI, 0x4140u), __byte_perm(wa, HI, 0x4342u),
+                   __byte_perm(wb, HI, 0x4342u), st.qb[kk][0], st.qb[kk][1]);
+        }
+      }
+      const uint2 ma = *reinterpret_cast<const uint2*>(kmeta + ta * 8);
+      const uint2 mb = *reinterpret_cast<const uint2*>(kmeta + tb * 8);
+      // sum_G d_G qsum_G: A row = token, k = group (lanes i = 0, 1 hold groups (0, 1), (2, 3); lanes
+      // i = 2, 3 meet a zero B fragment)
+      float zacc[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16816(zacc, (i & 1) ? ma.y : ma.x, (i & 1) ? mb.y : mb.x, 0u, 0u, st.zb, 0u);
+      const float2 da01 = __half22float2(u2h(ma.x)), da23 = __half22float2(u2h(ma.y));
+      const float2 db01 = __half22float2(u2h(mb.x)), db23 = __half22float2(u2h(mb.y));
+      constexpr float OFFSET = 1152.0f;
+      la = da01.x * (acc[0][0] + acc[0][1]) + da01.y * (acc[1][0] + acc[1][1]) + da23.x * (acc[2][0] + acc[2][1]) +
+           da23.y * (acc[3][0] + acc[3][1]) - OFFSET * (zacc[0] + zacc[1]);
+      lb = db01.x * (acc[0][2] + acc[0][3]) + db01.y * (acc[1][2] + acc[1][3]) + db23.x * (acc[2][2] + acc[2][3]) +
+           db23.y * (acc[3][2] + acc[3][3]) - OFFSET * (zacc[2] + zacc[3]);
+    } else if (KF == KVQ_TQ3_QJL) {
       // record byte 16i + 2kk + e of a token = its A operands of k-step kk, slot e (k = 2i, 2i+1 for
       // e = 0, 2i + 8, 2i + 9 for e = 1): two 3-bit codes and two QJL sign bits.  One byte_perm
       // puts the byte above this lane's table offset; the entry's centroid pair and +-1 sign pair
@@ -708,6 +760,9 @@ struct Kernel {
       __half* nrm = reinterpret_cast<__half*>(stage + OFF_KMETA);
       for (int idx = lane; idx < 2 * HALF; idx += 32)
         if ((idx % HALF) >= ntok) nrm[idx] = __float2half_rn(0.f);
+    } else if (KF == KVQ_Q8G32) {
+      for (int t = ntok + lane; t < HALF; t += 32)
+        *reinterpret_cast<uint2*>(stage + OFF_KMETA + t * 8) = make_uint2(0u, 0u);
     } else {
       for (int t = ntok + lane; t < HALF; t += 32)
         *reinterpret_cast<uint4*>(stage + OFF_KMETA + t * 16) = make_uint4(0u, 0u, 0u, 0u);
@@ -1449,7 +1504,9 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
 }  // namespace
 
 int decode_consumer_warps(int k_format) {
-  return k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW : Geo<KVQ_Q4G32>::NCW;
+  return k_format == KVQ_TQ3_QJL ? Geo<KVQ_TQ3_QJL>::NCW
+         : k_format == KVQ_Q8G32 ? Geo<KVQ_Q8G32>::NCW
+                                 : Geo<KVQ_Q4G32>::NCW;
 }
 
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format) {
@@ -1515,7 +1572,9 @@ static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  return a.k_format == KVQ_TQ3_QJL ? launch_kf<KVQ_TQ3_QJL>(a, s) : launch_kf<KVQ_Q4G32>(a, s);
+  return a.k_format == KVQ_TQ3_QJL ? launch_kf<KVQ_TQ3_QJL>(a, s)
+         : a.k_format == KVQ_Q8G32 ? launch_kf<KVQ_Q8G32>(a, s)
+                                   : launch_kf<KVQ_Q4G32>(a, s);
 }
 
 }  // namespace kvq

@@ -18,6 +18,9 @@ LIB_PATH = os.path.join(HERE, "_lib", "libkvq.so")
 
 KVQ_Q4G32 = 1
 KVQ_TQ3_QJL = 3
+KVQ_Q8G32 = 4
+# the key formats by the names the workloads and the oracle use
+K_FORMATS = {"q4g32": KVQ_Q4G32, "tq3_qjl": KVQ_TQ3_QJL, "q8g32": KVQ_Q8G32}
 KVQ_IN_F32 = 0
 KVQ_IN_BF16 = 1
 

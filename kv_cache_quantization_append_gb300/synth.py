@@ -15,6 +15,8 @@ Workloads (names are the shapes they stand in for; no dataset or weights are use
                         tokens, Q4G32, window 128.
   llama3.1-8b-tq-b8-32k: 32 layers, 32/8 heads, B=8 x 32768, bf16 N(0,1) with 4 channels x12,
                         K = TQ3 + QJL, V = Q4G32, window 128.
+  llama3.2-3b-32k-k8v4: the llama3.2-3b-32k shape and inputs (same seeds) with keys at 8 bits
+                        (Q8G32) and values at 4 bits (Q4G32): the asymmetric K/V split.
   dense27b-ragged-b32 : 62 layers (one allocated and timed), 32/16 heads, B=32 with lengths
                         uniform in [1024, 65536] (numpy default_rng(7)), 64-token pages, bf16
                         N(0,1) with 1% of channels (1 of 128) x10 in K and V, Q4G32, window 128;
@@ -46,6 +48,11 @@ WORKLOADS = {
                                   ctx=32768, window=128, k_format="tq3_qjl", v_format="q4g32",
                                   sinkhorn=False, in_dtype="bf16", wht_seed=0, qjl_seed=4242,
                                   outlier_count=4, outlier_scale=12.0, outliers_in_v=True),
+    # same index as llama3.2-3b-32k: the same seeded K, V and q, only the key format differs
+    "llama3.2-3b-32k-k8v4": dict(index=2, n_layers=28, batch=1, n_q_heads=24, n_kv_heads=8, ctx=32768,
+                                 window=128, k_format="q8g32", v_format="q4g32", sinkhorn=False,
+                                 in_dtype="bf16", wht_seed=0, outlier_frac=0.02, outlier_scale=8.0,
+                                 outliers_in_v=True),
     "dense27b-ragged-b32": dict(index=5, n_layers=62, alloc_layers=1, batch=32, n_q_heads=32,
                                 n_kv_heads=16, ctx_range=(1024, 65536), len_seed=7, window=128,
                                 page_tokens=64, k_format="q4g32", v_format="q4g32", sinkhorn=False,

@@ -10,8 +10,8 @@ from oracle import attention
 
 from . import layout
 
-FMT = {"q4g32": lib.KVQ_Q4G32, "tq3_qjl": lib.KVQ_TQ3_QJL}
-OFMT = {"q4g32": attention.Q4G32, "tq3_qjl": attention.TQ3_QJL}
+FMT = dict(lib.K_FORMATS)
+OFMT = {"q4g32": attention.Q4G32, "tq3_qjl": attention.TQ3_QJL, "q8g32": attention.Q8G32}
 
 
 def make_pair(n_layers, n_kv, n_q, max_batch, max_seq_len, window=128, k_format="q4g32",
@@ -40,6 +40,8 @@ def compare_codes(gpu: QuantKVCache, ora: attention.OracleCache, layer: int, b: 
     got = layout.read_unit(gpu.buffer, gpu.cfg, layer, b, h, n, block_table)
     if ora.cfg.k_format == attention.TQ3_QJL:
         want = {"k_code": ora.k["code"], "k_bits": ora.k["bits"], "k_norm": ora.k["norm"], "k_gamma": ora.k["gamma"]}
+    elif ora.cfg.k_format == attention.Q8G32:
+        want = {"k_code": ora.k["code"], "k_scale": ora.k["scale"]}
     else:
         want = {"k_code": ora.k["code"], "k_scale": ora.k["scale"], "k_zero": ora.k["zero"]}
     want.update({"v_code": ora.v["code"], "v_scale": ora.v["scale"], "v_zero": ora.v["zero"]})

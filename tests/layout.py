@@ -19,9 +19,9 @@ def _a256(x: int) -> int:
 
 
 def regions(cfg, total: int) -> dict:
-    tq = cfg.k_format == 3
-    kmeta = 4 if tq else 16
-    half_bytes = 128 * H + kmeta * H + 16 * H          # K main | V main | K meta | V meta (32 tokens)
+    kmain = {1: 64, 3: 64, 4: 128}[cfg.k_format]        # K main bytes per token: Q4G32, TQ3_QJL, Q8G32
+    kmeta = {1: 16, 3: 4, 4: 8}[cfg.k_format]
+    half_bytes = (kmain + 64) * H + kmeta * H + 16 * H  # K main | V main | K meta | V meta (32 tokens)
     page_bytes = 2 * half_bytes
     maxpps = -(-cfg.max_seq_len // P)
     n_pages = cfg.n_pages or cfg.max_batch * maxpps
@@ -37,7 +37,7 @@ def regions(cfg, total: int) -> dict:
     off_sigk = off_sigv - sig
     return dict(page_bytes=page_bytes, half_bytes=half_bytes, n_pages=n_pages, maxpps=maxpps,
                 off_pages=off_pages, off_ringk=off_ringk, off_ringv=off_ringv, off_sigk=off_sigk,
-                off_sigv=off_sigv, kmeta=kmeta, off_bt=off_bt)
+                off_sigv=off_sigv, kmain=kmain, kmeta=kmeta, off_bt=off_bt)
 
 
 def _gather(buf: torch.Tensor, starts: np.ndarray, n: int) -> np.ndarray:
@@ -73,6 +73,21 @@ def _q4v_codes(half_v: np.ndarray, t: np.ndarray) -> np.ndarray:
     return out
 
 
+def _q8k_codes(rec: np.ndarray, t: np.ndarray) -> np.ndarray:
+    """Q8G32 K record [T][128] of tokens with index t in their half-page: 16-byte chunk m = 2i + h at
+    16 (m ^ (t & 1)); byte b of its word w = channel 16 (4h + w) + 2i + (b & 1) + 8 (b >> 1); stored
+    bytes u = c + 128."""
+    out = np.zeros((len(t), 128), np.int8)
+    for m in range(8):
+        i, h = m >> 1, m & 1
+        pos = 16 * (m ^ (t & 1))
+        for w in range(4):
+            for b in range(4):
+                ch = 16 * (4 * h + w) + 2 * i + (b & 1) + 8 * (b >> 1)
+                out[:, ch] = (rec[np.arange(len(t)), pos + 4 * w + b].astype(np.int16) - 128).astype(np.int8)
+    return out
+
+
 def _tq3_fields(rec: np.ndarray):
     """TQ3 key record [T][64]: byte j holds the 3-bit codes of channels 2j (bits 0-2) and 2j + 1
     (bits 3-5) and the QJL sign bits of projections 2j (bit 6) and 2j + 1 (bit 7)."""
@@ -93,17 +108,21 @@ def read_unit(buf: torch.Tensor, cfg, layer: int, b: int, h: int, n_tokens: int,
             ((pos % P) // H) * R["half_bytes"])           # the half-page holding each position
     t = pos % H
     out = {}
-    kmeta0 = base + 128 * H
+    vmain0 = base + R["kmain"] * H
+    kmeta0 = vmain0 + 64 * H
     vmeta0 = kmeta0 + R["kmeta"] * H
     if cfg.k_format == 3:
         out["k_code"], out["k_bits"] = _tq3_fields(_gather(buf, base + t * 64, 64))
         out["k_norm"] = _gather(buf, kmeta0 + t * 2, 2).view(np.float16)[:, 0]
         out["k_gamma"] = _gather(buf, kmeta0 + 2 * H + t * 2, 2).view(np.float16)[:, 0]
+    elif cfg.k_format == 4:
+        out["k_code"] = _q8k_codes(_gather(buf, base + t * 128, 128), t)
+        out["k_scale"] = _gather(buf, kmeta0 + t * 8, 8).view(np.float16)
     else:
         out["k_code"] = _q4k_codes(_gather(buf, base + t * 64, 64))
         m = _gather(buf, kmeta0 + t * 16, 16).view(np.float16)
         out["k_scale"], out["k_zero"] = m[:, :4], m[:, 4:]
-    out["v_code"] = _q4v_codes(_gather(buf, base + 64 * H, 64 * H), t)
+    out["v_code"] = _q4v_codes(_gather(buf, vmain0, 64 * H), t)
     sc = np.stack([_gather(buf, vmeta0 + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
     zr = np.stack([_gather(buf, vmeta0 + 8 * H + (G * H + t) * 2, 2).view(np.float16)[:, 0] for G in range(4)], 1)
     out["v_scale"], out["v_zero"] = sc, zr

@@ -25,6 +25,7 @@ SAMPLES = {
     "qwen3-4b-kvarn-128k": [(35, 0, 5), (0, 0, 0)],
     "llama3.1-8b-tq-b8-32k": [(31, 7, 7), (4, 3, 2)],
     "dense27b-ragged-b32": [(0, 0, 0), (0, 17, 9), (0, 31, 15)],
+    "llama3.2-3b-32k-k8v4": [(0, 0, 0), (27, 0, 7)],
 }
 
 
@@ -78,7 +79,8 @@ def test_full_size_sampled_units(gpu_lib, name):
         del k, v
         ora.append(0, harness.to_np(ku), harness.to_np(vu), np.array([0]))
         got = layout.read_unit(cache.buffer, cache.cfg, layer, b, h, L, bt)
-        names = ("code", "bits", "norm", "gamma") if w["k_format"] == "tq3_qjl" else ("code", "scale", "zero")
+        names = {"tq3_qjl": ("code", "bits", "norm", "gamma"), "q8g32": ("code", "scale")}.get(
+            w["k_format"], ("code", "scale", "zero"))
         for n in names:
             wv, gv = ora.k[n][0, 0, 0, :L], got["k_" + n]
             assert np.array_equal(wv.view(np.uint8), gv.view(np.uint8)), f"{name} {layer},{b},{h} k_{n}"

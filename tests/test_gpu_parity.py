@@ -199,6 +199,52 @@ def test_turboquant_keys(gpu_lib):
         harness.assert_attention_close(got, want)
 
 
+@pytest.mark.parametrize("sinkhorn", [False, True])
+def test_8bit_keys(gpu_lib, sinkhorn):
+    """[TQ] "when to use what": K kept at 8 bits, V at 4 bits (GQA 3, B = 2, different lengths), plain
+    and Sinkhorn-balanced: codes and scales bit-exact, attention within 2e-3."""
+    w = synth.WORKLOADS["qwen3-4b-kvarn-128k" if sinkhorn else "llama3.2-3b-32k-k8v4"]
+    Lyr, H, Hq, B, L = 2, 2, 6, 2, 900
+    gpu, ora, _ = harness.make_pair(Lyr, H, Hq, B, 1024, window=128, k_format="q8g32", sinkhorn=sinkhorn)
+    for l in range(Lyr):
+        k, v = _inputs(w, l, B, H, Hq, L)
+        if sinkhorn:
+            kc, vc = k[0, :, :512].contiguous(), v[0, :, :512].contiguous()
+            gpu.calibrate(l, kc, vc)
+            ora.calibrate(l, harness.to_np(kc), harness.to_np(vc))
+        gpu.append(l, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+        ora.append(l, harness.to_np(k), harness.to_np(v), np.zeros(B, np.int64))
+    torch.cuda.synchronize()
+    for l in range(Lyr):
+        for b in range(B):
+            for h in range(H):
+                harness.compare_codes(gpu, ora, l, b, h, L)
+        q = synth.queries(w, l, B, Hq, device="cuda")
+        got, want = _decode_both(gpu, ora, l, q, np.array([L, L - 321]))
+        harness.assert_attention_close(got, want)
+
+
+@pytest.mark.parametrize("window", [128, 0])
+def test_8bit_keys_ragged_edge_lengths(gpu_lib, window):
+    """Q8 keys at the edge lengths of the step list (half-page tails, window boundaries, empty)."""
+    lens = np.array([0, 1, 31, 32, 33, 127, 128, 129, 160, 191, 192, 700], dtype=np.int32)
+    B = len(lens)
+    w = synth.WORKLOADS["llama3.2-3b-32k-k8v4"]
+    gpu, ora, _ = harness.make_pair(1, 2, 4, B, 768, window=window, k_format="q8g32")
+    T = int(lens.max())
+    k, v = _inputs(w, 0, B, 2, 4, T)
+    gpu.append(0, k, v, torch.zeros(B, dtype=torch.int32, device="cuda"))
+    ora.append(0, harness.to_np(k), harness.to_np(v), np.zeros(B, np.int64))
+    torch.cuda.synchronize()
+    q = synth.queries(w, 0, B, 4, device="cuda")
+    got, want = _decode_both(gpu, ora, 0, q, lens)
+    for b in range(B):
+        if lens[b] == 0:
+            assert not got[b].any()
+        else:
+            harness.assert_attention_close(got[b], want[b])
+
+
 def test_paged_ragged_batch(gpu_lib):
     """dense-27B-shaped (GQA 2) paged cache: shuffled block table, chunked ragged prefill."""
     w = synth.WORKLOADS["dense27b-ragged-b32"]
@@ -254,12 +300,13 @@ def test_out_of_range_append_is_flagged_and_skipped(gpu_lib):
     assert gpu.status() == 0                        # read-and-clear
 
 
-@pytest.mark.parametrize("variant", ["bf16", "f32", "sinkhorn", "tq3_keys", "paged"])
+@pytest.mark.parametrize("variant", ["bf16", "f32", "sinkhorn", "tq3_keys", "paged", "q8_keys", "q8_sinkhorn"])
 def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
     """Appends of 1..257 tokens starting at odd, even, half-page and page offsets, with sequences
     skipped (pos = -1) in some calls: every stored field of every written position and the window
     ring bit-exact with the oracle (covers both append kernels and the split between them)."""
-    w = synth.WORKLOADS["qwen3-4b-kvarn-128k" if variant == "sinkhorn" else "llama3.2-3b-32k"]
+    balanced = variant in ("sinkhorn", "q8_sinkhorn")
+    w = synth.WORKLOADS["qwen3-4b-kvarn-128k" if balanced else "llama3.2-3b-32k"]
     B, H, Hq, cap, W = 4, 2, 4, 1024, 64
     starts = np.array([0, 1, 31, 63], np.int32)
     chunks = [16, 1, 17, 31, 5, 32, 33, 100, 15, 257]
@@ -270,10 +317,11 @@ def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
         perm = np.random.default_rng(5).permutation(n_pages)
         bt = perm[:B * maxpps].reshape(B, maxpps).astype(np.int32)
     gpu, ora, _ = harness.make_pair(1, H, Hq, B, cap, window=W, in_dtype="f32" if variant == "f32" else "bf16",
-                                    sinkhorn=variant == "sinkhorn",
-                                    k_format="tq3_qjl" if variant == "tq3_keys" else "q4g32",
+                                    sinkhorn=balanced,
+                                    k_format={"tq3_keys": "tq3_qjl", "q8_keys": "q8g32",
+                                              "q8_sinkhorn": "q8g32"}.get(variant, "q4g32"),
                                     n_pages=n_pages, block_table=bt)
-    if variant == "sinkhorn":
+    if balanced:
         kc, vc = _inputs(w, 0, 1, H, Hq, 256, t0=4096)
         gpu.calibrate(0, kc[0].contiguous(), vc[0].contiguous())
         ora.calibrate(0, harness.to_np(kc[0]), harness.to_np(vc[0]))
@@ -293,8 +341,10 @@ def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
         last_T[live] = T
     torch.cuda.synchronize()
     assert gpu.status() == 0
-    names = (("k_code", "code"), ("k_bits", "bits"), ("k_norm", "norm"), ("k_gamma", "gamma")) \
-        if variant == "tq3_keys" else (("k_code", "code"), ("k_scale", "scale"), ("k_zero", "zero"))
+    names = {"tq3_keys": (("k_code", "code"), ("k_bits", "bits"), ("k_norm", "norm"), ("k_gamma", "gamma")),
+             "q8_keys": (("k_code", "code"), ("k_scale", "scale")),
+             "q8_sinkhorn": (("k_code", "code"), ("k_scale", "scale"))}.get(
+        variant, (("k_code", "code"), ("k_scale", "scale"), ("k_zero", "zero")))
     for b in range(B):
         s0, s1 = int(starts[b]), int(pos[b])
         for h in range(H):

@@ -42,7 +42,7 @@ def test_strerror(kvq):
 def _cfg(w, layers=None):
     return lib.make_config(layers or w.get("alloc_layers", w["n_layers"]), w["n_kv_heads"], w["n_q_heads"],
                            w["batch"], w.get("ctx", w.get("ctx_range", (0, 0))[1]), window=w["window"],
-                           k_format=lib.KVQ_TQ3_QJL if w["k_format"] == "tq3_qjl" else lib.KVQ_Q4G32,
+                           k_format=lib.K_FORMATS[w["k_format"]],
                            sinkhorn=w["sinkhorn"])
 
 
