@@ -259,6 +259,31 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
 int kv_decode_attention_noalloc(kvq_cache* cache, int32_t layer, const void* q, float* out,
                                 const int32_t* seq_lens, int32_t batch, void* stream);
 
+/*
+ * Chunked prefill ([QC] v3.2 batched-prefill note: a batched prefill writes exactly what per-token
+ * steps write; its attention is read the same way): append ``n_tokens`` new K/V vectors to each of
+ * the first ``batch`` sequences at pos[b] .. pos[b] + n_tokens - 1 (exactly as kv_quant_append),
+ * and compute the attention of their queries: query t of sequence b attends to positions
+ * [0, pos[b] + t], the newest ``window`` of them through their raw values and the rest through
+ * their quantised records -- what n_tokens single-token append + decode steps would compute.
+ *   layer      0..n_layers-1, or -1 for all layers (k, v, q, out then carry a leading layer axis)
+ *   k, v       device, cfg.in_dtype, [L?][batch][n_kv_heads][n_tokens][128]
+ *   q          device, cfg.in_dtype, [L?][batch][n_q_heads][n_tokens][128]
+ *   out        device float [L?][batch][n_q_heads][n_tokens][128]; rows of a sequence with
+ *              pos[b] < 0 (not part of the call) or pos[b] + n_tokens > max_seq_len (flagged
+ *              KVQ_DEV_POS_RANGE, nothing appended) are zeros
+ *   pos        device int32 [batch]
+ *   scratch    device, >= kv_prefill_scratch_bytes(cache, layer, batch) bytes, any contents: holds a
+ *              copy of the window ring taken before the chunk's append (its raw values are read by
+ *              the chunk's first queries after the append has overwritten their ring slots)
+ * Three launches on ``stream``: the ring copy, the append, the attention (tensor-core logits and
+ * P.V over tiles of 32 positions, 64 (query, head) rows per block).
+ */
+size_t kv_prefill_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t batch);
+int kv_prefill_attention(kvq_cache* cache, int32_t layer, const void* k, const void* v, const void* q,
+                         float* out, const int32_t* pos, int32_t batch, int32_t n_tokens, void* scratch,
+                         size_t scratch_bytes, void* stream);
+
 /* Read and clear the device status word (synchronises ``stream``); *flags gets KVQ_DEV_* bits. */
 int kv_status(kvq_cache* cache, uint32_t* flags, void* stream);
 

@@ -55,5 +55,19 @@ class QuantKVCache:
         kv_decode_attention(self.handle, layer, q, out, seq_lens, self.scratch(layer, q.shape[-3]), stream)
         return out
 
+    def prefill(self, layer: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor, pos: torch.Tensor,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Append the chunk (k, v at pos) and return its queries' attention [L?][B][Hq][T][128]."""
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        need = lib.kv_prefill_scratch_bytes(self.handle, layer, q.shape[-4])
+        key = ("prefill", layer == -1, q.shape[-4])
+        t = self._scratch.get(key)
+        if t is None or t.numel() < need:
+            t = torch.empty(need, dtype=torch.uint8, device=self.buffer.device)
+            self._scratch[key] = t
+        lib.kv_prefill_attention(self.handle, layer, k, v, q, out, pos, t, stream)
+        return out
+
     def status(self) -> int:
         return kv_status(self.handle)

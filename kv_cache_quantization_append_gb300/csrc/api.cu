@@ -2,6 +2,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -350,6 +351,74 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   a.n_units = n_units;
   a.n_ctas = ctas;
   return cuda_err(launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t kv_prefill_scratch_bytes(const kvq_cache* cache, int32_t layer, int32_t batch) {
+  Layout L;
+  if (check_cache(cache, &L) != KVQ_OK || batch < 1 || batch > cache->cfg.max_batch) return 0;
+  int l0, nl;
+  if (layers_of_call(cache, layer, &l0, &nl) != KVQ_OK) return 0;
+  return std::max<size_t>(256, prefill_scratch_bytes(nl, batch, cache->cfg.n_kv_heads, cache->cfg.window));
+}
+
+int kv_prefill_attention(kvq_cache* cache, int32_t layer, const void* k, const void* v, const void* q,
+                         float* out, const int32_t* pos, int32_t batch, int32_t n_tokens, void* scratch,
+                         size_t scratch_bytes, void* stream) {
+  Layout L;
+  int rc = check_cache(cache, &L);
+  if (rc != KVQ_OK) return rc;
+  if (!k || !v || !q || !out || !pos || !scratch) return KVQ_ERR_INVALID_ARG;
+  if (batch < 1 || batch > cache->cfg.max_batch || n_tokens < 1) return KVQ_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out) || !aligned16(pos) || !aligned16(scratch))
+    return KVQ_ERR_ALIGN;
+  int l0, nl;
+  if ((rc = layers_of_call(cache, layer, &l0, &nl)) != KVQ_OK) return rc;
+  if (scratch_bytes < kv_prefill_scratch_bytes(cache, layer, batch)) return KVQ_ERR_CAPACITY;
+  if ((rc = check_device(cache)) != KVQ_OK) return rc;
+  AppendArgs ap;
+  ap.p = dev_ptrs(*cache, L);
+  ap.L = L;
+  ap.block_table = cache->block_table;
+  ap.k = k;
+  ap.v = v;
+  ap.pos = pos;
+  ap.layer0 = l0;
+  ap.n_layers_call = nl;
+  ap.batch = batch;
+  ap.T = n_tokens;
+  ap.Hkv = cache->cfg.n_kv_heads;
+  ap.W = cache->cfg.window;
+  ap.max_seq_len = cache->cfg.max_seq_len;
+  ap.k_format = cache->cfg.k_format;
+  ap.sinkhorn = cache->cfg.sinkhorn;
+  ap.in_bf16 = cache->cfg.in_dtype == KVQ_IN_BF16;
+  ap.max_batch = cache->cfg.max_batch;
+  PrefillArgs a;
+  a.p = ap.p;
+  a.L = L;
+  a.block_table = cache->block_table;
+  a.k = k;
+  a.v = v;
+  a.q = q;
+  a.out = out;
+  a.pos = pos;
+  const size_t snap = prefill_scratch_bytes(nl, batch, cache->cfg.n_kv_heads, cache->cfg.window) / 2;
+  a.snap_k = static_cast<float*>(scratch);
+  a.snap_v = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + snap);
+  a.layer0 = l0;
+  a.n_layers_call = nl;
+  a.batch = batch;
+  a.max_batch = cache->cfg.max_batch;
+  a.Hkv = cache->cfg.n_kv_heads;
+  a.g = cache->cfg.n_q_heads / cache->cfg.n_kv_heads;
+  a.W = cache->cfg.window;
+  a.T = n_tokens;
+  a.k_format = cache->cfg.k_format;
+  a.sinkhorn = cache->cfg.sinkhorn;
+  a.in_bf16 = ap.in_bf16;
+  a.max_pages_per_seq = cache->max_pages_per_seq;
+  a.max_seq_len = cache->cfg.max_seq_len;
+  return cuda_err(launch_prefill(a, ap, static_cast<cudaStream_t>(stream)));
 }
 
 int kv_status(kvq_cache* cache, uint32_t* flags, void* stream) {

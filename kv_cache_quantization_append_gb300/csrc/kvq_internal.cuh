@@ -106,6 +106,23 @@ size_t decode_record_slots(int n_units, int n_ctas, int k_format);
 int decode_consumer_warps(int k_format);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+struct PrefillArgs {
+  DevPtrs p;
+  Layout L;
+  const int32_t* block_table;
+  const void* k;     // [L?][batch][Hkv][T][128] cfg.in_dtype: the chunk's raw keys
+  const void* v;
+  const void* q;     // [L?][batch][Hq][T][128] cfg.in_dtype
+  float* out;        // [L?][batch][Hq][T][128]
+  const int32_t* pos;
+  float* snap_k;     // [n_layers_call][batch][Hkv][W][128]: the window ring before the chunk's append
+  float* snap_v;
+  int layer0, n_layers_call, batch, max_batch, Hkv, g, W, T, k_format, sinkhorn, in_bf16;
+  int max_pages_per_seq, max_seq_len;
+};
+size_t prefill_scratch_bytes(int n_layers_call, int batch, int Hkv, int W);
+cudaError_t launch_prefill(const PrefillArgs& a, const AppendArgs& app, cudaStream_t s);
+
 // ---------------------------------------------------------------- device helpers
 #ifdef __CUDACC__
 __device__ __forceinline__ float4 load4_in(const void* base, size_t elem_off, int bf16) {

@@ -31,7 +31,8 @@ DEV_TIMEOUT = 8
 
 EXPORTS = ("kv_cache_bytes", "kv_cache_init", "kv_calibrate_scratch_bytes", "kv_calibrate",
            "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention",
-           "kv_decode_attention_noalloc", "kv_status", "kv_strerror")
+           "kv_decode_attention_noalloc", "kv_prefill_scratch_bytes", "kv_prefill_attention",
+           "kv_status", "kv_strerror")
 NOALLOC_SCRATCH_MAX = 32 * 1024 * 1024
 
 
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_decode_scratch_bytes": (SZ, [cachep, I32, I32]),
         "kv_decode_attention": (ctypes.c_int, [cachep, I32, P, P, P, I32, P, SZ, P]),
         "kv_decode_attention_noalloc": (ctypes.c_int, [cachep, I32, P, P, P, I32, P]),
+        "kv_prefill_scratch_bytes": (SZ, [cachep, I32, I32]),
+        "kv_prefill_attention": (ctypes.c_int, [cachep, I32, P, P, P, P, P, I32, I32, P, SZ, P]),
         "kv_status": (ctypes.c_int, [cachep, U32P, P]),
         "kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -233,6 +236,26 @@ def kv_decode_attention_noalloc(cache: kvq_cache, layer: int, q: torch.Tensor, o
     B = _check_decode_shapes(cache, layer, q, out, seq_lens)
     _check(load().kv_decode_attention_noalloc(ctypes.byref(cache), layer, _ptr(q), _ptr(out),
                                               _ptr(seq_lens), B, _stream(stream)))
+
+
+def kv_prefill_scratch_bytes(cache: kvq_cache, layer: int, batch: int) -> int:
+    return int(load().kv_prefill_scratch_bytes(ctypes.byref(cache), layer, batch))
+
+
+def kv_prefill_attention(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch.Tensor, q: torch.Tensor,
+                         out: torch.Tensor, pos: torch.Tensor, scratch: torch.Tensor, stream=None):
+    """Append a chunk and attend its queries.  k, v: [L?][B][Hkv][T][128]; q: [L?][B][Hq][T][128];
+    out: float32 like q; pos: int32 [B]; scratch: device bytes, at least kv_prefill_scratch_bytes."""
+    if pos.dtype != torch.int32 or out.dtype != torch.float32:
+        raise KVQError("pos must be int32 and out float32")
+    _check_in_dtype(cache, k, v, q)
+    B, T = _check_append_shapes(cache, layer, k, v, pos)
+    lead = (_layers_in_call(cache, layer),) if layer == -1 else ()
+    _check_shape("q", q, lead + (B, cache.cfg.n_q_heads, T, 128))
+    _check_shape("out", out, tuple(q.shape))
+    _check(load().kv_prefill_attention(ctypes.byref(cache), layer, _ptr(k), _ptr(v), _ptr(q), _ptr(out),
+                                       _ptr(pos), B, T, _ptr(scratch), scratch.numel() * scratch.element_size(),
+                                       _stream(stream)))
 
 
 def kv_status(cache: kvq_cache, stream=None) -> int:
