@@ -21,9 +21,13 @@ Codec arithmetic is IEEE float32 in a fixed operation order with no fused multip
 numpy ufunc call below rounds once), because the codes it decides must match the GPU bit for bit.
 Attention is evaluated in float64 on the exact dequantized values.
 
+``blocks`` holds the two block codecs next to the cache (the outlier-channel split behind
+TurboQuant's 2.5 / 3.5-bit results, and TBQ3_0 / TBQ4_0-style 256-value blocks), pinned by
+``tests/test_oracle_blocks.py``.
+
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts the pages or mathematics
 fix.  One reading has no outside pin beyond invariants: the Sinkhorn balancing statistic
 (``sinkhorn_sigma``) -- "parity unpinned" beyond the invariants listed in its docstring.
 """
 
-from . import codec, attention  # noqa: F401
+from . import codec, attention, blocks  # noqa: F401

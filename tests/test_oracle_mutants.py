@@ -98,6 +98,26 @@ MUTANTS = [
     ("attention.py", "p = np.where(active, np.asarray(pos) + t, -1)", "p = np.where(active, np.asarray(pos), -1)"),
     ("attention.py", "out[:, :, t] = cache.decode(layer, q[:, :, t], lens)",
                      "out[:, :, t] = cache.decode(layer, q[:, :, 0], lens)"),
+    # block codecs: TBQ blocks and the outlier-channel split
+    ("blocks.py", "x = np.stack((a + b, a - b), axis=-2).reshape(lead + (n,))",
+                  "x = np.stack((a - b, a + b), axis=-2).reshape(lead + (n,))"),
+    ("blocks.py", "return hadamard_n(x * signs) * c_n(x.shape[-1])", "return hadamard_n(x) * c_n(x.shape[-1])"),
+    ("blocks.py", "return (hadamard_n(y) * c_n(y.shape[-1])) * signs", "return hadamard_n(y * signs) * c_n(y.shape[-1])"),
+    ("blocks.py", "s = (b[..., 0] + b[..., 1]) + (b[..., 2] + b[..., 3])",
+                  "s = ((b[..., 0] + b[..., 1]) + b[..., 2]) + b[..., 3]"),
+    ("blocks.py", "s = s[..., :m] + s[..., m:2 * m]", "s = s[..., 0:2 * m:2] + s[..., 1:2 * m:2]"),
+    ("blocks.py", "cent = (c64 / np.sqrt(float(dim))).astype(F16)", "cent = (c64 / np.sqrt(float(dim + 1))).astype(F16)"),
+    ("blocks.py", "return cent, (c32[:-1] + c32[1:]) / F32(2.0)",
+                  "return cent, c32[:-1] + (c32[1:] - c32[:-1]) / F32(3.0)"),
+    ("blocks.py", "code = (u[..., None] >= bnd).sum(axis=-1)", "code = (u[..., None] > bnd).sum(axis=-1)"),
+    ("blocks.py", "u = y * inv[..., None]", "u = y"),
+    ("blocks.py", "return norm.astype(F32)[..., None] * cent.astype(F32)[code]", "return cent.astype(F32)[code]"),
+    ("blocks.py", "bitarr = ((code[..., None] >> np.arange(bits, dtype=np.uint8)) & 1)",
+                  "bitarr = ((code[..., None] >> np.arange(bits - 1, -1, -1, dtype=np.uint8)) & 1)"),
+    ("blocks.py", "order = np.lexsort((np.arange(codec.D), -ms))", "order = np.lexsort((-np.arange(codec.D), -ms))"),
+    ("blocks.py", "cr, nr = mse_encode(rotate_n(x[..., r], s[SPLIT_N:]), hi_bits - 1)",
+                  "cr, nr = mse_encode(rotate_n(x[..., r], s[:SPLIT_N]), hi_bits - 1)"),
+    ("blocks.py", "return np.concatenate([_f16_bytes(no), _f16_bytes(nr),", "return np.concatenate([_f16_bytes(nr), _f16_bytes(no),"),
 ]
 
 # Child interpreter: build the ``oracle`` package from its sources with one replacement applied,
@@ -109,7 +129,7 @@ fn, old, new = sys.argv[1], sys.argv[2], sys.argv[3]
 pkg = types.ModuleType("oracle")
 pkg.__path__ = []
 sys.modules["oracle"] = pkg
-for name in ("codec", "attention"):
+for name in ("codec", "attention", "blocks"):
     path = "oracle/%s.py" % name
     src = open(path).read()
     if name + ".py" == fn and old:
@@ -122,7 +142,7 @@ for name in ("codec", "attention"):
     setattr(pkg, name, mod)
     exec(compile(src, path, "exec"), mod.__dict__)
 sys.exit(pytest.main(["-q", "-x", "-p", "no:cacheprovider", "-W", "ignore::RuntimeWarning",
-                      "tests/test_oracle_pins.py"]))
+                      "tests/test_oracle_pins.py", "tests/test_oracle_blocks.py"]))
 """
 
 
