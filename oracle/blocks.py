@@ -172,10 +172,14 @@ def split_record_bytes(hi_bits: int) -> int:
 
 
 def split_outliers(calib: np.ndarray) -> np.ndarray:
-    """The 64 channels with the largest mean square over a calibration block [T][128] (float64
-    sums; ties to the lower channel index), ascending."""
-    ms = np.mean(np.asarray(calib, np.float64) ** 2, axis=0)
-    order = np.lexsort((np.arange(codec.D), -ms))  # largest first, lower index first among equals
+    """The 64 channels with the largest mean square over a calibration block [T][128], ascending.
+    Each channel's sum of squares is taken in float64, token by token in order (the squares of
+    float32 inputs are exact in float64); ties go to the lower channel index."""
+    x = np.asarray(calib, np.float64)
+    ss = np.zeros(codec.D, np.float64)
+    for t in range(x.shape[0]):
+        ss = ss + x[t] * x[t]
+    order = np.lexsort((np.arange(codec.D), -ss))  # largest first, lower index first among equals
     return np.sort(order[:SPLIT_N]).astype(np.int16)
 
 

@@ -114,7 +114,7 @@ MUTANTS = [
     ("blocks.py", "return norm.astype(F32)[..., None] * cent.astype(F32)[code]", "return cent.astype(F32)[code]"),
     ("blocks.py", "bitarr = ((code[..., None] >> np.arange(bits, dtype=np.uint8)) & 1)",
                   "bitarr = ((code[..., None] >> np.arange(bits - 1, -1, -1, dtype=np.uint8)) & 1)"),
-    ("blocks.py", "order = np.lexsort((np.arange(codec.D), -ms))", "order = np.lexsort((-np.arange(codec.D), -ms))"),
+    ("blocks.py", "order = np.lexsort((np.arange(codec.D), -ss))", "order = np.lexsort((-np.arange(codec.D), -ss))"),
     ("blocks.py", "cr, nr = mse_encode(rotate_n(x[..., r], s[SPLIT_N:]), hi_bits - 1)",
                   "cr, nr = mse_encode(rotate_n(x[..., r], s[:SPLIT_N]), hi_bits - 1)"),
     ("blocks.py", "return np.concatenate([_f16_bytes(no), _f16_bytes(nr),", "return np.concatenate([_f16_bytes(nr), _f16_bytes(no),"),
