@@ -367,6 +367,119 @@ def time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src):
     return res
 
 
+PREFILL_CHUNK = {"llama3.1-8b-tq-b8-32k": 1024, "llama3.2-3b-32k": 2048, "llama3.2-3b-32k-k8v4": 2048,
+                 "qwen3-4b-kvarn-128k": 1024, "dense27b-ragged-b32": 1024}
+PREFILL_REPS = 2
+
+
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            if "bf16_tflops" in d:
+                return float(d["bf16_tflops"]), "measured"
+        except (OSError, ValueError):
+            pass
+    return 1900.0, "fallback"
+
+
+def time_prefill(name, cache, w, layers, lens, dev, stream):
+    """Chunked prefill of layer 0: the last T positions of every sequence rewritten by one
+    kv_prefill_attention call (append + attention of the chunk's T queries over the whole context).
+    Reported with the method's multiply-adds per (query head, attended position): key width
+    (128; 256 for TQ3 keys, codes and QJL signs) for the logits + 128 for P.V; the tensor-core
+    work executed is three times that (fp16 hi/lo products)."""
+    B, H, Hq = w["batch"], w["n_kv_heads"], w["n_q_heads"]
+    T = min(PREFILL_CHUNK.get(name, 1024), int(lens.min()))
+    pos_np = (lens - T).astype(np.int32)
+    k, v = synth.kv_tokens(w, 0, B, H, 0, T, device=dev)
+    q = synth.chunk_queries(w, 0, B, Hq, T, device=dev)
+    pos = torch.as_tensor(pos_np, device=dev)
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lay = 0
+    cache.prefill(lay, k, v, q, pos, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(PREFILL_REPS):
+        cache.prefill(lay, k, v, q, pos, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if cache.status() != 0:
+        raise RuntimeError("device status set during the prefill timing")
+    s = e0.elapsed_time(e1) / PREFILL_REPS / 1e3
+    kd = 256 if w["k_format"] == "tq3_qjl" else 128
+    attended = float(sum(int(T) * int(p) + T * (T + 1) / 2 for p in pos_np))   # per (query head): sum over t of pos + t + 1
+    flops = 2.0 * (kd + 128) * attended * Hq
+    peak, src = bf16_peak()
+    achieved = 3 * flops / s / 1e12
+    return {"layers": 1, "tokens_per_sequence": int(T), "us": s * 1e6, "tokens_per_s": B * T / s,
+            "algorithmic_tflops": flops / s / 1e12,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": src,
+                         "note": "executed fp16 mma.sync work (3 x the method's multiply-adds: hi/lo products) "
+                                 "against the measured dense bf16 GEMM rate"},
+            "kernels": "snapshot_kernel + append kernels + prefill_kernel"}
+
+
+CODEC_BLOCKS = 1 << 21        # 256-value TBQ blocks timed (2^29 bf16 values: 1 GiB in)
+CODEC_REPS = 5
+
+
+def time_block_codecs(dev, stream):
+    """Encode and decode throughput of the block codecs on seeded bf16 N(0,1) data (1 GiB in): TBQ3 /
+    TBQ4 blocks and the 2.5 / 3.5-bit outlier split (64 sets, outliers from each set's first 1024
+    vectors).  Algorithmic bytes = the input read + the output written."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(424242)
+    x = torch.randn(CODEC_BLOCKS, 256, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    peak, src = hbm_peak()
+    res = {}
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(CODEC_REPS):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / CODEC_REPS / 1e3
+
+    def entry(nbytes, s):
+        gbs = nbytes / s / 1e9
+        return {"us": s * 1e6, "achieved_gbs": gbs, "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak,
+                                                                  "unit": "GB/s", "frac": gbs / peak, "peak_source": src}}
+
+    for bits in (3, 4):
+        rb = lib.kv_tbq_block_bytes(bits)
+        blk = torch.empty(CODEC_BLOCKS, rb, dtype=torch.uint8, device=dev)
+        out = torch.empty(CODEC_BLOCKS, 256, dtype=torch.float32, device=dev)
+        se = timed(lambda: lib.kv_tbq_encode(bits, 0, x, blk))
+        sd = timed(lambda: lib.kv_tbq_decode(bits, 0, blk, out))
+        res[f"tbq{bits}_encode"] = entry(CODEC_BLOCKS * (512 + rb), se)
+        res[f"tbq{bits}_decode"] = entry(CODEC_BLOCKS * (rb + 1024), sd)
+        del blk, out
+    xv = x.view(64, -1, 128)
+    nv = xv.shape[0] * xv.shape[1]
+    outl = torch.empty(64, 64, dtype=torch.int16, device=dev)
+    lib.kv_split_outliers(xv[:, :1024].contiguous(), outl)
+    for hi in (3, 4):
+        rb = lib.kv_split_record_bytes(hi)
+        rec = torch.empty(nv, rb, dtype=torch.uint8, device=dev)
+        out = torch.empty(xv.shape, dtype=torch.float32, device=dev)
+        se = timed(lambda: lib.kv_split_encode(hi, 0, outl, xv, rec))
+        sd = timed(lambda: lib.kv_split_decode(hi, 0, outl, rec, out))
+        res[f"split{hi - 0.5:g}bit_encode"] = entry(nv * (256 + rb), se)
+        res[f"split{hi - 0.5:g}bit_decode"] = entry(nv * (rb + 512), sd)
+        del rec, out
+    del x
+    torch.cuda.empty_cache()
+    return res
+
+
 def decode_roofline(name, w, layers, lens, dec_us, calls):
     peak, peak_src = hbm_peak()
     alg = algorithmic_bytes(w, layers, lens)
@@ -396,6 +509,7 @@ def measure_other_workload(name, args, dev, stream):
                                          "vs_all_layer_call": g_s * 1e6 / dec_us}
     peak, peak_src = hbm_peak()
     res["bulk_append"] = time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src)
+    res["prefill"] = time_prefill(name, cache, w, layers, lens, dev, stream)
     del cache, qs, out
     torch.cuda.empty_cache()
     return res
@@ -476,6 +590,7 @@ def run_gpu(args):
     d2h_bytes = int(out_h.numel() * 4)
     peak, peak_src = hbm_peak()
     append_res = time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src)
+    prefill_res = time_prefill(args.workload, cache, w, layers, lens, dev, stream)
     del cache, qs, out, q_h, q_d, k_d, v_d
     torch.cuda.empty_cache()
 
@@ -500,6 +615,8 @@ def run_gpu(args):
             "decode_per_layer_graph": per_layer,
             "clocks": clk.summary(),
             "bulk_append": append_res,
+            "prefill": prefill_res,
+            "block_codecs": time_block_codecs(dev, stream),
         }
         if layers < w["n_layers"]:
             # only `layers` of the model's layers are allocated and timed; the whole-model step

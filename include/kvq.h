@@ -284,6 +284,51 @@ int kv_prefill_attention(kvq_cache* cache, int32_t layer, const void* k, const v
                          float* out, const int32_t* pos, int32_t batch, int32_t n_tokens, void* scratch,
                          size_t scratch_bytes, void* stream);
 
+/*
+ * Block codecs next to the cache: the TurboQuant MSE quantiser ([TQ] "key idea" row: random
+ * rotation, per-coordinate optimal scalar quantiser of the unit vector, its norm) on other blocks.
+ * Both rotate with randomized Walsh-Hadamard transforms whose signs are the SplitMix64 stream of
+ * ``seed`` (its first 128 are a cache's rotation signs for the same seed), code each coordinate
+ * with the 2^b-level Lloyd-Max codebook of N(0, 1/n) (fp16 centroids, fp32 midpoints, ties up) and
+ * store the norm as fp16; codes are little-endian bit streams.  Asynchronous on ``stream``; device
+ * pointers 16-byte aligned (``blocks`` of TBQ: any alignment).
+ *
+ * TBQ3_0 / TBQ4_0-style blocks ([TQ] "what the blogbot verified": the llama.cpp proposal adding
+ * TBQ3_0 / TBQ4_0; "limits and counterpoints": about 3.0625 / 4.0625 bits per value): 256
+ * consecutive values (e.g. two 128-value heads of a token row), 256-point rotation, record = fp16
+ * norm + 256 codes of ``bits`` (3 or 4) bits = 98 / 130 bytes.
+ *   x        device, in_dtype (KVQ_IN_F32 / KVQ_IN_BF16), [n_blocks][256]
+ *   blocks   device bytes [n_blocks][kv_tbq_block_bytes(bits)]
+ *   decode output: device float [n_blocks][256]
+ */
+size_t kv_tbq_block_bytes(int32_t bits);
+int kv_tbq_encode(int32_t bits, uint64_t seed, const void* x, int32_t in_dtype, int64_t n_blocks, void* blocks,
+                  void* stream);
+int kv_tbq_decode(int32_t bits, uint64_t seed, const void* blocks, int64_t n_blocks, float* x, void* stream);
+
+/*
+ * Outlier-channel split ([TQ] "method comparison" table: LongBench at 2.5 and 3.5 bits; "what the
+ * blogbot verified": non-integer widths come from splitting off outlier channels): per set (e.g. a
+ * (layer, kv-head)), the 64 channels with the largest mean square over a calibration block are
+ * coded at ``hi_bits`` (3 or 4) and the other 64 at hi_bits - 1 -- 2.5 or 3.5 bits a channel, norms
+ * aside -- each set in ascending channel order, rotated by a 64-point transform (signs 0..63 and
+ * 64..127).  Record = fp16 norm of the outlier set, of the others, then their code streams: 44 / 60
+ * bytes per 128-value vector.
+ *   kv_split_outliers: calib device, in_dtype, [n_sets][n_tokens][128]; outliers device int16
+ *     [n_sets][64] (out), ascending; sums of squares in float64 over the tokens in order, ties to the
+ *     lower channel.
+ *   kv_split_encode / decode: vectors [n_vectors][128] in n_sets equal consecutive groups, group s
+ *     coded with outliers[s]; records device [n_vectors][kv_split_record_bytes(hi_bits)]; decode
+ *     output device float [n_vectors][128].
+ */
+size_t kv_split_record_bytes(int32_t hi_bits);
+int kv_split_outliers(const void* calib, int32_t in_dtype, int32_t n_sets, int32_t n_tokens, int16_t* outliers,
+                      void* stream);
+int kv_split_encode(int32_t hi_bits, uint64_t seed, const int16_t* outliers, int32_t n_sets, const void* x,
+                    int32_t in_dtype, int64_t n_vectors, void* records, void* stream);
+int kv_split_decode(int32_t hi_bits, uint64_t seed, const int16_t* outliers, int32_t n_sets, const void* records,
+                    int64_t n_vectors, float* x, void* stream);
+
 /* Read and clear the device status word (synchronises ``stream``); *flags gets KVQ_DEV_* bits. */
 int kv_status(kvq_cache* cache, uint32_t* flags, void* stream);
 

@@ -17,7 +17,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libkvq.so")
-SOURCES = ["api.cu", "append.cu", "append_bulk.cu", "calibrate.cu", "decode.cu", "noalloc.cu", "prefill.cu"]
+SOURCES = ["api.cu", "append.cu", "append_bulk.cu", "blocks.cu", "calibrate.cu", "decode.cu", "noalloc.cu",
+           "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-ffp-contract=off",
          "--expt-relaxed-constexpr"]

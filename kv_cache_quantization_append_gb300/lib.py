@@ -32,7 +32,8 @@ DEV_TIMEOUT = 8
 EXPORTS = ("kv_cache_bytes", "kv_cache_init", "kv_calibrate_scratch_bytes", "kv_calibrate",
            "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention",
            "kv_decode_attention_noalloc", "kv_prefill_scratch_bytes", "kv_prefill_attention",
-           "kv_status", "kv_strerror")
+           "kv_tbq_block_bytes", "kv_tbq_encode", "kv_tbq_decode", "kv_split_record_bytes",
+           "kv_split_outliers", "kv_split_encode", "kv_split_decode", "kv_status", "kv_strerror")
 NOALLOC_SCRATCH_MAX = 32 * 1024 * 1024
 
 
@@ -81,6 +82,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_decode_attention_noalloc": (ctypes.c_int, [cachep, I32, P, P, P, I32, P]),
         "kv_prefill_scratch_bytes": (SZ, [cachep, I32, I32]),
         "kv_prefill_attention": (ctypes.c_int, [cachep, I32, P, P, P, P, P, I32, I32, P, SZ, P]),
+        "kv_tbq_block_bytes": (SZ, [I32]),
+        "kv_tbq_encode": (ctypes.c_int, [I32, ctypes.c_uint64, P, I32, ctypes.c_int64, P, P]),
+        "kv_tbq_decode": (ctypes.c_int, [I32, ctypes.c_uint64, P, ctypes.c_int64, P, P]),
+        "kv_split_record_bytes": (SZ, [I32]),
+        "kv_split_outliers": (ctypes.c_int, [P, I32, I32, I32, P, P]),
+        "kv_split_encode": (ctypes.c_int, [I32, ctypes.c_uint64, P, I32, P, I32, ctypes.c_int64, P, P]),
+        "kv_split_decode": (ctypes.c_int, [I32, ctypes.c_uint64, P, I32, P, ctypes.c_int64, P, P]),
         "kv_status": (ctypes.c_int, [cachep, U32P, P]),
         "kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     }
@@ -256,6 +264,68 @@ def kv_prefill_attention(cache: kvq_cache, layer: int, k: torch.Tensor, v: torch
     _check(load().kv_prefill_attention(ctypes.byref(cache), layer, _ptr(k), _ptr(v), _ptr(q), _ptr(out),
                                        _ptr(pos), B, T, _ptr(scratch), scratch.numel() * scratch.element_size(),
                                        _stream(stream)))
+
+
+def _in_dtype_of(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KVQ_IN_BF16
+    if t.dtype == torch.float32:
+        return KVQ_IN_F32
+    raise KVQError(f"float32 or bfloat16 input expected, got {t.dtype}")
+
+
+def kv_tbq_block_bytes(bits: int) -> int:
+    return int(load().kv_tbq_block_bytes(bits))
+
+
+def kv_tbq_encode(bits: int, seed: int, x: torch.Tensor, blocks: torch.Tensor, stream=None):
+    """x: [..., 256] float32/bf16 (n_blocks = numel / 256); blocks: uint8 [n_blocks][98 or 130]."""
+    nb = x.numel() // 256
+    if x.shape[-1] != 256 or blocks.dtype != torch.uint8 or blocks.numel() != nb * kv_tbq_block_bytes(bits):
+        raise KVQError("x must be [..., 256] and blocks uint8 of n_blocks * kv_tbq_block_bytes(bits) bytes")
+    _check(load().kv_tbq_encode(bits, seed, _ptr(x), _in_dtype_of(x), nb, _ptr(blocks), _stream(stream)))
+
+
+def kv_tbq_decode(bits: int, seed: int, blocks: torch.Tensor, out: torch.Tensor, stream=None):
+    """blocks: uint8 [n_blocks][98 or 130]; out: float32 [..., 256] with n_blocks * 256 values."""
+    nb = out.numel() // 256
+    if out.dtype != torch.float32 or out.shape[-1] != 256 or blocks.numel() != nb * kv_tbq_block_bytes(bits):
+        raise KVQError("out must be float32 [..., 256] and blocks n_blocks * kv_tbq_block_bytes(bits) bytes")
+    _check(load().kv_tbq_decode(bits, seed, _ptr(blocks), nb, _ptr(out), _stream(stream)))
+
+
+def kv_split_record_bytes(hi_bits: int) -> int:
+    return int(load().kv_split_record_bytes(hi_bits))
+
+
+def kv_split_outliers(calib: torch.Tensor, outliers: torch.Tensor, stream=None):
+    """calib: [n_sets][n_tokens][128] float32/bf16; outliers: int16 [n_sets][64] (written)."""
+    if calib.dim() != 3 or calib.shape[-1] != 128 or outliers.dtype != torch.int16:
+        raise KVQError("calib must be [n_sets][n_tokens][128] and outliers int16")
+    _check_shape("outliers", outliers, (calib.shape[0], 64))
+    _check(load().kv_split_outliers(_ptr(calib), _in_dtype_of(calib), calib.shape[0], calib.shape[1],
+                                    _ptr(outliers), _stream(stream)))
+
+
+def kv_split_encode(hi_bits: int, seed: int, outliers: torch.Tensor, x: torch.Tensor, records: torch.Tensor,
+                    stream=None):
+    """x: [n_sets][...][128]; records: uint8 [n_vectors][44 or 60]; outliers: int16 [n_sets][64]."""
+    n_sets = outliers.shape[0]
+    nv = x.numel() // 128
+    if x.shape[0] != n_sets or x.shape[-1] != 128 or records.numel() != nv * kv_split_record_bytes(hi_bits):
+        raise KVQError("x must be [n_sets][...][128] and records n_vectors * kv_split_record_bytes bytes")
+    _check(load().kv_split_encode(hi_bits, seed, _ptr(outliers), n_sets, _ptr(x), _in_dtype_of(x), nv,
+                                  _ptr(records), _stream(stream)))
+
+
+def kv_split_decode(hi_bits: int, seed: int, outliers: torch.Tensor, records: torch.Tensor, out: torch.Tensor,
+                    stream=None):
+    n_sets = outliers.shape[0]
+    nv = out.numel() // 128
+    if out.dtype != torch.float32 or out.shape[0] != n_sets or records.numel() != nv * kv_split_record_bytes(hi_bits):
+        raise KVQError("out must be float32 [n_sets][...][128] and records n_vectors * kv_split_record_bytes bytes")
+    _check(load().kv_split_decode(hi_bits, seed, _ptr(outliers), n_sets, _ptr(records), nv, _ptr(out),
+                                  _stream(stream)))
 
 
 def kv_status(cache: kvq_cache, stream=None) -> int:

@@ -141,6 +141,15 @@ def kv_tokens(w: dict, layer: int, batch: int, n_kv_heads: int, t0: int, T: int,
     return k.to(dt).contiguous(), v.to(dt).contiguous()
 
 
+def chunk_queries(w: dict, layer: int, batch: int, n_q_heads: int, T: int, device="cpu",
+                  dtype=None) -> torch.Tensor:
+    """Queries of a T-token prefill chunk [B][Hq][T][128], N(0, 1), in one draw."""
+    dt = dtype or (torch.float32 if w["in_dtype"] == "f32" else torch.bfloat16)
+    g = _gen(layer_seed(w, layer, 60000), device)
+    return torch.randn(batch, n_q_heads, T, D, generator=g, device=device,
+                       dtype=torch.float32).to(dt).contiguous()
+
+
 def queries(w: dict, layer: int, batch: int, n_q_heads: int, step: int = 0, device="cpu",
             dtype=None) -> torch.Tensor:
     """Decode queries [B][Hq][128], N(0, 1)."""

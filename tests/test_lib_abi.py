@@ -145,6 +145,28 @@ def test_cache_bytes_null_config(kvq):
     assert kvq.kv_cache_bytes(None) == 0
 
 
+def test_block_codec_sizes_and_refusals(kvq):
+    """Record sizes are the pages' bit widths; unsupported widths and bad arguments are refused
+    before any device work."""
+    import ctypes
+
+    assert lib.kv_tbq_block_bytes(3) == 98 and lib.kv_tbq_block_bytes(4) == 130
+    assert lib.kv_tbq_block_bytes(2) == 0 and lib.kv_tbq_block_bytes(5) == 0
+    assert lib.kv_split_record_bytes(3) == 44 and lib.kv_split_record_bytes(4) == 60
+    assert lib.kv_split_record_bytes(2) == 0
+    P = ctypes.c_void_p
+    d = P(FAKE_DEV)
+    assert kvq.kv_tbq_encode(5, 0, d, 1, 4, d, None) == KVQ_ERR_UNSUPPORTED
+    assert kvq.kv_tbq_encode(3, 0, d, 7, 4, d, None) == KVQ_ERR_UNSUPPORTED
+    assert kvq.kv_tbq_encode(3, 0, None, 1, 4, d, None) == KVQ_ERR_INVALID_ARG
+    assert kvq.kv_tbq_encode(3, 0, P(FAKE_DEV + 4), 1, 4, d, None) == KVQ_ERR_ALIGN
+    assert kvq.kv_tbq_decode(4, 0, d, -1, d, None) == KVQ_ERR_INVALID_ARG
+    assert kvq.kv_split_encode(3, 0, d, 3, d, 1, 10, d, None) == KVQ_ERR_INVALID_ARG     # 10 vectors, 3 sets
+    assert kvq.kv_split_encode(5, 0, d, 1, d, 1, 10, d, None) == KVQ_ERR_UNSUPPORTED
+    assert kvq.kv_split_decode(4, 0, None, 1, d, 10, d, None) == KVQ_ERR_INVALID_ARG
+    assert kvq.kv_split_outliers(d, 1, 0, 10, d, None) == KVQ_ERR_INVALID_ARG
+
+
 # ------------------------------------------------------------------ the header from plain C
 C_PROGRAM = r"""
 #include <stdio.h>
