@@ -128,56 +128,6 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, int lane, int
   hadamard_warp(y0, y1, y2, y3, lane);
   float y[4] = {__fmul_rn(y0, C_WHT), __fmul_rn(y1, C_WHT), __fmul_rn(y2, C_WHT), __fmul_rn(y3, C_WHT)};
 
-  if (kv == 0 && a.k_format == KVQ_TQ3_QJL) {
-    // ---- TurboQuant key: unit vector, 3-bit Lloyd-Max codes, residual QJL signs
-    const CodebookDev* cb = a.p.cb;
-    const float n = __fsqrt_rn(sumsq_warp(y[0], y[1], y[2], y[3]));
-    const float inv = __fdiv_rn(1.0f, fmaxf(n, FLT_MIN));
-    float r[4];
-    uint32_t c12 = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float u = __fmul_rn(y[e], inv);
-      int code = 0;
-#pragma unroll
-      for (int k = 0; k < 7; ++k) code += (cb->bnd[k] <= u) ? 1 : 0;
-      r[e] = __fsub_rn(u, __half2float(cb->cent[code]));
-      c12 |= (uint32_t)code << (3 * e);
-    }
-    const float gamma = __fsqrt_rn(sumsq_warp(r[0], r[1], r[2], r[3]));
-    // t_i = sum_{j = 0..127 in order} S[i][j] * r_j for i = 4*lane + e
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const float4* st = reinterpret_cast<const float4*>(a.p.qjl_t) + lane;
-#pragma unroll 2
-    for (int jq = 0; jq < D / 4; ++jq) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = 4 * jq + e;
-        const float rj = __shfl_sync(FULL, r[e], jq);
-        const float4 s4 = st[j * (D / 4)];
-        acc[0] = __fadd_rn(acc[0], __fmul_rn(s4.x, rj));
-        acc[1] = __fadd_rn(acc[1], __fmul_rn(s4.y, rj));
-        acc[2] = __fadd_rn(acc[2], __fmul_rn(s4.z, rj));
-        acc[3] = __fadd_rn(acc[3], __fmul_rn(s4.w, rj));
-      }
-    }
-    // record byte 2*lane + e holds the codes of channels 4*lane + 2e, +1 (bits 0-2, 3-5) and the
-    // sign bits of projections 4*lane + 2e, +1 (bits 6, 7): this lane's halfword
-    uint32_t hw = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t code = (c12 >> (3 * e)) & 7u, bitv = acc[e] >= 0.0f ? 1u : 0u;
-      hw |= (code << (8 * (e >> 1) + 3 * (e & 1))) | (bitv << (8 * (e >> 1) + 6 + (e & 1)));
-    }
-    reinterpret_cast<uint16_t*>(pg + (size_t)tin * 64)[lane] = (uint16_t)hw;
-    if (lane == 0) {
-      __half* meta = reinterpret_cast<__half*>(pg + a.L.off_kmeta);
-      meta[tin] = __float2half_rn(n);
-      meta[HALF + tin] = __float2half_rn(gamma);
-    }
-    return;
-  }
-
   // ---- Q4G32 or Q8G32 (optionally Sinkhorn-balanced: y / sigma per channel)
   if (a.sinkhorn) {
     const __half* sig = (kv ? a.p.sigv : a.p.sigk) + ((size_t)layer * H + h) * D + 4 * lane;
@@ -245,6 +195,155 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
     if (j < nv) encode_vector(a, lane, kv, layer, b, h, t0 + j, p0 + t0 + j, x[j]);
 }
 
+// ---------------------------------------------------------------- TurboQuant keys
+// [TQ] "key idea" row: unit vector, 3-bit Lloyd-Max codes, then the 1-bit QJL sketch of the
+// residual: bit i = (t_i >= 0), t_i = sum over j = 0..127 in order of RN(S[i][j] * r_j).  The
+// projection (128 x 128 separately rounded multiplies and adds per vector, in that order, so the
+// signs are reproducible bit for bit) is the cost: the transposed projection is staged in shared
+// memory once per CTA and every warp streams TQ_VPW vectors through it, the residuals read as
+// broadcast shared-memory words, the products and sums as packed f32x2 operations (each half
+// rounded like the scalar operation).
+constexpr int TQ_WARPS = 8;
+constexpr int TQ_VPW = 4;
+constexpr size_t TQ_SMEM = (size_t)(D * D + TQ_WARPS * TQ_VPW * D) * sizeof(float);
+
+struct TqKey {
+  uint8_t* pg;     // the token's half-page (nullptr: no record written)
+  int tin;         // token within the half-page
+  uint32_t c12;    // this lane's four 3-bit codes
+  float n, gamma;  // norm and residual norm
+};
+
+// Ring copy, page lookup, rotation, norm, codes and residual of one key vector; the residual
+// (channels 4 lane .. +3) goes to rs[4 lane ..].
+__device__ __forceinline__ TqKey tq_key_prepare(const AppendArgs& a, int lane, int layer, int b, int h, int t, int p,
+                                                float4 xin, float* rs) {
+  TqKey k{nullptr, p % HALF, 0u, 0.f, 0.f};
+  const int H = a.Hkv;
+  if (a.W > 0 && t >= a.T - a.W) {
+    float* dst = a.p.ringk + ((((size_t)layer * a.max_batch + b) * H + h) * a.W + (size_t)(p % a.W)) * D + 4 * lane;
+    *reinterpret_cast<float4*>(dst) = xin;
+  }
+  const int phys = a.block_table[(size_t)b * a.L.max_pages_per_seq + p / PAGE];
+  if (phys < 0 || phys >= a.L.n_pages) {
+    if (lane == 0) atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
+  } else {
+    k.pg = a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + h) * (size_t)a.L.page_bytes +
+           (size_t)((p % PAGE) / HALF) * a.L.half_bytes;
+  }
+  // rotation y = c * H (s . x): sign flip (exact), butterfly, one multiply by c
+  const float4 sg = *reinterpret_cast<const float4*>(a.p.signs + 4 * lane);
+  float y0 = __fmul_rn(xin.x, sg.x), y1 = __fmul_rn(xin.y, sg.y);
+  float y2 = __fmul_rn(xin.z, sg.z), y3 = __fmul_rn(xin.w, sg.w);
+  hadamard_warp(y0, y1, y2, y3, lane);
+  const float y[4] = {__fmul_rn(y0, C_WHT), __fmul_rn(y1, C_WHT), __fmul_rn(y2, C_WHT), __fmul_rn(y3, C_WHT)};
+  const CodebookDev* cb = a.p.cb;
+  k.n = __fsqrt_rn(sumsq_warp(y[0], y[1], y[2], y[3]));
+  const float inv = __fdiv_rn(1.0f, fmaxf(k.n, FLT_MIN));
+  float r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float u = __fmul_rn(y[e], inv);
+    int code = 0;
+#pragma unroll
+    for (int q = 0; q < 7; ++q) code += (cb->bnd[q] <= u) ? 1 : 0;
+    r[e] = __fsub_rn(u, __half2float(cb->cent[code]));
+    k.c12 |= (uint32_t)code << (3 * e);
+  }
+  k.gamma = __fsqrt_rn(sumsq_warp(r[0], r[1], r[2], r[3]));
+  *reinterpret_cast<float4*>(rs + 4 * lane) = make_float4(r[0], r[1], r[2], r[3]);
+  return k;
+}
+
+__global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const AppendArgs a) {
+  extern __shared__ __align__(16) float tq_smem[];
+  const float* sT = tq_smem;  // [j][i] = S[i][j]
+  const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  float* rs = tq_smem + D * D + wl * TQ_VPW * D;  // this warp's residuals [TQ_VPW][128]
+  // a dependent decode launch may start its set-up now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;");
+  for (int i = threadIdx.x; i < D * D / 4; i += TQ_WARPS * 32)
+    reinterpret_cast<float4*>(tq_smem)[i] = reinterpret_cast<const float4*>(a.p.qjl_t)[i];
+  __syncthreads();
+  const int nq = (a.T + TQ_VPW - 1) / TQ_VPW;
+  const unsigned total = (unsigned)a.n_layers_call * a.batch * a.Hkv * nq;
+  for (unsigned wid = blockIdx.x * TQ_WARPS + wl; wid < total; wid += gridDim.x * TQ_WARPS) {
+    const int tq = (int)(wid % nq);
+    unsigned rest = wid / nq;
+    const int h = (int)(rest % a.Hkv);
+    rest /= a.Hkv;
+    const int b = (int)(rest % a.batch);
+    const int ll = (int)(rest / a.batch);
+    const int layer = a.layer0 + ll;
+    const int p0 = a.pos[b];
+    if (p0 < 0) continue;  // sequence not part of this append
+    if ((long long)p0 + a.T > a.max_seq_len) {
+      if (lane == 0 && tq == 0 && h == 0) atomicOr(a.p.status, KVQ_DEV_POS_RANGE);
+      continue;
+    }
+    const int t0 = tq * TQ_VPW;
+    const int nv = min(TQ_VPW, a.T - t0);
+    const size_t vec0 = (((size_t)ll * a.batch + b) * a.Hkv + h) * a.T + t0;
+    float4 x[TQ_VPW];
+#pragma unroll
+    for (int v = 0; v < TQ_VPW; ++v)
+      if (v < nv) x[v] = load4_in(a.k, (vec0 + v) * D + 4 * lane, a.in_bf16);
+    TqKey key[TQ_VPW];
+#pragma unroll
+    for (int v = 0; v < TQ_VPW; ++v) {
+      if (v < nv) {
+        key[v] = tq_key_prepare(a, lane, layer, b, h, t0 + v, p0 + t0 + v, x[v], rs + v * D);
+      } else {
+        key[v] = TqKey{nullptr, 0, 0u, 0.f, 0.f};
+        *reinterpret_cast<float4*>(rs + v * D + 4 * lane) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    __syncwarp();
+    // t_i for i = 4 lane + e, e = 0..3, of each vector: pairs (0, 1) and (2, 3) packed
+    float acc[TQ_VPW][4];
+#pragma unroll
+    for (int v = 0; v < TQ_VPW; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
+#pragma unroll 2
+    for (int jq = 0; jq < D / 4; ++jq) {
+      float4 r4[TQ_VPW];
+#pragma unroll
+      for (int v = 0; v < TQ_VPW; ++v) r4[v] = *reinterpret_cast<const float4*>(rs + v * D + 4 * jq);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float4 s4 = *reinterpret_cast<const float4*>(sT + (4 * jq + e) * D + 4 * lane);
+#pragma unroll
+        for (int v = 0; v < TQ_VPW; ++v) {
+          const float rj = e == 0 ? r4[v].x : e == 1 ? r4[v].y : e == 2 ? r4[v].z : r4[v].w;
+          float p0v = s4.x, p1v = s4.y, p2v = s4.z, p3v = s4.w;
+          mul2(p0v, p1v, rj, rj);
+          mul2(p2v, p3v, rj, rj);
+          add2(acc[v][0], acc[v][1], p0v, p1v);
+          add2(acc[v][2], acc[v][3], p2v, p3v);
+        }
+      }
+    }
+    // record byte 2 lane + e holds the codes of channels 4 lane + 2e, +1 (bits 0-2, 3-5) and the
+    // sign bits of projections 4 lane + 2e, +1 (bits 6, 7): this lane's halfword
+#pragma unroll
+    for (int v = 0; v < TQ_VPW; ++v) {
+      if (key[v].pg == nullptr) continue;
+      uint32_t hw = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t code = (key[v].c12 >> (3 * e)) & 7u, bitv = acc[v][e] >= 0.0f ? 1u : 0u;
+        hw |= (code << (8 * (e >> 1) + 3 * (e & 1))) | (bitv << (8 * (e >> 1) + 6 + (e & 1)));
+      }
+      reinterpret_cast<uint16_t*>(key[v].pg + (size_t)key[v].tin * 64)[lane] = (uint16_t)hw;
+      if (lane == 0) {
+        __half* meta = reinterpret_cast<__half*>(key[v].pg + a.L.off_kmeta);
+        meta[key[v].tin] = __float2half_rn(key[v].n);
+        meta[HALF + key[v].tin] = __float2half_rn(key[v].gamma);
+      }
+    }
+    __syncwarp();  // the residual buffer is reused by the next group
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s) {
@@ -256,25 +355,48 @@ cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_append_tq_keys(const AppendArgs& a, cudaStream_t s) {
+  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + TQ_VPW - 1) / TQ_VPW);
+  if (warps <= 0) return cudaSuccess;
+  if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_tq_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TQ_SMEM);
+  if (e != cudaSuccess) return e;
+  // the projection is loaded once per CTA: at most two CTAs per SM, each looping over warp groups
+  const long long want = (warps + TQ_WARPS - 1) / TQ_WARPS;
+  const long long cap = 2LL * (sms > 0 ? sms : 1);
+  append_tq_keys_kernel<<<(unsigned)(want < cap ? want : cap), TQ_WARPS * 32, TQ_SMEM, s>>>(a);
+  return cudaGetLastError();
+}
+
 // Appends of at least BULK_MIN_T tokens per sequence go to the four-lanes-per-token kernel
-// (append_bulk.cu) for Q4G32 vectors; shorter ones, and TurboQuant keys, to the warp-per-vector
-// kernel above.  Both write identical bytes.
+// (append_bulk.cu) for Q4G32 and Q8G32 vectors; shorter ones to the warp-per-vector kernel above;
+// TurboQuant keys of any length to append_tq_keys_kernel.  All write identical bytes.
 constexpr int BULK_MIN_T = 16;
 
 cudaError_t launch_append(const AppendArgs& a0, cudaStream_t s) {
   AppendArgs a = a0;
   // the bulk kernel's grid has y = (layer, kv-head, K|V) and z = sequence (at most 65535 each)
   if (a.T < BULK_MIN_T || (long long)a.n_layers_call * a.Hkv * 2 > 65535 || a.batch > 65535) {
+    if (a.k_format == KVQ_TQ3_QJL) {
+      const cudaError_t e = launch_append_tq_keys(a, s);
+      if (e != cudaSuccess) return e;
+      a.kv_lo = 1;
+      a.kv_n = 1;
+      return launch_append_warps(a, s);
+    }
     a.kv_lo = 0;
     a.kv_n = 2;
     return launch_append_warps(a, s);
   }
   if (a.k_format == KVQ_TQ3_QJL) {
-    a.kv_lo = 0;
-    a.kv_n = 1;
-    const cudaError_t e = launch_append_warps(a, s);
+    const cudaError_t e = launch_append_tq_keys(a, s);
     if (e != cudaSuccess) return e;
     a.kv_lo = 1;
+    a.kv_n = 1;
     return launch_append_bulk(a, s);
   }
   a.kv_lo = 0;
