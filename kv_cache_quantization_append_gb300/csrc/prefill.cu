@@ -128,17 +128,22 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
-// D[tmem] (+)= A[tmem] * B[smem]^T
+// D[tmem] (+)= A[tmem] * B[smem]^T, issued by the warp's elected lane (lane 0 of a converged warp);
+// every lane of the warp executes the call
 __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
+      "{\n.reg .pred p, e;\nelect.sync _|e, 0xffffffff;\nsetp.ne.b32 p, %4, 0;\n"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d),
       "r"(a), "l"(b), "r"(id), "r"(acc)
       : "memory");
 }
-// arrive on bar once every tcgen05 operation this thread issued so far has completed
+// arrive on bar once every tcgen05 operation the elected lane issued so far has completed (the
+// same lane that issued the products: elect.sync picks the lowest lane of a converged warp)
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+  asm volatile(
+      "{\n.reg .pred e;\nelect.sync _|e, 0xffffffff;\n"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
+      : "memory");
 }
 
 #define KVQ_R8(o, i) o(r[i + 0]), o(r[i + 1]), o(r[i + 2]), o(r[i + 3]), o(r[i + 4]), o(r[i + 5]), o(r[i + 6]), o(r[i + 7])
@@ -360,60 +365,60 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   auto tile_j0 = [&](int it) { return it < nqt ? it * NT : rbeg + (it - nqt) * NT; };
 
   if (warp == MMA_WARP) {
-    // ================================================================ MMA issue (one thread)
-    // Order: logits of tile it, then P.V of tile it - 1, so the logits of the next tile run on the
-    // tensor cores while the softmax warps work on the previous one.  The k-step loops stay rolled
-    // (descriptors advanced by constants in their 14-bit start-address field): four roles share
-    // each scheduler's instruction cache.
-    if (lane == 0) {
-      const uint32_t sbase = smem_u32(smem);
-      bool ok = true;
-      for (int it = 0; it <= ntiles && ok; ++it) {
-        if (it < ntiles) {
-          // logits of tile it into S buffer it & 1 (free once P.V of tile it - 2 has read its weights)
-          const int s = it % NS, bb = it & 1;
-          ok = bar_wait(&kfull[s], (it / NS) & 1, &abort_sh, a.p.status);
-          if (ok && it >= 2) ok = bar_wait(&pvdone[bb], ((it - 2) >> 1) & 1, &abort_sh, a.p.status);
-          if (!ok) break;
-          tc_fence_after();
-          uint64_t kh = sdesc(sbase + s * C::STAGE, 1024, 128);
-          uint32_t qa = tmem + C::C_QHI;
-          const uint32_t dS = tmem + C::C_S + NT * bb;
+    // ================================================================ MMA issue
+    // The whole warp runs the loop (so descriptors and addresses stay warp-uniform) and one
+    // elected lane issues each tcgen05.mma / commit: issued from a divergent single-lane branch,
+    // every product cost ~1.7x more issue time.  Order: logits of tile it, then P.V of tile it - 1,
+    // so the logits of the next tile run on the tensor cores while the softmax warps work on the
+    // previous one.  The k-step loops stay rolled (descriptors advanced by constants in their
+    // 14-bit start-address field): four roles share each scheduler's instruction cache.
+    const uint32_t sbase = smem_u32(smem);
+    bool ok = true;
+    for (int it = 0; it <= ntiles && ok; ++it) {
+      if (it < ntiles) {
+        // logits of tile it into S buffer it & 1 (free once P.V of tile it - 2 has read its weights)
+        const int s = it % NS, bb = it & 1;
+        ok = __all_sync(FULL, bar_wait(&kfull[s], (it / NS) & 1, &abort_sh, a.p.status) &&
+                                  (it < 2 || bar_wait(&pvdone[bb], ((it - 2) >> 1) & 1, &abort_sh, a.p.status)));
+        if (!ok) break;
+        tc_fence_after();
+        uint64_t kh = sdesc(sbase + s * C::STAGE, 1024, 128);
+        uint32_t qa = tmem + C::C_QHI;
+        const uint32_t dS = tmem + C::C_S + NT * bb;
 #pragma unroll 1
-          for (int ks = 0; ks < KD / 16; ++ks, kh += 128, qa += 8) {
-            mma_ts(dS, qa, kh, IDESC_S, ks > 0);
-            mma_ts(dS, qa, kh + (C::K_PLANE >> 4), IDESC_S, 1);
-            mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
-          }
-          mma_commit(&sfull[bb]);
-          mma_commit(&kempty[s]);
+        for (int ks = 0; ks < KD / 16; ++ks, kh += 128, qa += 8) {
+          mma_ts(dS, qa, kh, IDESC_S, ks > 0);
+          mma_ts(dS, qa, kh + (C::K_PLANE >> 4), IDESC_S, 1);
+          mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
         }
-        if (it >= 1) {
-          // P.V of tile it - 1: weights from S buffer (it - 1) & 1 (k-step ks: hi pairs in columns
-          // 16 ks .. +7, lo pairs in 16 ks + 8 .. +15), values from its stage
-          const int j = it - 1, s = j % NS, bb = j & 1;
-          ok = bar_wait(&pfull[bb], (j >> 1) & 1, &abort_sh, a.p.status);
-          if (ok) ok = bar_wait(&vfull[s], (j / NS) & 1, &abort_sh, a.p.status);
-          if (!ok) break;
-          tc_fence_after();
-          uint64_t vh = sdesc(sbase + s * C::STAGE + 2 * C::K_PLANE, 2048, 128);
-          uint32_t pa = tmem + C::C_S + NT * bb;
+        mma_commit(&sfull[bb]);
+        mma_commit(&kempty[s]);
+      }
+      if (it >= 1) {
+        // P.V of tile it - 1: weights from S buffer (it - 1) & 1 (k-step ks: hi pairs in columns
+        // 16 ks .. +7, lo pairs in 16 ks + 8 .. +15), values from its stage
+        const int j = it - 1, s = j % NS, bb = j & 1;
+        ok = __all_sync(FULL, bar_wait(&pfull[bb], (j >> 1) & 1, &abort_sh, a.p.status) &&
+                                  bar_wait(&vfull[s], (j / NS) & 1, &abort_sh, a.p.status));
+        if (!ok) break;
+        tc_fence_after();
+        uint64_t vh = sdesc(sbase + s * C::STAGE + 2 * C::K_PLANE, 2048, 128);
+        uint32_t pa = tmem + C::C_S + NT * bb;
 #pragma unroll 1
-          for (int ks = 0; ks < NT / 16; ++ks, vh += 256, pa += 16) {
-            mma_ts(tmem + C::C_O, pa, vh, IDESC_O, (j > 0 || ks > 0));
-            mma_ts(tmem + C::C_O, pa, vh + (C::V_PLANE >> 4), IDESC_O, 1);
-            mma_ts(tmem + C::C_O, pa + 8, vh, IDESC_O, 1);
-          }
-          mma_commit(&vempty[s]);
-          mma_commit(&pvdone[bb]);
+        for (int ks = 0; ks < NT / 16; ++ks, vh += 256, pa += 16) {
+          mma_ts(tmem + C::C_O, pa, vh, IDESC_O, (j > 0 || ks > 0));
+          mma_ts(tmem + C::C_O, pa, vh + (C::V_PLANE >> 4), IDESC_O, 1);
+          mma_ts(tmem + C::C_O, pa + 8, vh, IDESC_O, 1);
         }
+        mma_commit(&vempty[s]);
+        mma_commit(&pvdone[bb]);
       }
-      // every product issued lands before the output is read or the columns are freed (the wait is
-      // bounded; a CTA that gave up still waits here for what it issued)
-      mma_commit(&ofull);
-      const unsigned long long t0w = gtimer();
-      while (!bar_try(&ofull, 0) && gtimer() - t0w < WAIT_NS) {
-      }
+    }
+    // every product issued lands before the output is read or the columns are freed (the wait is
+    // bounded; a CTA that gave up still waits here for what it issued)
+    mma_commit(&ofull);
+    const unsigned long long t0w = gtimer();
+    while (!bar_try(&ofull, 0) && gtimer() - t0w < WAIT_NS) {
     }
     __syncwarp();
   } else if (warp >= DQ_WARP0) {
@@ -437,9 +442,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       uint4 vs, vz;    // value scales and zeros of the octet
       bool bad;
     };
-    auto load_words = [&](int it, Words& w) {
-      const int j0 = it * NT;  // quantised tiles only
-      const int phys = bt_seq[j0 / PAGE];
+    // block-table entries are read two tiles ahead (bt1: tile it + 1, bt2: tile it + 2), so the page
+    // addresses of a prefetch never wait on a table load
+    auto bt_at = [&](int it) { return it < nqt ? __ldg(bt_seq + it) : 0; };
+    auto load_words = [&](int it, int phys, Words& w) {
+      const int j0 = it * NT;  // quantised tiles only (one page each)
       w.bad = phys < 0 || phys >= a.L.n_pages;
       w.k0 = w.k1 = w.vs = w.vz = make_uint4(0u, 0u, 0u, 0u);
       w.kx = 0u;
@@ -478,13 +485,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       }
     };
     Words cur, nxt;
-    if (nqt > 0) load_words(0, cur);
+    if (nqt > 0) load_words(0, bt_at(0), cur);
+    int bt1 = bt_at(1), bt2 = bt_at(2);
     for (int it = 0; it < ntiles; ++it) {
       const int s = it % NS;
       const uint32_t ph = (uint32_t)((it / NS) & 1) ^ 1u;  // phase of the stage's previous use
       const bool raw = it >= nqt;
       const int j0 = tile_j0(it);
-      if (it + 1 < nqt) load_words(it + 1, nxt);
+      if (it + 1 < nqt) load_words(it + 1, bt1, nxt);
+      bt1 = bt2;
+      bt2 = bt_at(it + 3);
       uint8_t* khi = smem + s * C::STAGE;
       uint8_t* klo = khi + C::K_PLANE;
       uint8_t* vhi = klo + C::K_PLANE;
@@ -646,15 +656,16 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     const int P = row < nrows ? p0 + t0 + row / g : -1;
     float mref = -INFINITY, lsum = 0.f;
     bool ok = true;
+    // block-table entries of tiles it and it + 1, read ahead
+    int bt0 = nqt > 0 ? __ldg(bt_seq) : 0, bt1 = nqt > 1 ? __ldg(bt_seq + 1) : 0;
     for (int it = 0; it < ntiles && ok; ++it) {
       const int bb = it & 1;
       const bool raw = it >= nqt;
       const int j0 = tile_j0(it);
-      bool bad = false;
-      if (!raw) {
-        const int phys = bt_seq[j0 / PAGE];
-        bad = phys < 0 || phys >= a.L.n_pages;
-      }
+      const int phys = bt0;
+      bt0 = bt1;
+      bt1 = it + 2 < nqt ? __ldg(bt_seq + it + 2) : 0;
+      const bool bad = !raw && (phys < 0 || phys >= a.L.n_pages);
       // valid positions of this row in the tile: [lo, hi]
       int lo = 1, hi = 0;
       if (P >= 0 && !bad) {
