@@ -262,6 +262,10 @@ def weak_scaling_value(tokens_per_step_per_rank: float, world: int, ms_per_step_
 # ------------------------------------------------------------------ GPU arm
 DECODE_ROOFLINE_MIN_S = 1.0   # the decode-only pass runs at least this long, whatever --steps is
 BULK_APPEND_REPS = 10
+# FP32 rate of interleaved packed multiplies and adds (mul.rn.f32x2 / add.rn.f32x2, each half rounded
+# like the scalar operation), measured on a GB300 with independent chains: 236.5 results per SM
+# clock, 74.4 Tops/s over 152 SMs at 2070 MHz (scalar adds alone: 120 per clock)
+FP32_PAIR_PEAK_TOPS = 74.4
 
 
 def step_inputs(w, layers, lens, dev, nbuf=8):
@@ -361,9 +365,19 @@ def time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src):
     a_bytes = bulk_append_bytes(w, layers, Tc)
     res = {"tokens_per_sequence": Tc, "us": a_s * 1e6, "algorithmic_bytes": a_bytes,
            "achieved_gbs": a_bytes / a_s / 1e9, "tokens_per_s": layers * B * Tc / a_s,
-           "kernel": "append_bulk_kernel" + (" + append_kernel (TQ3 keys)" if w["k_format"] == "tq3_qjl" else "")}
+           "kernel": ("append_tq_keys_kernel + append_bulk_kernel (values)" if w["k_format"] == "tq3_qjl"
+                      else "append_bulk_kernel")}
     res["roofline"] = {"bound": "hbm", "achieved": res["achieved_gbs"], "peak": peak, "unit": "GB/s",
                        "frac": res["achieved_gbs"] / peak, "peak_source": peak_src}
+    if w["k_format"] == "tq3_qjl":
+        # TurboQuant keys: the QJL projection (128 x 128 separately rounded products and sums per key,
+        # in the codec's order) bounds the keys kernel on the FP32 pipes, not on HBM
+        ops = float(layers * B * H * Tc) * 2 * 128 * 128
+        res["roofline_keys"] = {
+            "bound": "alu", "achieved": ops / a_s / 1e12, "peak": FP32_PAIR_PEAK_TOPS, "unit": "Tops/s",
+            "frac": ops / a_s / 1e12 / FP32_PAIR_PEAK_TOPS, "peak_source": "measured (packed fp32 multiply/add)",
+            "note": "projection operations over the whole append call (keys and values kernels): a lower "
+                    "bound for the keys kernel's own rate"}
     return res
 
 
@@ -418,8 +432,8 @@ def time_prefill(name, cache, w, layers, lens, dev, stream):
             "algorithmic_tflops": flops / s / 1e12,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": src,
-                         "note": "executed fp16 mma.sync work (3 x the method's multiply-adds: hi/lo products) "
-                                 "against the measured dense bf16 GEMM rate"},
+                         "note": "executed fp16 tcgen05 products (3 x the method's multiply-adds: hi/lo "
+                                 "products) against the measured dense bf16 GEMM rate"},
             "kernels": "snapshot_kernel + append kernels + prefill_kernel"}
 
 
