@@ -29,9 +29,10 @@
 //    base 2 against a lazily raised reference (raised only when a row's maximum passes it by 8, so
 //    weights stay below 2^8 and the output rows are rescaled rarely), and write the weights back in
 //    place as fp16 hi/lo: the A operand of O += Phi Vhi + Phi Vlo + Plo Vhi.
-//  * Warp roles: 4 softmax warps (TMEM lane quarters), 1 MMA-issuing warp (one thread; it also
-//    owns the TMEM allocation), 8 dequantising warps filling an NS-stage shared-memory ring; every
-//    hand-off is an mbarrier (tcgen05.commit for the tensor-core side), every wait bounded.
+//  * Warp roles: 4 softmax warps (TMEM lane quarters), 2 MMA-issuing warps (the logits, and P.V;
+//    the first owns the TMEM allocation), 8 dequantising warps filling an NS-stage shared-memory
+//    ring; every hand-off is an mbarrier (tcgen05.commit for the tensor-core side), every wait
+//    bounded.
 //  * Quantised and raw tiles cover disjoint (row, position) pairs through their masks: position j
 //    is quantised for query P when j <= P - window, raw when P - window < j <= P.
 //  * The output row is normalised, unfolded (sigma_v) and unrotated at the end.
@@ -46,8 +47,9 @@ namespace {
 constexpr int ROWS = 128;    // (query, head) rows per CTA = MMA M = TMEM lanes
 constexpr int NT = 64;       // key positions per tile (one page) = logits N
 constexpr int N_SOFT = 4;    // softmax warps
-constexpr int MMA_WARP = 4;  // lane 0 issues every tcgen05.mma; the warp owns the TMEM allocation
-constexpr int DQ_WARP0 = 5;  // first dequantising warp
+constexpr int MMA_WARP = 4;  // issues the logits products; the warp owns the TMEM allocation
+constexpr int PV_WARP = 5;   // issues the P.V products
+constexpr int DQ_WARP0 = 6;  // first dequantising warp
 constexpr int N_DQ = 8;
 constexpr int THREADS = (DQ_WARP0 + N_DQ) * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -222,7 +224,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   constexpr int KD = C::KD, NS = C::NS;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) uint64_t kfull[NS], kempty[NS], vfull[NS], vempty[NS];
-  __shared__ __align__(8) uint64_t sfull[2], pfull[2], pvdone[2], ofull;
+  __shared__ __align__(8) uint64_t sfull[2], pfull[2], pvdone[2], ofull, sdone;
   __shared__ uint32_t tmem_base_sh;
   __shared__ float cent_sh[8];
   __shared__ int abort_sh;
@@ -273,6 +275,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       bar_init(&pvdone[i], 1);
     }
     bar_init(&ofull, 1);
+    bar_init(&sdone, 1);
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -364,18 +367,18 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
 
   auto tile_j0 = [&](int it) { return it < nqt ? it * NT : rbeg + (it - nqt) * NT; };
 
-  if (warp == MMA_WARP) {
+  if (warp == MMA_WARP || warp == PV_WARP) {
     // ================================================================ MMA issue
-    // The whole warp runs the loop (so descriptors and addresses stay warp-uniform) and one
-    // elected lane issues each tcgen05.mma / commit: issued from a divergent single-lane branch,
-    // every product cost ~1.7x more issue time.  Order: logits of tile it, then P.V of tile it - 1,
-    // so the logits of the next tile run on the tensor cores while the softmax warps work on the
-    // previous one.  The k-step loops stay rolled (descriptors advanced by constants in their
-    // 14-bit start-address field): four roles share each scheduler's instruction cache.
+    // Two issuing warps on different schedulers: MMA_WARP issues every logits product, PV_WARP
+    // every P.V product.  Each whole warp runs its loop (so descriptors and addresses stay
+    // warp-uniform) and one elected lane issues each tcgen05.mma / commit: issued from a divergent
+    // single-lane branch, every product cost ~1.7x more issue time.  The k-step loops stay rolled
+    // (descriptors advanced by constants in their 14-bit start-address field): four roles share
+    // each scheduler's instruction cache.
     const uint32_t sbase = smem_u32(smem);
     bool ok = true;
-    for (int it = 0; it <= ntiles && ok; ++it) {
-      if (it < ntiles) {
+    if (warp == MMA_WARP) {
+      for (int it = 0; it < ntiles; ++it) {
         // logits of tile it into S buffer it & 1 (free once P.V of tile it - 2 has read its weights)
         const int s = it % NS, bb = it & 1;
         ok = __all_sync(FULL, bar_wait(&kfull[s], (it / NS) & 1, &abort_sh, a.p.status) &&
@@ -394,19 +397,20 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         mma_commit(&sfull[bb]);
         mma_commit(&kempty[s]);
       }
-      if (it >= 1) {
-        // P.V of tile it - 1: weights from S buffer (it - 1) & 1 (k-step ks: hi pairs in columns
-        // 16 ks .. +7, lo pairs in 16 ks + 8 .. +15), values from its stage
-        const int j = it - 1, s = j % NS, bb = j & 1;
-        ok = __all_sync(FULL, bar_wait(&pfull[bb], (j >> 1) & 1, &abort_sh, a.p.status) &&
-                                  bar_wait(&vfull[s], (j / NS) & 1, &abort_sh, a.p.status));
+    } else {
+      for (int it = 0; it < ntiles; ++it) {
+        // P.V of tile it: weights from S buffer it & 1 (k-step ks: hi pairs in columns 16 ks .. +7,
+        // lo pairs in 16 ks + 8 .. +15), values from its stage
+        const int s = it % NS, bb = it & 1;
+        ok = __all_sync(FULL, bar_wait(&pfull[bb], (it >> 1) & 1, &abort_sh, a.p.status) &&
+                                  bar_wait(&vfull[s], (it / NS) & 1, &abort_sh, a.p.status));
         if (!ok) break;
         tc_fence_after();
         uint64_t vh = sdesc(sbase + s * C::STAGE + 2 * C::K_PLANE, 2048, 128);
         uint32_t pa = tmem + C::C_S + NT * bb;
 #pragma unroll 1
         for (int ks = 0; ks < NT / 16; ++ks, vh += 256, pa += 16) {
-          mma_ts(tmem + C::C_O, pa, vh, IDESC_O, (j > 0 || ks > 0));
+          mma_ts(tmem + C::C_O, pa, vh, IDESC_O, (it > 0 || ks > 0));
           mma_ts(tmem + C::C_O, pa, vh + (C::V_PLANE >> 4), IDESC_O, 1);
           mma_ts(tmem + C::C_O, pa + 8, vh, IDESC_O, 1);
         }
@@ -414,11 +418,12 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         mma_commit(&pvdone[bb]);
       }
     }
-    // every product issued lands before the output is read or the columns are freed (the wait is
-    // bounded; a CTA that gave up still waits here for what it issued)
-    mma_commit(&ofull);
+    // every product this warp issued lands before the output is read or the columns are freed
+    // (the wait is bounded; a CTA that gave up still waits here for what it issued)
+    uint64_t* done = warp == PV_WARP ? &ofull : &sdone;
+    mma_commit(done);
     const unsigned long long t0w = gtimer();
-    while (!bar_try(&ofull, 0) && gtimer() - t0w < WAIT_NS) {
+    while (!bar_try(done, 0) && gtimer() - t0w < WAIT_NS) {
     }
     __syncwarp();
   } else if (warp >= DQ_WARP0) {
