@@ -426,14 +426,17 @@ def time_prefill(name, cache, w, layers, lens, dev, stream):
     kd = 256 if w["k_format"] == "tq3_qjl" else 128
     attended = float(sum(int(T) * int(p) + T * (T + 1) / 2 for p in pos_np))   # per (query head): sum over t of pos + t + 1
     flops = 2.0 * (kd + 128) * attended * Hq
+    # products executed per method multiply-add: 3 (hi/lo splits), except TQ3 keys' centroid half,
+    # whose fp16 centroids are exact (2: the query's hi and lo)
+    exec_macs = (2 * 128 + 3 * 128 + 3 * 128) if w["k_format"] == "tq3_qjl" else 3 * (kd + 128)
     peak, src = bf16_peak()
-    achieved = 3 * flops / s / 1e12
+    achieved = 2.0 * exec_macs * attended * Hq / s / 1e12
     return {"layers": 1, "tokens_per_sequence": int(T), "us": s * 1e6, "tokens_per_s": B * T / s,
             "algorithmic_tflops": flops / s / 1e12,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "peak_source": src,
-                         "note": "executed fp16 tcgen05 products (3 x the method's multiply-adds: hi/lo "
-                                 "products) against the measured dense bf16 GEMM rate"},
+                         "note": "executed fp16 tcgen05 products (hi/lo splits: 3 per method multiply-add, 2 "
+                                 "for TQ3 keys' exact centroids) against the measured dense bf16 GEMM rate"},
             "kernels": "snapshot_kernel + append kernels + prefill_kernel"}
 
 

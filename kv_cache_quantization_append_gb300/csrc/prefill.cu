@@ -66,17 +66,22 @@ constexpr uint32_t IDESC_O = idesc(ROWS, D);   // P.V: 128 x 128
 template <int KF>
 struct Cfg {
   static constexpr bool TQ = KF == KVQ_TQ3_QJL;
-  static constexpr int KD = TQ ? 256 : 128;          // width of the key space the logits are taken in
+  static constexpr int KD = TQ ? 256 : 128;          // width of the query: [q~] or [q~, S q~]
   static constexpr int NS = TQ ? 2 : 3;              // pipeline stages
-  static constexpr uint32_t K_PLANE = NT * KD * 2;   // one fp16 plane (hi or lo) of a key tile
+  static constexpr uint32_t K_PLANE = NT * D * 2;    // one fp16 plane of a key tile: 64 positions x 128
+  // key planes: hi, lo (Q4G32 / Q8G32 keys and every raw tile); TQ3 quantised tiles: exact
+  // centroids, then the QJL part's hi and lo
+  static constexpr int K_PLANES = TQ ? 3 : 2;
   static constexpr uint32_t V_PLANE = D * NT * 2;    // one fp16 plane of a transposed value tile
-  static constexpr uint32_t STAGE = 2 * K_PLANE + 2 * V_PLANE;
+  static constexpr uint32_t V_OFF = K_PLANES * K_PLANE;
+  static constexpr uint32_t STAGE = V_OFF + 2 * V_PLANE;
   static constexpr uint32_t SMEM = NS * STAGE;
   static constexpr uint32_t Q_STRIDE = 2 * KD * 2 + 16;  // query staging row: hi halves, lo halves, pad
   // tensor-memory columns: Q hi | Q lo | O | S/P buffer 0 | S/P buffer 1
   static constexpr uint32_t C_QHI = 0, C_QLO = KD / 2, C_O = KD, C_S = KD + D;
   static_assert(C_S + 2 * NT <= TMEM_COLS, "tensor memory");
-  static_assert((uint32_t)ROWS * Q_STRIDE <= SMEM, "query staging fits the ring");
+  static_assert((uint32_t)ROWS * Q_STRIDE + (uint32_t)(THREADS / 32) * D * 4 <= SMEM,
+                "query staging and the projection rows fit the ring");
   static_assert((uint32_t)ROWS * (D + 4) * 4 <= SMEM, "output staging fits the ring");
 };
 
@@ -226,7 +231,8 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
   __shared__ __align__(8) uint64_t kfull[NS], kempty[NS], vfull[NS], vempty[NS];
   __shared__ __align__(8) uint64_t sfull[2], pfull[2], pvdone[2], ofull, sdone;
   __shared__ uint32_t tmem_base_sh;
-  __shared__ float cent_sh[8];
+  __shared__ uint32_t cent2_sh[64];
+  __shared__ uint4 nbuf[N_SOFT][8];  // TQ3: the current tile's 64 position norms (fp16), per softmax warp  // TQ3: half2 (cent[v & 7], cent[v >> 3]) of a record byte's codes v
   __shared__ int abort_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -279,7 +285,9 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
     abort_sh = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (C::TQ && tid < 8) cent_sh[tid] = __half2float(a.p.cb->cent[tid]);
+  if (C::TQ && tid < 64)
+    cent2_sh[tid] = (uint32_t)__half_as_ushort(a.p.cb->cent[tid & 7]) |
+                    ((uint32_t)__half_as_ushort(a.p.cb->cent[tid >> 3]) << 16);
   if (warp == MMA_WARP) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_sh)),
                  "r"(TMEM_COLS)
@@ -388,11 +396,29 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
         uint64_t kh = sdesc(sbase + s * C::STAGE, 1024, 128);
         uint32_t qa = tmem + C::C_QHI;
         const uint32_t dS = tmem + C::C_S + NT * bb;
+        if (C::TQ && it < nqt) {
+          // TQ3 quantised tile: S' = Q~ . C (exact centroids: hi and lo of the query) + (S q~) . W
+          // (hi/lo of the QJL part); the softmax multiplies column j by the position's norm
 #pragma unroll 1
-        for (int ks = 0; ks < KD / 16; ++ks, kh += 128, qa += 8) {
-          mma_ts(dS, qa, kh, IDESC_S, ks > 0);
-          mma_ts(dS, qa, kh + (C::K_PLANE >> 4), IDESC_S, 1);
-          mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
+          for (int ks = 0; ks < D / 16; ++ks, kh += 128, qa += 8) {
+            mma_ts(dS, qa, kh, IDESC_S, ks > 0);
+            mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
+          }
+          kh += (C::K_PLANE >> 4) - 128 * (D / 16);  // the QJL planes; qa now at the S q~ columns
+#pragma unroll 1
+          for (int ks = 0; ks < D / 16; ++ks, kh += 128, qa += 8) {
+            mma_ts(dS, qa, kh, IDESC_S, 1);
+            mma_ts(dS, qa, kh + (C::K_PLANE >> 4), IDESC_S, 1);
+            mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
+          }
+        } else {
+          // hi/lo key planes against the first 128 query columns
+#pragma unroll 1
+          for (int ks = 0; ks < D / 16; ++ks, kh += 128, qa += 8) {
+            mma_ts(dS, qa, kh, IDESC_S, ks > 0);
+            mma_ts(dS, qa, kh + (C::K_PLANE >> 4), IDESC_S, 1);
+            mma_ts(dS, qa + (C::C_QLO - C::C_QHI), kh, IDESC_S, 1);
+          }
         }
         mma_commit(&sfull[bb]);
         mma_commit(&kempty[s]);
@@ -406,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
                                   bar_wait(&vfull[s], (it / NS) & 1, &abort_sh, a.p.status));
         if (!ok) break;
         tc_fence_after();
-        uint64_t vh = sdesc(sbase + s * C::STAGE + 2 * C::K_PLANE, 2048, 128);
+        uint64_t vh = sdesc(sbase + s * C::STAGE + C::V_OFF, 2048, 128);
         uint32_t pa = tmem + C::C_S + NT * bb;
 #pragma unroll 1
         for (int ks = 0; ks < NT / 16; ++ks, vh += 256, pa += 16) {
@@ -502,7 +528,7 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       bt2 = bt_at(it + 3);
       uint8_t* khi = smem + s * C::STAGE;
       uint8_t* klo = khi + C::K_PLANE;
-      uint8_t* vhi = klo + C::K_PLANE;
+      uint8_t* vhi = khi + C::V_OFF;
       uint8_t* vlo = vhi + C::V_PLANE;
       if (!raw && cur.bad && dq == 0) atomicOr(a.p.status, KVQ_DEV_BAD_PAGE);
       // ---------------- keys
@@ -541,24 +567,32 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
             }
         } else {
           // TQ3: bytes 16 part .. +15 = codes of channels 32 part .. +31 and signs of projections
-          // 32 part .. +31 (byte j: channels 2j, 2j+1)
-          const float nn = __half2float(__ushort_as_half((unsigned short)(cur.kx & 0xffffu)));
-          const float wq = nn * QJL_CONST * __half2float(__ushort_as_half((unsigned short)(cur.kx >> 16)));
+          // 32 part .. +31 (byte j: channels 2j, 2j+1).  The norm n is left out (the softmax applies
+          // it per position): plane 0 gets the exact fp16 centroids, planes 1 and 2 the hi and lo of
+          // w = sqrt(pi/2)/128 gamma with the sign of each projection (sign flips are exact)
+          const bool okk = !cur.bad && j0 + kt < qend;
+          const float w = QJL_CONST * __half2float(__ushort_as_half((unsigned short)(cur.kx >> 16)));
+          const __half whi = __float2half_rn(okk ? w : 0.f);
+          const __half wlo = __float2half_rn(okk ? w - __half2float(whi) : 0.f);
+          const uint32_t whi2 = (uint32_t)__half_as_ushort(whi) * 0x10001u;
+          const uint32_t wlo2 = (uint32_t)__half_as_ushort(wlo) * 0x10001u;
+          uint8_t* kw2 = khi + 2 * C::K_PLANE;
           uint4 cw = cur.k0;  // word x of the 16 bytes is consumed at step x (the loop stays rolled)
 #pragma unroll 1
           for (int x = 0; x < 4; ++x) {
-            float vc[8], vs[8];
+            uint32_t cc[4], sh[4], sl[4];
 #pragma unroll
             for (int y = 0; y < 4; ++y) {
-              const uint32_t byte = (cw.x >> (8 * y)) & 0xffu;
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                vc[2 * y + e] = nn * cent_sh[(byte >> (3 * e)) & 7u];
-                vs[2 * y + e] = ((byte >> (6 + e)) & 1u) ? wq : -wq;
-              }
+              const uint32_t byte = (cw.x >> (8 * y)) & 0xffu, nb = ~byte;
+              const uint32_t m = ((nb & 0x40u) << 9) | ((nb & 0x80u) << 24);  // clear bit: -w
+              cc[y] = okk ? cent2_sh[byte & 63u] : 0u;
+              sh[y] = whi2 ^ m;
+              sl[y] = wlo2 ^ m;
             }
-            store8(khi, klo, cm_off(kt, 8 * (4 * kpart + x), NT), vc);
-            store8(khi, klo, cm_off(kt, D + 8 * (4 * kpart + x), NT), vs);
+            const uint32_t off = cm_off(kt, 8 * (4 * kpart + x), NT);
+            *reinterpret_cast<uint4*>(khi + off) = make_uint4(cc[0], cc[1], cc[2], cc[3]);
+            *reinterpret_cast<uint4*>(klo + off) = make_uint4(sh[0], sh[1], sh[2], sh[3]);
+            *reinterpret_cast<uint4*>(kw2 + off) = make_uint4(sl[0], sl[1], sl[2], sl[3]);
             cw = make_uint4(cw.y, cw.z, cw.w, 0u);
           }
         }
@@ -585,11 +619,6 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           const uint32_t off = cm_off(t, 4 * lane, NT);
           *reinterpret_cast<uint2*>(khi + off) = hv;
           *reinterpret_cast<uint2*>(klo + off) = lv;
-          if (C::TQ) {
-            const uint32_t offs = cm_off(t, D + 4 * lane, NT);
-            *reinterpret_cast<uint2*>(khi + offs) = make_uint2(0u, 0u);
-            *reinterpret_cast<uint2*>(klo + offs) = make_uint2(0u, 0u);
-          }
         }
       }
       fence_async_smem();
@@ -682,6 +711,17 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
           hi = P;
         }
       }
+      // TQ3 quantised tile: the positions' norms n (fp16, the page's key metadata), requested before
+      // the wait; column j of the tile's logits is n_j S'_j
+      if (C::TQ && !raw && !bad) {
+        __syncwarp();  // the previous tile's reads of the warp's buffer are done
+        if (lane < 8) {
+          const uint8_t* pgp = a.p.pages + (((size_t)layer * a.L.n_pages + phys) * H + h) * (size_t)a.L.page_bytes;
+          nbuf[warp][lane] =
+              __ldg(reinterpret_cast<const uint4*>(pgp + (size_t)(lane >> 2) * a.L.half_bytes + a.L.off_kmeta) + (lane & 3));
+        }
+        __syncwarp();
+      }
       // waits are decided warp-wide: the tensor-memory loads and stores below are warp-collective
       if (!__all_sync(FULL, bar_wait(&sfull[bb], (it >> 1) & 1, &abort_sh, a.p.status))) {
         ok = false;
@@ -695,9 +735,11 @@ __global__ void __launch_bounds__(THREADS, 1) prefill_kernel(const __grid_consta
       const bool all_valid = j0 >= lo && j0 + NT - 1 <= hi;
       float x[NT];
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const bool scale_n = C::TQ && !raw && !bad;
 #pragma unroll
       for (int c = 0; c < NT; ++c) {
-        const float sv = __uint_as_float(sr[c >> 5][c & 31]);
+        float sv = __uint_as_float(sr[c >> 5][c & 31]);
+        if (C::TQ && scale_n) sv *= __half2float(reinterpret_cast<const __half*>(nbuf[warp])[c]);
         x[c] = (all_valid || (j0 + c >= lo && j0 + c <= hi)) ? sv : -INFINITY;
         m4[c & 3] = fmaxf(m4[c & 3], x[c]);
       }
