@@ -1468,8 +1468,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   // step k uses slot warp + NCW*(k mod NSLOT), phase k / NSLOT of that slot
   for (int k = 0, j = 0, ph = 0; k < n; ++k) {
     const int slot = K.warp + NCW * j;
-    // decided warp-wide: the warp's mma.sync and shuffles below need every lane
-    if (!__all_sync(FULL, mbar_wait(full + slot, ph, a.p.status))) break;
+    if (!mbar_wait(full + slot, ph, a.p.status)) break;
     if (++j == GE::NSLOT) {
       j = 0;
       ph ^= 1;
