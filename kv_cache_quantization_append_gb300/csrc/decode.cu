@@ -41,6 +41,7 @@ constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wai
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
 constexpr int MERGE_WARPS = 8;  // warps per CTA of the merge kernels
 constexpr long long WIDE_MERGE_RECORDS = 48;  // above this many records per unit, merge with a CTA per head
+constexpr int WIDE_MERGE_WARPS = 16;          // warps per CTA of merge_wide_kernel (each a slice of the records)
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
@@ -1172,17 +1173,17 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const __grid_co
 // the GPU: hundreds of records per unit): one CTA per (unit, query head), its warps merging
 // consecutive slices of the records in parallel; the eight partial states are then combined in
 // slice order by the first warp (a fixed order: deterministic), which writes the output.
-__global__ void __launch_bounds__(MERGE_WARPS * 32) merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(WIDE_MERGE_WARPS * 32) merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  __shared__ float4 sO[MERGE_WARPS][2][32];
-  __shared__ float sM[MERGE_WARPS][2], sL[MERGE_WARPS][2];
+  __shared__ float4 sO[WIDE_MERGE_WARPS][2][32];
+  __shared__ float sM[WIDE_MERGE_WARPS][2], sL[WIDE_MERGE_WARPS][2];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int u = blockIdx.x / a.g, hh = blockIdx.x % a.g;
   const int2 info = __ldcg(a.unit_info + u);
   float4 sg, sv;
   if (w == 0) merge_constants(a, u, lane, sg, sv);
-  const int per = (info.y + MERGE_WARPS - 1) / MERGE_WARPS;
+  const int per = (info.y + WIDE_MERGE_WARPS - 1) / WIDE_MERGE_WARPS;
   const int r0 = min(info.y, w * per), r1 = min(info.y, r0 + per);
   float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
@@ -1200,11 +1201,11 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_wide_kernel(const __gr
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     float M = -INFINITY;
-    for (int j = 0; j < MERGE_WARPS; ++j)
+    for (int j = 0; j < WIDE_MERGE_WARPS; ++j)
       if (sL[j][k] > 0.f) M = fmaxf(M, sM[j][k]);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
-    for (int j = 0; j < MERGE_WARPS; ++j) {
+    for (int j = 0; j < WIDE_MERGE_WARPS; ++j) {
       if (!(sL[j][k] > 0.f)) continue;
       const float f = exp2f(sM[j][k] - M);
       const float4 x = sO[j][k][lane];
@@ -1565,6 +1566,7 @@ static cudaError_t launch_kf(const DecodeArgs& a, cudaStream_t s) {
   mcfg.dynamicSmemBytes = 0;
   if (recs_per_unit > WIDE_MERGE_RECORDS) {
     mcfg.gridDim = dim3((unsigned)tasks);
+    mcfg.blockDim = dim3(WIDE_MERGE_WARPS * 32);
     return cudaLaunchKernelEx(&mcfg, merge_wide_kernel, a);
   }
   mcfg.gridDim = dim3((unsigned)((tasks + MERGE_WARPS - 1) / MERGE_WARPS));
