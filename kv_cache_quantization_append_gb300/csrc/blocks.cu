@@ -46,10 +46,12 @@ __device__ __forceinline__ float sgn(const BlockArgs& a, int j) {
   return (a.sign_bits[j >> 5] >> (j & 31)) & 1u ? -1.0f : 1.0f;
 }
 
+// code = number of boundaries <= u (ties go up), by binary search over the levels - 1 ascending
+// boundaries (a NaN compares false everywhere: code 0, as the plain count)
 __device__ __forceinline__ int code_of(float u, const float* bnd, int levels) {
   int c = 0;
-#pragma unroll
-  for (int k = 0; k < MAX_LEVELS - 1; ++k) c += (k < levels - 1 && bnd[k] <= u) ? 1 : 0;
+  for (int st = levels >> 1; st >= 1; st >>= 1)
+    if (bnd[c + st - 1] <= u) c += st;
   return c;
 }
 
@@ -74,19 +76,39 @@ __device__ __forceinline__ void hadamard256(float (&v)[8], int lane) {
   }
 }
 
+// this lane's 8 rotation signs (values 8 lane .. 8 lane + 7) as bits
+__device__ __forceinline__ uint32_t lane_signs8(const BlockArgs& a, int lane) {
+  return (a.sign_bits[lane >> 2] >> (8 * (lane & 3))) & 0xffu;
+}
+// v * (+-1): the sign flip is exact, so it equals the multiply
+__device__ __forceinline__ float flip(float v, uint32_t bits, int j) {
+  return __uint_as_float(__float_as_uint(v) ^ (((bits >> j) & 1u) << 31));
+}
+__device__ __forceinline__ void load8(const BlockArgs& a, long long blk, int lane, float (&v)[8]) {
+  const size_t e0 = (size_t)blk * 256 + 8 * lane;
+  const float4 lo = load4_in(a.x, e0, a.in_bf16), hi = load4_in(a.x, e0 + 4, a.in_bf16);
+  v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+  v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+}
+
+// Each warp walks its blocks with the next block's values loaded before the current one is coded.
 __global__ void __launch_bounds__(WARPS * 32) tbq_encode_kernel(const __grid_constant__ BlockArgs a) {
+  __shared__ float sbnd[MAX_LEVELS];
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x < MAX_LEVELS) sbnd[threadIdx.x] = a.bnd[0][threadIdx.x];
+  __syncthreads();
   const int b = a.bits[0], L = a.levels[0];
   const float c = 0.0625f;  // 1/sqrt(256)
-  for (long long blk = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5); blk < a.n_items;
-       blk += (long long)gridDim.x * WARPS) {
+  const uint32_t sb = lane_signs8(a, lane);
+  const long long stride = (long long)gridDim.x * WARPS;
+  long long blk = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+  float nxt[8];
+  if (blk < a.n_items) load8(a, blk, lane, nxt);
+  for (; blk < a.n_items; blk += stride) {
     float v[8];
-    const size_t e0 = (size_t)blk * 256 + 8 * lane;
-    const float4 lo = load4_in(a.x, e0, a.in_bf16), hi = load4_in(a.x, e0 + 4, a.in_bf16);
-    v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
-    v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], sgn(a, 8 * lane + j));
+    for (int j = 0; j < 8; ++j) v[j] = flip(nxt[j], sb, j);
+    if (blk + stride < a.n_items) load8(a, blk + stride, lane, nxt);
     hadamard256(v, lane);
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], c);
@@ -105,7 +127,7 @@ __global__ void __launch_bounds__(WARPS * 32) tbq_encode_kernel(const __grid_con
     const float inv = __fdiv_rn(1.0f, fmaxf(n, FLT_MIN));
     uint32_t field = 0;  // this lane's 8 codes, b bits each, little endian
 #pragma unroll
-    for (int j = 0; j < 8; ++j) field |= (uint32_t)code_of(__fmul_rn(v[j], inv), a.bnd[0], L) << (b * j);
+    for (int j = 0; j < 8; ++j) field |= (uint32_t)code_of(__fmul_rn(v[j], inv), sbnd, L) << (b * j);
     uint8_t* dst = a.rec + (size_t)blk * a.rec_bytes;
     for (int k = 0; k < b; ++k) dst[2 + b * lane + k] = (uint8_t)(field >> (8 * k));
     // the fp16 norm as one 16-bit store (records have even sizes, so it is aligned); written as two
@@ -115,23 +137,38 @@ __global__ void __launch_bounds__(WARPS * 32) tbq_encode_kernel(const __grid_con
 }
 
 __global__ void __launch_bounds__(WARPS * 32) tbq_decode_kernel(const __grid_constant__ BlockArgs a) {
+  __shared__ float scent[MAX_LEVELS];
   const int lane = threadIdx.x & 31;
+  if (threadIdx.x < MAX_LEVELS) scent[threadIdx.x] = __half2float(a.cent[0][threadIdx.x]);
+  __syncthreads();
   const int b = a.bits[0];
+  const uint32_t cmask = (1u << b) - 1u;
   const float c = 0.0625f;
-  for (long long blk = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5); blk < a.n_items;
-       blk += (long long)gridDim.x * WARPS) {
-    const uint8_t* src = a.rec_in + (size_t)blk * a.rec_bytes;
-    uint32_t field = 0;
-    for (int k = 0; k < b; ++k) field |= (uint32_t)src[2 + b * lane + k] << (8 * k);
-    const float n = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(src)));
+  const uint32_t sb = lane_signs8(a, lane);
+  const long long stride = (long long)gridDim.x * WARPS;
+  long long blk = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+  // the record's norm and this lane's code bytes, loaded one block ahead
+  uint32_t field_n = 0, n_n = 0;
+  auto fetch = [&](long long k) {
+    const uint8_t* src = a.rec_in + (size_t)k * a.rec_bytes;
+    uint32_t f = 0;
+    for (int q = 0; q < b; ++q) f |= (uint32_t)__ldg(src + 2 + b * lane + q) << (8 * q);
+    field_n = f;
+    n_n = __ldg(reinterpret_cast<const uint16_t*>(src));
+  };
+  if (blk < a.n_items) fetch(blk);
+  for (; blk < a.n_items; blk += stride) {
+    const uint32_t field = field_n;
+    const float n = __half2float(__ushort_as_half((unsigned short)n_n));
+    if (blk + stride < a.n_items) fetch(blk + stride);
     float v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(n, __half2float(a.cent[0][(field >> (b * j)) & ((1u << b) - 1u)]));
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(n, scent[(field >> (b * j)) & cmask]);
     hadamard256(v, lane);
     float* dst = a.out + (size_t)blk * 256 + 8 * lane;
     float o[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) o[j] = __fmul_rn(__fmul_rn(v[j], c), sgn(a, 8 * lane + j));
+    for (int j = 0; j < 8; ++j) o[j] = flip(__fmul_rn(v[j], c), sb, j);
     reinterpret_cast<float4*>(dst)[0] = make_float4(o[0], o[1], o[2], o[3]);
     reinterpret_cast<float4*>(dst)[1] = make_float4(o[4], o[5], o[6], o[7]);
   }
@@ -178,30 +215,47 @@ __device__ __forceinline__ void build_perm(const int16_t* outl, int16_t* perm, u
   __syncwarp();
 }
 
+// Each warp walks its vectors with the next vector's values gathered before the current one is coded
+// (when it belongs to the same set; at a set boundary they are gathered after the new permutation).
 __global__ void __launch_bounds__(WARPS * 32) split_encode_kernel(const __grid_constant__ BlockArgs a) {
   __shared__ int16_t sperm[WARPS][128];
   __shared__ uint32_t smask[WARPS][4];
   __shared__ uint32_t swords[WARPS][16];
+  __shared__ float sbnd[2][MAX_LEVELS];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  if (threadIdx.x < 2 * MAX_LEVELS) sbnd[threadIdx.x / MAX_LEVELS][threadIdx.x % MAX_LEVELS] = a.bnd[threadIdx.x / MAX_LEVELS][threadIdx.x % MAX_LEVELS];
+  __syncthreads();
   const int s = lane >> 4, i = lane & 15;
   const int b = a.bits[s], L = a.levels[s];
   const int bo = a.bits[0];
+  float sg[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sg[e] = sgn(a, 64 * s + 4 * i + e);
+  const long long stride = (long long)gridDim.x * WARPS;
+  long long vec = (long long)blockIdx.x * WARPS + wl;
   long long cur_set = -1;
-  for (long long vec = (long long)blockIdx.x * WARPS + wl; vec < a.n_items; vec += (long long)gridDim.x * WARPS) {
-    const long long set = vec / a.per_set;
-    if (set != cur_set) {
-      build_perm(a.outliers + set * 64, sperm[wl], smask[wl], lane);
-      cur_set = set;
-    }
-    float v[4];
+  float nxt[4];
+  auto gather = [&](long long k) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int p = 64 * s + 4 * i + e;
-      const size_t idx = (size_t)vec * D + (sperm[wl][p] & 127);  // in range even for a malformed list
-      const float x = a.in_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.x)[idx])
-                                : static_cast<const float*>(a.x)[idx];
-      v[e] = __fmul_rn(x, sgn(a, p));
+      const size_t idx = (size_t)k * D + (sperm[wl][p] & 127);  // in range even for a malformed list
+      nxt[e] = a.in_bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.x)[idx])
+                         : static_cast<const float*>(a.x)[idx];
     }
+  };
+  if (vec < a.n_items) {
+    cur_set = vec / a.per_set;
+    build_perm(a.outliers + cur_set * 64, sperm[wl], smask[wl], lane);
+    gather(vec);
+  }
+  for (; vec < a.n_items; vec += stride) {
+    float v[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(nxt[e], sg[e]);
+    const long long next = vec + stride;
+    const bool next_same = next < a.n_items && next / a.per_set == cur_set;
+    if (next_same) gather(next);
     hadamard64(v, lane);
 #pragma unroll
     for (int e = 0; e < 4; ++e) v[e] = __fmul_rn(v[e], 0.125f);
@@ -217,7 +271,7 @@ __global__ void __launch_bounds__(WARPS * 32) split_encode_kernel(const __grid_c
     const int base = 32 + (s ? 64 * bo : 0) + b * 4 * i;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const uint32_t code = (uint32_t)code_of(__fmul_rn(v[e], inv), a.bnd[s], L);
+      const uint32_t code = (uint32_t)code_of(__fmul_rn(v[e], inv), sbnd[s], L);
       const int bit = base + b * e;
       atomicOr(&swords[wl][bit >> 5], code << (bit & 31));
       if ((bit & 31) + b > 32) atomicOr(&swords[wl][(bit >> 5) + 1], code >> (32 - (bit & 31)));
@@ -230,6 +284,11 @@ __global__ void __launch_bounds__(WARPS * 32) split_encode_kernel(const __grid_c
     uint32_t* dst = reinterpret_cast<uint32_t*>(a.rec + (size_t)vec * a.rec_bytes);
     if (lane < a.rec_bytes / 4) dst[lane] = swords[wl][lane];
     __syncwarp();
+    if (next < a.n_items && !next_same) {
+      cur_set = next / a.per_set;
+      build_perm(a.outliers + cur_set * 64, sperm[wl], smask[wl], lane);
+      gather(next);
+    }
   }
 }
 
@@ -237,20 +296,34 @@ __global__ void __launch_bounds__(WARPS * 32) split_decode_kernel(const __grid_c
   __shared__ int16_t sperm[WARPS][128];
   __shared__ uint32_t smask[WARPS][4];
   __shared__ uint32_t swords[WARPS][16];
+  __shared__ float scent[2][MAX_LEVELS];
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
+  if (threadIdx.x < 2 * MAX_LEVELS)
+    scent[threadIdx.x / MAX_LEVELS][threadIdx.x % MAX_LEVELS] = __half2float(a.cent[threadIdx.x / MAX_LEVELS][threadIdx.x % MAX_LEVELS]);
+  __syncthreads();
   const int s = lane >> 4, i = lane & 15;
   const int b = a.bits[s];
   const int bo = a.bits[0];
+  const int nwords = a.rec_bytes / 4;
+  float sg[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) sg[e] = sgn(a, 64 * s + 4 * i + e);
+  const long long stride = (long long)gridDim.x * WARPS;
+  long long vec = (long long)blockIdx.x * WARPS + wl;
   long long cur_set = -1;
-  for (long long vec = (long long)blockIdx.x * WARPS + wl; vec < a.n_items; vec += (long long)gridDim.x * WARPS) {
+  // this lane's word of the record (lanes < nwords), loaded one vector ahead
+  uint32_t wnext = 0u;
+  if (vec < a.n_items && lane < nwords) wnext = __ldg(reinterpret_cast<const uint32_t*>(a.rec_in + (size_t)vec * a.rec_bytes) + lane);
+  for (; vec < a.n_items; vec += stride) {
     const long long set = vec / a.per_set;
     if (set != cur_set) {
       build_perm(a.outliers + set * 64, sperm[wl], smask[wl], lane);
       cur_set = set;
     }
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(a.rec_in + (size_t)vec * a.rec_bytes);
-    if (lane < a.rec_bytes / 4) swords[wl][lane] = src[lane];
-    if (lane >= a.rec_bytes / 4 && lane < 16) swords[wl][lane] = 0u;
+    if (lane < 16) swords[wl][lane] = lane < nwords ? wnext : 0u;
+    const long long next = vec + stride;
+    if (next < a.n_items && lane < nwords)
+      wnext = __ldg(reinterpret_cast<const uint32_t*>(a.rec_in + (size_t)next * a.rec_bytes) + lane);
     __syncwarp();
     const float n = __half2float(__ushort_as_half((uint16_t)(swords[wl][0] >> (16 * s))));
     const int base = 32 + (s ? 64 * bo : 0) + b * 4 * i;
@@ -260,14 +333,14 @@ __global__ void __launch_bounds__(WARPS * 32) split_decode_kernel(const __grid_c
       const int bit = base + b * e;
       uint32_t w = swords[wl][bit >> 5] >> (bit & 31);
       if ((bit & 31) + b > 32) w |= swords[wl][(bit >> 5) + 1] << (32 - (bit & 31));
-      v[e] = __fmul_rn(n, __half2float(a.cent[s][w & ((1u << b) - 1u)]));
+      v[e] = __fmul_rn(n, scent[s][w & ((1u << b) - 1u)]);
     }
     __syncwarp();
     hadamard64(v, lane);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int p = 64 * s + 4 * i + e;
-      a.out[(size_t)vec * D + (sperm[wl][p] & 127)] = __fmul_rn(__fmul_rn(v[e], 0.125f), sgn(a, p));
+      a.out[(size_t)vec * D + (sperm[wl][p] & 127)] = __fmul_rn(__fmul_rn(v[e], 0.125f), sg[e]);
     }
   }
 }
