@@ -303,14 +303,25 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
     float acc[TQ_VPW][4];
 #pragma unroll
     for (int v = 0; v < TQ_VPW; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
+    // the next quad's projection rows are read while the current quad's are used
+    float4 s4n[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s4n[e] = *reinterpret_cast<const float4*>(sT + e * D + 4 * lane);
 #pragma unroll 2
     for (int jq = 0; jq < D / 4; ++jq) {
+      float4 s4q[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s4q[e] = s4n[e];
+      if (jq + 1 < D / 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s4n[e] = *reinterpret_cast<const float4*>(sT + (4 * jq + 4 + e) * D + 4 * lane);
+      }
       float4 r4[TQ_VPW];
 #pragma unroll
       for (int v = 0; v < TQ_VPW; ++v) r4[v] = *reinterpret_cast<const float4*>(rs + v * D + 4 * jq);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float4 s4 = *reinterpret_cast<const float4*>(sT + (4 * jq + e) * D + 4 * lane);
+        const float4 s4 = s4q[e];
 #pragma unroll
         for (int v = 0; v < TQ_VPW; ++v) {
           const float rj = e == 0 ? r4[v].x : e == 1 ? r4[v].y : e == 2 ? r4[v].z : r4[v].w;
