@@ -210,6 +210,12 @@ def bulk_append_bytes(w, layers, T) -> int:
     return layers * w["batch"] * w["n_kv_heads"] * per_seq_head
 
 
+def launches_per_step(w):
+    """Kernels one timed step launches: the append (TurboQuant keys: a keys kernel and a values
+    kernel; otherwise one kernel for both), then the decode kernel and its merge kernel."""
+    return (2 if w["k_format"] == "tq3_qjl" else 1) + 2
+
+
 def bench_config(name, w, layers, lens, world) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
     cfg = {"workload": name, "layers": layers, "batch": int(w["batch"]),
@@ -628,7 +634,7 @@ def run_gpu(args):
             "roofline": roof,
             "e2e": {"value": weak_scaling_value(tokens_per_rank, world, e2e_ms / args.steps), "unit": "tokens/s",
                     "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_ms / args.steps},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": launches_per_step(w) * args.steps,
             "decode_per_layer_graph": per_layer,
             "clocks": clk.summary(),
             "bulk_append": append_res,
