@@ -230,6 +230,48 @@ constexpr int COST_Q = 16, COST_WIN = 16, COST_UNIT = 32;
 constexpr int COST_MAX_STEP = COST_UNIT + COST_Q;
 constexpr int SPEED_NORMAL = 10, SPEED_FAST = 11;
 
+// ---- the shared-memory arrays behind Seq, filled by the decode kernel's set-up
+// sequence b of (validated) length L: its steps (window chunks first, then quantised half-pages)
+__device__ __forceinline__ void seq_steps(int b, int L, int W, int* sL, int* sNW, int* sS, int* sC) {
+  const int Lq = W > 0 ? max(0, L - W) : L;
+  const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
+  const int nq = (Lq + HALF - 1) / HALF;
+  sL[b] = L;
+  sNW[b] = nw;
+  sS[b] = nw + nq;
+  sC[b] = (nw + nq) > 0 ? COST_UNIT + nw * COST_WIN + nq * COST_Q : 0;
+}
+// warp 0: exclusive prefix sums of the steps and costs of the B sequences, totals at index B
+__device__ __forceinline__ void seq_prefix(int lane, int B, const int* sS, const int* sC, int* sPre, int* sCpre) {
+  const int per = (B + 31) / 32, b0 = lane * per, b1 = min(B, b0 + per);
+  int s = 0, c = 0;
+  for (int b = b0; b < b1; ++b) {
+    s += sS[b];
+    c += sC[b];
+  }
+  int incl = s, cincl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(FULL, incl, o);
+    const int z = __shfl_up_sync(FULL, cincl, o);
+    if (lane >= o) {
+      incl += y;
+      cincl += z;
+    }
+  }
+  int run = incl - s, crun = cincl - c;
+  for (int b = b0; b < b1; ++b) {
+    sPre[b] = run;
+    run += sS[b];
+    sCpre[b] = crun;
+    crun += sC[b];
+  }
+  if (lane == 31) {
+    sPre[B] = incl;
+    sCpre[B] = cincl;
+  }
+}
+
 struct Pos {
   int ll, b, h, local;
 };
@@ -356,6 +398,34 @@ struct Kernel {
                                                  : nwin + (r3 - COST_UNIT - nwin * COST_WIN) / COST_Q;
     if (cost_at(p.ll, p.b, p.h, p.local) < y) advance(p, 1, B, H, sq);
     return p;
+  }
+  // from the per-sequence arrays: the call's steps and costs, and the number of warps with steps
+  __device__ __forceinline__ void totals() {
+    S_layer = (long long)H * sq.pre[B];
+    S = S_layer * a.n_layers_call;
+    C_layer = (long long)H * sq.cpre[B];
+    C = C_layer * a.n_layers_call;
+    nw = 0;
+    if (S > 0) {
+      // every range, even a normal-speed one, must span at least the longest step
+      nw = max(1LL, min((long long)gridDim.x * NCW, C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
+      SPtot = speed_before(nw);
+    }
+  }
+  // the step ranges of this CTA's warps, located once: lane j of the producer warp finds the first
+  // step of consumer warp j, lane NCW that of the next CTA's first warp (this CTA's end)
+  __device__ __forceinline__ void locate(int4* sWpos, long long* sWxs) const {
+    if (warp == NCW && lane <= NCW) {
+      const long long gwj = (long long)blockIdx.x * NCW + lane;
+      Pos p = {0, 0, 0, 0};
+      long long x = S;
+      if (gwj < nw) {
+        p = first_step(gwj);
+        x = step_index(p);
+      }
+      sWpos[lane] = make_int4(p.ll, p.b, p.h, p.local);
+      sWxs[lane] = x;
+    }
   }
   // This thread's share (index i of the grid's NCW * 32 * gridDim consumer threads) of the record
   // ranges of all units, for the merge kernel (a unit of an empty sequence has none)
@@ -1015,32 +1085,57 @@ struct Kernel {
 };
 
 // Combine the partial records of query head hh of unit u (records cf .. cf + nrec - 1, one per
-// warp that streamed part of the unit) in record order and write the head's output.  Latency-bound,
-// so the round trips are few: the unit's record range; then lane j reads both parts' (m, l) of
-// record j (32 records at a time, with running maxima across chunks) and the weights are reduced
-// in registers; then the head's accumulators of every record that holds a part (quantised, window)
-// are requested together, up to MERGE_BATCH per round, and summed per part in record order.  A
-// unit without records (empty sequence) gets zeros.
-constexpr int MERGE_BATCH = 16;
+// warp that streamed part of the unit) in record order and write the head's output.  Latency-bound:
+// a round trip to records just written by other SMs took ~2 us (measured inside the merge), so
+// the reads are issued together: after the unit's record range, one round trip per CHUNK records
+// brings their (m, l) entries (lane j: record j), this lane's channels of their quantised parts
+// and, speculatively, of the window parts of the unit's first MERGE_WIN_SPEC records (a unit's
+// window chunks are its first steps, so the records holding a window part are a prefix of its
+// records).  Records without a part for this head (weight 0) are skipped, whatever their stale
+// contents; a window part further on (a warp range shorter than the window) costs one more round
+// trip.  A unit without records (empty sequence) gets zeros.
+constexpr int MERGE_CHUNK = 16;       // records per round trip of merge_kernel (one warp per head)
+constexpr int WIDE_MERGE_CHUNK = 20;  // of merge_wide_kernel's quantised-part warps
+constexpr int MERGE_WIN_SPEC = 4;     // leading records whose window part is read speculatively
 
-// Merge records cf + r0 .. cf + r1 - 1 of unit u, query head hh, into the running state of both
-// parts (0 = quantised, rotated space; 1 = window): maxima Mk, sums Lk and this lane's channels
-// 4 lane .. +3 of the accumulators O, in record order.
+// Merge records cf + r0 .. cf + r1 - 1 of unit u, query head hh, into the running state of the
+// parts selected (QUANT: 0 = quantised, rotated space; WIN: 1 = window): maxima Mk, sums Lk and this
+// lane's channels 4 lane .. +3 of the accumulators O, in record order.  A window-only merge stops
+// at the first chunk without a window part.
+template <int CHUNK, bool QUANT, bool WIN>
 __device__ __forceinline__ void merge_records(const DecodeArgs& a, int u, int hh, int lane, int cf, int r0, int r1,
                                               float4 (&O)[2], float (&Mk)[2], float (&Lk)[2]) {
-  for (int base = r0; base < r1; base += 32) {
-    // head hh's (m, l) of both parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
+  static_assert(CHUNK <= 32, "one lane per record header");
+  for (int base = r0; base < r1; base += CHUNK) {
+    const int cnt = min(CHUNK, r1 - base);
+    // head hh's (m, l) of the selected parts of record base + lane: header [Qm[4], Ql[4], Wm[4], Wl[4]]
     float hd[4] = {-INFINITY, 0.f, -INFINITY, 0.f};
-    if (base + lane < r1) {
+    if (lane < cnt) {
       const float* hp = record_at(a, u, cf + base + lane);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) hd[i] = __ldcg(hp + 4 * i + hh);
+      for (int i = 0; i < 4; ++i)
+        if (i < 2 ? QUANT : WIN) hd[i] = __ldcg(hp + 4 * i + hh);
     }
-    const int cnt = min(32, r1 - base);
-    float f[2];
-    unsigned act[2];
+    float4 xq[QUANT ? CHUNK : 1], xw[WIN ? MERGE_WIN_SPEC : 1];
+    if (QUANT) {
+#pragma unroll
+      for (int r = 0; r < CHUNK; ++r) {
+        const float* rec = record_at(a, u, cf + base + r) + 16 + hh * D + 4 * lane;
+        xq[r] = r < cnt ? __ldcg(reinterpret_cast<const float4*>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    if (WIN) {
+#pragma unroll
+      for (int r = 0; r < MERGE_WIN_SPEC; ++r) {
+        const float* rec = record_at(a, u, cf + base + r) + 16 + (MAX_GQA + hh) * D + 4 * lane;
+        xw[r] = (base + r < MERGE_WIN_SPEC && r < cnt) ? __ldcg(reinterpret_cast<const float4*>(rec))
+                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float f[2] = {0.f, 0.f};
 #pragma unroll
     for (int k = 0; k < 2; ++k) {  // 0 = quantised part (rotated space), 1 = window part
+      if (!(k == 0 ? QUANT : WIN)) continue;
       const float mv = hd[2 * k], lv = hd[2 * k + 1];
       float m = lv > 0.f ? mv : -INFINITY;
 #pragma unroll
@@ -1055,38 +1150,45 @@ __device__ __forceinline__ void merge_records(const DecodeArgs& a, int u, int hh
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) lw += __shfl_xor_sync(FULL, lw, o);
       Lk[k] += lw;
-      // only records with a part k for this head (a window part is usually in one record)
-      act[k] = __ballot_sync(FULL, f[k] > 0.f && lane < cnt);
     }
-    // entries e = 32 k + j (record j, part k), lowest first: each part's records in order
-    unsigned long long todo = ((unsigned long long)act[1] << 32) | act[0];
-    while (todo) {
-      int e[MERGE_BATCH];
-      float4 x[MERGE_BATCH];
+    if (QUANT) {
 #pragma unroll
-      for (int r = 0; r < MERGE_BATCH; ++r) {
-        e[r] = todo ? __ffsll((long long)todo) - 1 : -1;
-        todo &= todo - 1;
-        const int j = max(e[r], 0) & 31, k = max(e[r], 0) >> 5;
-        const float* rec = record_at(a, u, cf + base + j) + 16 + (k * MAX_GQA + hh) * D + 4 * lane;
-        x[r] = e[r] >= 0 ? __ldcg(reinterpret_cast<const float4*>(rec)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int r = 0; r < MERGE_BATCH; ++r) {
-        const int j = max(e[r], 0) & 31, k = max(e[r], 0) >> 5;
-        const float f0j = __shfl_sync(FULL, f[0], j), f1j = __shfl_sync(FULL, f[1], j);
-        if (e[r] >= 0 && k == 0) {
-          O[0].x += f0j * x[r].x;
-          O[0].y += f0j * x[r].y;
-          O[0].z += f0j * x[r].z;
-          O[0].w += f0j * x[r].w;
-        } else if (e[r] >= 0) {
-          O[1].x += f1j * x[r].x;
-          O[1].y += f1j * x[r].y;
-          O[1].z += f1j * x[r].z;
-          O[1].w += f1j * x[r].w;
+      for (int r = 0; r < CHUNK; ++r) {
+        const float fr = __shfl_sync(FULL, f[0], r);
+        if (fr > 0.f) {
+          O[0].x += fr * xq[r].x;
+          O[0].y += fr * xq[r].y;
+          O[0].z += fr * xq[r].z;
+          O[0].w += fr * xq[r].w;
         }
       }
+    }
+    if (WIN) {
+#pragma unroll
+      for (int r = 0; r < MERGE_WIN_SPEC; ++r) {
+        const float fr = __shfl_sync(FULL, f[1], r);
+        if (base + r < MERGE_WIN_SPEC && fr > 0.f) {
+          O[1].x += fr * xw[r].x;
+          O[1].y += fr * xw[r].y;
+          O[1].z += fr * xw[r].z;
+          O[1].w += fr * xw[r].w;
+        }
+      }
+      // window parts beyond the speculatively read records, in record order
+      unsigned todo = __ballot_sync(FULL, f[1] > 0.f && base + lane >= MERGE_WIN_SPEC);
+      while (todo) {
+        const int j = __ffs(todo) - 1;
+        todo &= todo - 1;
+        const float fr = __shfl_sync(FULL, f[1], j);
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(record_at(a, u, cf + base + j) + 16 +
+                                                                 (MAX_GQA + hh) * D + 4 * lane));
+        O[1].x += fr * x.x;
+        O[1].y += fr * x.y;
+        O[1].z += fr * x.z;
+        O[1].w += fr * x.w;
+      }
+      // the records with a window part are a prefix: done once the chunk's last record has none
+      if (!QUANT && !(__shfl_sync(FULL, hd[3], cnt - 1) > 0.f)) break;
     }
   }
 }
@@ -1139,20 +1241,14 @@ __device__ __forceinline__ void merge_output(const DecodeArgs& a, int u, int hh,
 }
 
 
-// Combine the partial records of query head hh of unit u (records cf .. cf + nrec - 1, one per
-// warp that streamed part of the unit) in record order and write the head's output.  Latency-bound,
-// so the round trips are few: the unit's record range; then lane j reads both parts' (m, l) of
-// record j (32 records at a time, with running maxima across chunks) and the weights are reduced
-// in registers; then the head's accumulators of every record that holds a part (quantised, window)
-// are requested together, up to MERGE_BATCH per round, and summed per part in record order.  A
-// unit without records (empty sequence) gets zeros.
+// The merge of query head hh of unit u by one warp: its record range, then its records (above).
 __device__ void merge_head(const DecodeArgs& a, int u, int hh, int lane) {
   const int2 info = __ldcg(a.unit_info + u);
   float4 sg, sv;
   merge_constants(a, u, lane, sg, sv);
   float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
-  merge_records(a, u, hh, lane, info.x, 0, info.y, O, Mk, Lk);
+  merge_records<MERGE_CHUNK, true, true>(a, u, hh, lane, info.x, 0, info.y, O, Mk, Lk);
   merge_output(a, u, hh, lane, O, Mk, Lk, sg, sv);
 }
 
@@ -1171,8 +1267,10 @@ __global__ void __launch_bounds__(MERGE_WARPS * 32) merge_kernel(const __grid_co
 
 // Calls whose units have many records each (a single layer's decode spread over every warp of
 // the GPU: hundreds of records per unit): one CTA per (unit, query head), its warps merging
-// consecutive slices of the records in parallel; the eight partial states are then combined in
-// slice order by the first warp (a fixed order: deterministic), which writes the output.
+// consecutive slices of the records' quantised parts in parallel (up to WIDE_MERGE_CHUNK records
+// each in one round trip) and the last warp the window parts (a prefix of the records); the first
+// warp then combines the warps' states in warp order (a fixed order: deterministic; lane j holds
+// warp j's maximum and sum, so the weights take one exponential per lane) and writes the output.
 __global__ void __launch_bounds__(WIDE_MERGE_WARPS * 32) merge_wide_kernel(const __grid_constant__ DecodeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1183,11 +1281,16 @@ __global__ void __launch_bounds__(WIDE_MERGE_WARPS * 32) merge_wide_kernel(const
   const int2 info = __ldcg(a.unit_info + u);
   float4 sg, sv;
   if (w == 0) merge_constants(a, u, lane, sg, sv);
-  const int per = (info.y + WIDE_MERGE_WARPS - 1) / WIDE_MERGE_WARPS;
-  const int r0 = min(info.y, w * per), r1 = min(info.y, r0 + per);
   float4 O[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
   float Mk[2] = {-INFINITY, -INFINITY}, Lk[2] = {0.f, 0.f};
-  merge_records(a, u, hh, lane, info.x, r0, r1, O, Mk, Lk);
+  constexpr int NQW = WIDE_MERGE_WARPS - 1;  // warps on the quantised parts
+  if (w < NQW) {
+    const int per = (info.y + NQW - 1) / NQW;
+    const int r0 = min(info.y, w * per), r1 = min(info.y, r0 + per);
+    merge_records<WIDE_MERGE_CHUNK, true, false>(a, u, hh, lane, info.x, r0, r1, O, Mk, Lk);
+  } else {
+    merge_records<MERGE_CHUNK, false, true>(a, u, hh, lane, info.x, 0, info.y, O, Mk, Lk);
+  }
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     sO[w][k][lane] = O[k];
@@ -1198,22 +1301,29 @@ __global__ void __launch_bounds__(WIDE_MERGE_WARPS * 32) merge_wide_kernel(const
   }
   __syncthreads();
   if (w != 0) return;
+  static_assert(WIDE_MERGE_WARPS <= 32, "one lane per slice");
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
-    float M = -INFINITY;
-    for (int j = 0; j < WIDE_MERGE_WARPS; ++j)
-      if (sL[j][k] > 0.f) M = fmaxf(M, sM[j][k]);
+    const float lj = lane < WIDE_MERGE_WARPS ? sL[lane][k] : 0.f;
+    const float mj = lj > 0.f ? sM[lane][k] : -INFINITY;
+    float M = mj;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    const float fj = lj > 0.f ? exp2f(mj - M) : 0.f;
+    float L = lj * fj;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(FULL, L, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
+#pragma unroll
     for (int j = 0; j < WIDE_MERGE_WARPS; ++j) {
-      if (!(sL[j][k] > 0.f)) continue;
-      const float f = exp2f(sM[j][k] - M);
-      const float4 x = sO[j][k][lane];
-      L += sL[j][k] * f;
-      acc.x += f * x.x;
-      acc.y += f * x.y;
-      acc.z += f * x.z;
-      acc.w += f * x.w;
+      const float f = __shfl_sync(FULL, fj, j);
+      if (f > 0.f) {
+        const float4 x = sO[j][k][lane];
+        acc.x += f * x.x;
+        acc.y += f * x.y;
+        acc.z += f * x.z;
+        acc.w += f * x.w;
+      }
     }
     O[k] = acc;
     Mk[k] = M;
@@ -1227,10 +1337,6 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   using GE = Geo<KF>;
   constexpr int NCW = GE::NCW, NSTAGE = GE::NSTAGE, NTHREADS = GE::NTHREADS;
   extern __shared__ __align__(1024) uint8_t smem[];
-  // launched as a programmatic dependent: the previous kernel of the stream may still be running
-  // and writing the inputs (the cache, q, lengths); wait for it before reading any of them.  (No
-  // early trigger for the merge kernel: its CTAs, resident early, slowed the streaming warps.)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   Kernel<KF> K(a, smem);
   const int tid = threadIdx.x;
   K.warp = tid >> 5;
@@ -1251,86 +1357,86 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + GE::SM_BARS);
   uint64_t* empty = full + NSTAGE;
   int4* desc = reinterpret_cast<int4*>(smem + GE::SM_DESC);
-
-  // the TQ3 decode table (2 KB in the cache header) is read once per CTA into the first stage, and
-  // expanded to its per-lane copies after the barrier below (the stages are idle until then)
-  if (KF == KVQ_TQ3_QJL && tid < 256)
-    reinterpret_cast<uint2*>(smem + GE::SM_STAGES)[tid] = a.p.cb->lut8[tid];
-  // ---- per-sequence step counts: window chunks first, then quantised half-pages
-  for (int b = tid; b < B; b += NTHREADS) {
-    int L = a.seq_lens[b];
-    if (L < 0 || L > a.max_seq_len) {
-      if (blockIdx.x == 0) atomicOr(a.p.status, KVQ_DEV_SEQLEN_RANGE);
-      L = 0;
-    }
-    const int Lq = W > 0 ? max(0, L - W) : L;
-    const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
-    const int nq = (Lq + HALF - 1) / HALF;
-    sL[b] = L;
-    sNW[b] = nw;
-    sS[b] = nw + nq;
-    sC[b] = (nw + nq) > 0 ? COST_UNIT + nw * COST_WIN + nq * COST_Q : 0;
-  }
-  __syncthreads();
-  if (K.warp == 0) {
-    const int lane = K.lane;
-    const int per = (B + 31) / 32, b0 = lane * per, b1 = min(B, b0 + per);
-    int s = 0, c = 0;
-    for (int b = b0; b < b1; ++b) {
-      s += sS[b];
-      c += sC[b];
-    }
-    int incl = s, cincl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULL, incl, o);
-      const int z = __shfl_up_sync(FULL, cincl, o);
-      if (lane >= o) {
-        incl += y;
-        cincl += z;
-      }
-    }
-    int run = incl - s, crun = cincl - c;
-    for (int b = b0; b < b1; ++b) {
-      sPre[b] = run;
-      run += sS[b];
-      sCpre[b] = crun;
-      crun += sC[b];
-    }
-    if (lane == 31) {
-      sPre[B] = incl;
-      sCpre[B] = cincl;
-    }
-  }
-  if (tid >= 32 && tid < 32 + 2 * NSTAGE) {
-    // one barrier per thread of warps 1-2 (full[NSTAGE] then empty[NSTAGE], contiguous)
-    mbar_init(full + (tid - 32), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  if (KF == KVQ_TQ3_QJL) {
-    // entry v: 32 lane copies of its centroid pair, then 32 lane copies of its sign pair
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(smem + GE::SM_STAGES);
-    uint32_t* lut = reinterpret_cast<uint32_t*>(smem + GE::SM_LUT);
-    for (int idx = tid; idx < 256 * 64; idx += NTHREADS) lut[idx] = src[2 * (idx >> 6) + ((idx >> 5) & 1)];
-  }
-  __syncthreads();
+  int4* sWpos = reinterpret_cast<int4*>(smem + GE::SM_WPOS);
+  long long* sWxs = reinterpret_cast<long long*>(smem + GE::SM_WPOS + (NCW + 1) * 16);
   K.sq.S = sS;
   K.sq.pre = sPre;
   K.sq.L = sL;
   K.sq.NW = sNW;
   K.sq.C = sC;
   K.sq.cpre = sCpre;
-
-  K.S_layer = (long long)H * sPre[B];
-  K.S = K.S_layer * a.n_layers_call;
-  K.C_layer = (long long)H * sCpre[B];
-  K.C = K.C_layer * a.n_layers_call;
-  if (K.S > 0) {
-    // every range, even a normal-speed one, must span at least the longest step
-    K.nw = max(1LL, min((long long)gridDim.x * NCW, K.C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
-    K.SPtot = K.speed_before(K.nw);
+  // Launched as a programmatic dependent: the previous kernel of the stream may still be running
+  // and writing the inputs (the cache, q, the lengths).  Q4G32 and Q8G32 keys: the split of the
+  // work is computed before waiting for it, from the lengths as they stand (read through L2, never
+  // cached in L1); after the wait the lengths are read again and the split recomputed if any
+  // changed.  Nothing else of the inputs is read, and nothing is written outside shared memory,
+  // before the wait.  TQ3 keys wait first: with the early split their consumers' code came out
+  // 0.4-0.8 % slower (measured), more than the split saves on an all-layer call.  (No early
+  // trigger for the merge kernel: its CTAs, resident early, slowed the streaming warps.)
+  if constexpr (KF == KVQ_TQ3_QJL) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the TQ3 decode table (2 KB in the cache header) is read once per CTA into the first stage,
+    // and expanded to its per-lane copies after the barrier below (the stages are idle until then)
+    if (tid < 256) reinterpret_cast<uint2*>(smem + GE::SM_STAGES)[tid] = a.p.cb->lut8[tid];
+    for (int b = tid; b < B; b += NTHREADS) {
+      int L = a.seq_lens[b];
+      if (L < 0 || L > a.max_seq_len) {
+        if (blockIdx.x == 0) atomicOr(a.p.status, KVQ_DEV_SEQLEN_RANGE);
+        L = 0;
+      }
+      seq_steps(b, L, W, sL, sNW, sS, sC);
+    }
+    __syncthreads();
+    if (K.warp == 0) seq_prefix(K.lane, B, sS, sC, sPre, sCpre);
+    if (tid >= 32 && tid < 32 + 2 * NSTAGE) {
+      // one barrier per thread of warps 1-2 (full[NSTAGE] then empty[NSTAGE], contiguous)
+      mbar_init(full + (tid - 32), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    {
+      // entry v: 32 lane copies of its centroid pair, then 32 lane copies of its sign pair
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(smem + GE::SM_STAGES);
+      uint32_t* lut = reinterpret_cast<uint32_t*>(smem + GE::SM_LUT);
+      for (int idx = tid; idx < 256 * 64; idx += NTHREADS) lut[idx] = src[2 * (idx >> 6) + ((idx >> 5) & 1)];
+    }
+    __syncthreads();
+    K.totals();
+    if (K.S == 0 || (long long)blockIdx.x * NCW >= K.nw) {
+      if (tid < NCW * 32) K.unit_info_share((long long)tid * gridDim.x + blockIdx.x);
+      return;
+    }
+    K.locate(sWpos, sWxs);
+  } else {
+    if (tid >= 32 && tid < 32 + 2 * NSTAGE) {
+      mbar_init(full + (tid - 32), 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    // pass 0 (before the wait) computes the split silently; pass 1 (after it) reads the lengths
+    // again, reports bad ones, and recomputes the split only if one changed
+    for (int pass = 0; pass < 2; ++pass) {
+      if (pass == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+      bool changed = false;
+      for (int b = tid; b < B; b += NTHREADS) {
+        int L = __ldcg(a.seq_lens + b);
+        if (L < 0 || L > a.max_seq_len) {
+          if (pass == 1 && blockIdx.x == 0) atomicOr(a.p.status, KVQ_DEV_SEQLEN_RANGE);
+          L = 0;
+        }
+        if (pass == 0 || L != sL[b]) {
+          changed = true;
+          seq_steps(b, L, W, sL, sNW, sS, sC);
+        }
+      }
+      if (!__syncthreads_or(changed)) continue;
+      if (K.warp == 0) seq_prefix(K.lane, B, sS, sC, sPre, sCpre);
+      __syncthreads();
+      K.totals();
+      if (K.S > 0 && (long long)blockIdx.x * NCW < K.nw) K.locate(sWpos, sWxs);
+    }
   }
+  __syncthreads();
   // the record ranges of all units, for the merge kernel: a share per consumer thread of the grid,
   // computed by warps with steps once their first copies are in flight
   const long long info_i = (long long)tid * gridDim.x + blockIdx.x;
@@ -1338,23 +1444,6 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
     if (tid < NCW * 32) K.unit_info_share(info_i);
     return;
   }
-
-  // ---- the step ranges of this CTA's warps, located once: lane j of the producer warp finds the
-  // first step of consumer warp j, lane NCW that of the next CTA's first warp (this CTA's end)
-  int4* sWpos = reinterpret_cast<int4*>(smem + GE::SM_WPOS);
-  long long* sWxs = reinterpret_cast<long long*>(smem + GE::SM_WPOS + (NCW + 1) * 16);
-  if (K.warp == NCW && K.lane <= NCW) {
-    const long long gwj = (long long)blockIdx.x * NCW + K.lane;
-    Pos p = {0, 0, 0, 0};
-    long long x = K.S;
-    if (gwj < K.nw) {
-      p = K.first_step(gwj);
-      x = K.step_index(p);
-    }
-    sWpos[K.lane] = make_int4(p.ll, p.b, p.h, p.local);
-    sWxs[K.lane] = x;
-  }
-  __syncthreads();
 
   if (K.warp == NCW) {
     // ======================= producer: lane w streams consumer warp w's contiguous step range.
