@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -169,6 +170,10 @@ static int check_device(const kvq_cache* c) {
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
   return dev == c->device ? KVQ_OK : KVQ_ERR_INVALID_ARG;
 }
+
+// give-up limit of the decode pipeline's waits (kv_set_wait_limit_ns)
+std::atomic<unsigned long long> g_decode_wait_ns{1000000000ull};
+unsigned long long decode_wait_ns() { return g_decode_wait_ns.load(); }
 
 int decode_ctas(int device) {
   int sms = 0;
@@ -350,6 +355,7 @@ int kv_decode_attention(kvq_cache* cache, int32_t layer, const void* q, float* o
   a.identity_pages = cache->block_table == reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(cache->dev) + L.off_bt);
   a.n_units = n_units;
   a.n_ctas = ctas;
+  a.wait_ns = decode_wait_ns();
   return cuda_err(launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -434,6 +440,12 @@ int kv_status(kvq_cache* cache, uint32_t* flags, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return KVQ_ERR_CUDA;
   *flags = v;
+  return KVQ_OK;
+}
+
+int kv_set_wait_limit_ns(uint64_t ns) {
+  if (ns < 1 || ns > 10000000000ull) return KVQ_ERR_INVALID_ARG;
+  g_decode_wait_ns.store(ns);
   return KVQ_OK;
 }
 

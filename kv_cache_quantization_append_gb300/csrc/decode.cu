@@ -1511,7 +1511,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
       } else {
         const unsigned long long now = globaltimer();
         if (t_idle == 0) t_idle = now;
-        if (__any_sync(FULL, now - t_idle > WAIT_NS)) {
+        if (__any_sync(FULL, now - t_idle > a.wait_ns)) {
           if (w == 0) atomicOr(a.p.status, KVQ_DEV_TIMEOUT);
           break;
         }

@@ -99,8 +99,10 @@ struct DecodeArgs {
   int layer0, n_layers_call, batch, max_batch, Hkv, g, W, max_seq_len, k_format, sinkhorn, in_bf16;
   int max_pages_per_seq, n_units, n_ctas;
   int identity_pages;  // block_table is the cache's own identity table (page p of sequence b = b * max_pages_per_seq + p)
+  unsigned long long wait_ns;  // give-up limit of the producer warps' wait for a released stage
 };
 int decode_ctas(int device);
+unsigned long long decode_wait_ns();
 size_t decode_scratch_bytes(int n_units, int n_ctas, int k_format);
 size_t decode_record_slots(int n_units, int n_ctas, int k_format);
 int decode_consumer_warps(int k_format);

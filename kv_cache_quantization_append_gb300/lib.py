@@ -33,7 +33,8 @@ EXPORTS = ("kv_cache_bytes", "kv_cache_init", "kv_calibrate_scratch_bytes", "kv_
            "kv_quant_append", "kv_decode_scratch_bytes", "kv_decode_attention",
            "kv_decode_attention_noalloc", "kv_prefill_scratch_bytes", "kv_prefill_attention",
            "kv_tbq_block_bytes", "kv_tbq_encode", "kv_tbq_decode", "kv_split_record_bytes",
-           "kv_split_outliers", "kv_split_encode", "kv_split_decode", "kv_status", "kv_strerror")
+           "kv_split_outliers", "kv_split_encode", "kv_split_decode", "kv_status", "kv_set_wait_limit_ns",
+           "kv_strerror")
 NOALLOC_SCRATCH_MAX = 32 * 1024 * 1024
 
 
@@ -90,6 +91,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "kv_split_encode": (ctypes.c_int, [I32, ctypes.c_uint64, P, I32, P, I32, ctypes.c_int64, P, P]),
         "kv_split_decode": (ctypes.c_int, [I32, ctypes.c_uint64, P, I32, P, ctypes.c_int64, P, P]),
         "kv_status": (ctypes.c_int, [cachep, U32P, P]),
+        "kv_set_wait_limit_ns": (ctypes.c_int, [ctypes.c_uint64]),
         "kv_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
@@ -332,6 +334,11 @@ def kv_status(cache: kvq_cache, stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check(load().kv_status(ctypes.byref(cache), ctypes.byref(v), _stream(stream)))
     return int(v.value)
+
+
+def kv_set_wait_limit_ns(ns: int) -> None:
+    """Give-up limit (ns, 1..1e10) of later decode calls' producer waits; the default is 1e9."""
+    _check(load().kv_set_wait_limit_ns(int(ns)))
 
 
 def kv_strerror(code: int) -> str:

@@ -273,3 +273,10 @@ def test_append_binding_refuses_mismatched_shapes():
     for layer, k, v, p in cases:
         with pytest.raises(lib.KVQError, match="shape|must be"):
             lib.kv_quant_append(c, layer, k, v, p)
+
+
+def test_wait_limit_range_is_checked(kvq):
+    """kv_set_wait_limit_ns refuses 0 and limits above 10 s (no device work either way)."""
+    assert kvq.kv_set_wait_limit_ns(0) == 1                 # KVQ_ERR_INVALID_ARG
+    assert kvq.kv_set_wait_limit_ns(10**10 + 1) == 1
+    assert kvq.kv_set_wait_limit_ns(10**9) == 0             # the default, restored
