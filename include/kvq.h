@@ -332,16 +332,15 @@ int kv_split_decode(int32_t hi_bits, uint64_t seed, const int16_t* outliers, int
 /* Read and clear the device status word (synchronises ``stream``); *flags gets KVQ_DEV_* bits. */
 int kv_status(kvq_cache* cache, uint32_t* flags, void* stream);
 
-/* Diagnostics: the give-up limit, in nanoseconds, of the decode copy pipeline's producer wait (a
- * producer warp waiting for its consumers to release a stage) for every later kv_decode_attention /
- * _noalloc call of this process.  Default 1e9 (~1 s); ns must lie in [1, 1e10], else
- * KVQ_ERR_INVALID_ARG and the limit is unchanged.  A producer whose wait runs out stops issuing
- * copies and sets KVQ_DEV_TIMEOUT in the status word; its consumers then give up on the stages that
- * never come after their own ~1 s limit, and the call's output is incomplete.  The streaming kernel
- * still waits for every copy it started before its blocks exit, so the device stays usable.  Meant
- * for tests of that give-up path (with a limit of a few nanoseconds a producer gives up at its first
- * idle moment; the call then takes ~1 s); the prefill and append kernels keep their own ~1 s
- * limits.  Not thread-safe against concurrent decode launches from other host threads. */
+/* The stall limit, in nanoseconds, of the decode copy pipeline's producer wait (a producer warp
+ * waiting for its consumers to release a stage) for every later kv_decode_attention / _noalloc
+ * call of this process: a serving loop can tighten the ~1 s default to detect a stalled decode
+ * sooner.  ns must lie in [1, 1e10], else KVQ_ERR_INVALID_ARG and the limit is unchanged.  A
+ * producer whose wait runs out stops issuing copies and sets KVQ_DEV_TIMEOUT in the status word
+ * (the call's output is then incomplete); its consumers give up on the stages that never come after
+ * their own ~1 s limit, and the streaming kernel still waits for every copy it started before its
+ * blocks exit.  The prefill and append kernels keep their own ~1 s limits.  Not thread-safe against
+ * concurrent decode launches from other host threads. */
 int kv_set_wait_limit_ns(uint64_t ns);
 
 /* Static string for a KVQ_* status code. */

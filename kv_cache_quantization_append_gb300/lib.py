@@ -337,7 +337,7 @@ def kv_status(cache: kvq_cache, stream=None) -> int:
 
 
 def kv_set_wait_limit_ns(ns: int) -> None:
-    """Give-up limit (ns, 1..1e10) of later decode calls' producer waits; the default is 1e9."""
+    """Stall limit (ns, 1..1e10) of later decode calls' producer waits; the default is 1e9."""
     _check(load().kv_set_wait_limit_ns(int(ns)))
 
 
