@@ -10,8 +10,9 @@ over every layer (one streaming launch over all layers, then a small launch that
 partial softmax states).  Every cache is larger than L2, so every step streams it from HBM.
 
 Prints one JSON line.  ``value`` = cached tokens attended per second, device-timed with CUDA events
-over K steps on resident inputs; ``e2e`` = the same through the public API with the step's inputs
-copied from pinned host memory and the output copied back inside the timed region.  ``roofline``
+over K steps on resident inputs; ``e2e`` = the same through the public API with every step's inputs
+copied from pinned host memory and its output copied back inside the timed region (the copies on
+their own streams, overlapping the neighbouring steps' compute as a serving loop would).  ``roofline``
 is the decode call alone, timed over at least one second of back-to-back calls.  ``workloads``
 carries the same decode roofline, the per-layer call form and the bulk (prefill-sized) append for
 the other large configurations (Llama-3.2-3B at 32K, Qwen3-4B KVarN at 128K, the ragged 27B-class
@@ -587,30 +588,62 @@ def run_gpu(args):
                      "launches_per_step": 2 * layers, "vs_all_layer_call": g_s * 1e6 / dec_us,
                      "tokens_per_s": weak_scaling_value(float(lens.sum()), world, g_s * 1e3)}
 
-    # end-to-end through the public API: host inputs in, host output out, every step
+    # end-to-end through the public API: host inputs in, host output out, every step.  The copies
+    # run on their own streams (one per direction, double-buffered device inputs and outputs), so
+    # that step i+1's inputs land and step i's output leaves while the GPU computes: the pipeline a
+    # serving loop runs.  Every step's copies are inside the timed region.
     q_h = [q.cpu().pin_memory() for q in qs]
     k_h, v_h = knew.cpu().pin_memory(), vnew.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=torch.float32).pin_memory()
-    q_d = torch.empty_like(qs[0])
-    k_d, v_d = torch.empty_like(knew), torch.empty_like(vnew)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for i in range(args.warmup):
-        q_d.copy_(q_h[i % nbuf], non_blocking=True)
+    out_h = [torch.empty(out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    q_d = [torch.empty_like(qs[0]) for _ in range(2)]
+    k_d, v_d = [torch.empty_like(knew) for _ in range(2)], [torch.empty_like(vnew) for _ in range(2)]
+    out_d = [torch.empty_like(out) for _ in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # buffer j's inputs landed
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # the step using buffer j finished computing
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # buffer j's output copied out
+
+    def run_e2e(n, start_event=None):
+        def h2d(i):
+            j = i % 2
+            with torch.cuda.stream(h2d_s):
+                if i >= 2:
+                    h2d_s.wait_event(ev_done[j])       # the step that used buffer j has read it
+                q_d[j].copy_(q_h[i % nbuf], non_blocking=True)
+                k_d[j].copy_(k_h, non_blocking=True)
+                v_d[j].copy_(v_h, non_blocking=True)
+                ev_in[j].record(h2d_s)
+        if start_event is not None:
+            h2d_s.wait_event(start_event)
+        h2d(0)
+        for i in range(n):
+            j = i % 2
+            if i + 1 < n:
+                h2d(i + 1)
+            stream.wait_event(ev_in[j])
+            if i >= 2:
+                stream.wait_event(ev_out[j])           # out_d[j] of step i-2 has been copied out
+            cache.append(-1, k_d[j], v_d[j], pos)
+            cache.decode(-1, q_d[j], seq, out_d[j])
+            ev_done[j].record(stream)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(ev_done[j])
+                out_h[j].copy_(out_d[j], non_blocking=True)
+                ev_out[j].record(d2h_s)
+        stream.wait_stream(h2d_s)
+        stream.wait_stream(d2h_s)
+
+    run_e2e(args.warmup)
     torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
-        q_d.copy_(q_h[i % nbuf], non_blocking=True)
-        k_d.copy_(k_h, non_blocking=True)
-        v_d.copy_(v_h, non_blocking=True)
-        cache.append(-1, k_d, v_d, pos)
-        cache.decode(-1, q_d, seq, out)
-        out_h.copy_(out, non_blocking=True)
+    run_e2e(args.steps, e0)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
 
     h2d_bytes = int(q_h[0].numel() * q_h[0].element_size() + 2 * knew.numel() * knew.element_size())
-    d2h_bytes = int(out_h.numel() * 4)
+    d2h_bytes = int(out_h[0].numel() * 4)
     peak, peak_src = hbm_peak()
     append_res = time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src)
     prefill_res = time_prefill(args.workload, cache, w, layers, lens, dev, stream)
