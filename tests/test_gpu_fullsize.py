@@ -5,7 +5,7 @@ seeded inputs, the same block table for the paged workload), the newest token of
 appended and one decode launch covers all layers.  A few (layer, sequence, kv-head) units are then
 recomputed by the CPU oracle from the same inputs: every stored code, scale, zero, norm, sign bit,
 Sinkhorn scale and ring value of the unit must match bit for bit, and its attention outputs must be
-within 2e-3 of the oracle's max |out|.
+within 2e-3 of the oracle's max |out|, from the all-layer call and from a per-layer call alike.
 """
 
 import numpy as np
@@ -59,6 +59,8 @@ def test_full_size_sampled_units(gpu_lib, name):
     assert cache.status() == 0
     bt = None if cache.block_table is None else cache.block_table.cpu().numpy()
     proj = synth.qjl_projection(w["qjl_seed"]) if w["k_format"] == "tq3_qjl" else None
+    lens_t = torch.as_tensor(lens.astype(np.int32), device="cuda")
+    per_layer = {}  # layer -> output of a per-layer decode call
     for (layer, b, h) in SAMPLES[name]:
         L = int(lens[b])
         ocfg = attention.OracleConfig(n_layers=1, n_kv_heads=1, n_q_heads=g, max_batch=1, max_seq_len=L,
@@ -95,6 +97,14 @@ def test_full_size_sampled_units(gpu_lib, name):
         qg = harness.to_np(q[layer, b, h * g:(h + 1) * g])
         want = ora.decode_unit(0, 0, 0, qg, L)
         rel = harness.assert_attention_close(harness.to_np(out[layer, b, h * g:(h + 1) * g]), want)
-        print(f"{name} unit ({layer}, {b}, {h}) L={L}: max|err| / max|out| = {rel:.2e}")
+        # the same unit through a per-layer call (one layer's units spread over the whole grid: the
+        # CTA-per-head merge for the single-sequence workloads)
+        if layer not in per_layer:
+            per_layer[layer] = cache.decode(layer, q[layer].contiguous(), lens_t)
+            torch.cuda.synchronize()
+            assert cache.status() == 0
+        rel_l = harness.assert_attention_close(harness.to_np(per_layer[layer][b, h * g:(h + 1) * g]), want)
+        print(f"{name} unit ({layer}, {b}, {h}) L={L}: max|err| / max|out| = {rel:.2e} "
+              f"(per-layer call {rel_l:.2e})")
     del cache
     torch.cuda.empty_cache()
