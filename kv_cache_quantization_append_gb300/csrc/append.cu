@@ -200,7 +200,8 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
 // residual: bit i = (t_i >= 0), t_i = sum over j = 0..127 in order of RN(S[i][j] * r_j).  The
 // projection (128 x 128 separately rounded multiplies and adds per vector, in that order, so the
 // signs are reproducible bit for bit) is the cost: the transposed projection is staged in shared
-// memory once per CTA and every warp streams TQ_VPW vectors through it, the residuals read as
+// memory once per CTA and every warp streams TQ_VPW vectors (one, for appends of fewer tokens per
+// sequence) through it, the residuals read as
 // broadcast shared-memory words, the products and sums as packed f32x2 operations (each half
 // rounded like the scalar operation).
 constexpr int TQ_WARPS = 8;
@@ -255,17 +256,30 @@ __device__ __forceinline__ TqKey tq_key_prepare(const AppendArgs& a, int lane, i
   return k;
 }
 
+template <int VPW>
 __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const AppendArgs a) {
   extern __shared__ __align__(16) float tq_smem[];
   const float* sT = tq_smem;  // [j][i] = S[i][j]
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
-  float* rs = tq_smem + D * D + wl * TQ_VPW * D;  // this warp's residuals [TQ_VPW][128]
+  float* rs = tq_smem + D * D + wl * TQ_VPW * D;  // this warp's residuals [VPW][128]
   // a dependent decode launch may start its set-up now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;");
-  for (int i = threadIdx.x; i < D * D / 4; i += TQ_WARPS * 32)
-    reinterpret_cast<float4*>(tq_smem)[i] = reinterpret_cast<const float4*>(a.p.qjl_t)[i];
+  // the transposed projection, 64 KB: each thread's 16 rows of 16 bytes requested 8 at a time
+  // before any is stored (one at a time, the loads were 16 dependent round trips: most of a
+  // one-token append)
+  constexpr int STAGE_N = D * D / 4 / (TQ_WARPS * 32), STAGE_BATCH = 8;
+  static_assert(STAGE_N % STAGE_BATCH == 0, "whole batches");
+#pragma unroll 1
+  for (int r0 = 0; r0 < STAGE_N; r0 += STAGE_BATCH) {
+    float4 t[STAGE_BATCH];
+#pragma unroll
+    for (int r = 0; r < STAGE_BATCH; ++r)
+      t[r] = reinterpret_cast<const float4*>(a.p.qjl_t)[threadIdx.x + (r0 + r) * TQ_WARPS * 32];
+#pragma unroll
+    for (int r = 0; r < STAGE_BATCH; ++r) reinterpret_cast<float4*>(tq_smem)[threadIdx.x + (r0 + r) * TQ_WARPS * 32] = t[r];
+  }
   __syncthreads();
-  const int nq = (a.T + TQ_VPW - 1) / TQ_VPW;
+  const int nq = (a.T + VPW - 1) / VPW;
   const unsigned total = (unsigned)a.n_layers_call * a.batch * a.Hkv * nq;
   for (unsigned wid = blockIdx.x * TQ_WARPS + wl; wid < total; wid += gridDim.x * TQ_WARPS) {
     const int tq = (int)(wid % nq);
@@ -281,16 +295,16 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
       if (lane == 0 && tq == 0 && h == 0) atomicOr(a.p.status, KVQ_DEV_POS_RANGE);
       continue;
     }
-    const int t0 = tq * TQ_VPW;
-    const int nv = min(TQ_VPW, a.T - t0);
+    const int t0 = tq * VPW;
+    const int nv = min(VPW, a.T - t0);
     const size_t vec0 = (((size_t)ll * a.batch + b) * a.Hkv + h) * a.T + t0;
-    float4 x[TQ_VPW];
+    float4 x[VPW];
 #pragma unroll
-    for (int v = 0; v < TQ_VPW; ++v)
+    for (int v = 0; v < VPW; ++v)
       if (v < nv) x[v] = load4_in(a.k, (vec0 + v) * D + 4 * lane, a.in_bf16);
-    TqKey key[TQ_VPW];
+    TqKey key[VPW];
 #pragma unroll
-    for (int v = 0; v < TQ_VPW; ++v) {
+    for (int v = 0; v < VPW; ++v) {
       if (v < nv) {
         key[v] = tq_key_prepare(a, lane, layer, b, h, t0 + v, p0 + t0 + v, x[v], rs + v * D);
       } else {
@@ -300,9 +314,9 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
     }
     __syncwarp();
     // t_i for i = 4 lane + e, e = 0..3, of each vector: pairs (0, 1) and (2, 3) packed
-    float acc[TQ_VPW][4];
+    float acc[VPW][4];
 #pragma unroll
-    for (int v = 0; v < TQ_VPW; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
+    for (int v = 0; v < VPW; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
     // the next quad's projection rows are read while the current quad's are used
     float4 s4n[4];
 #pragma unroll
@@ -316,14 +330,14 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
 #pragma unroll
         for (int e = 0; e < 4; ++e) s4n[e] = *reinterpret_cast<const float4*>(sT + (4 * jq + 4 + e) * D + 4 * lane);
       }
-      float4 r4[TQ_VPW];
+      float4 r4[VPW];
 #pragma unroll
-      for (int v = 0; v < TQ_VPW; ++v) r4[v] = *reinterpret_cast<const float4*>(rs + v * D + 4 * jq);
+      for (int v = 0; v < VPW; ++v) r4[v] = *reinterpret_cast<const float4*>(rs + v * D + 4 * jq);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float4 s4 = s4q[e];
 #pragma unroll
-        for (int v = 0; v < TQ_VPW; ++v) {
+        for (int v = 0; v < VPW; ++v) {
           const float rj = e == 0 ? r4[v].x : e == 1 ? r4[v].y : e == 2 ? r4[v].z : r4[v].w;
           float p0v = s4.x, p1v = s4.y, p2v = s4.z, p3v = s4.w;
           mul2(p0v, p1v, rj, rj);
@@ -336,7 +350,7 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
     // record byte 2 lane + e holds the codes of channels 4 lane + 2e, +1 (bits 0-2, 3-5) and the
     // sign bits of projections 4 lane + 2e, +1 (bits 6, 7): this lane's halfword
 #pragma unroll
-    for (int v = 0; v < TQ_VPW; ++v) {
+    for (int v = 0; v < VPW; ++v) {
       if (key[v].pg == nullptr) continue;
       uint32_t hw = 0;
 #pragma unroll
@@ -367,19 +381,25 @@ cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_append_tq_keys(const AppendArgs& a, cudaStream_t s) {
-  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + TQ_VPW - 1) / TQ_VPW);
+  // a warp projects TQ_VPW vectors of a sequence at a time; appends of fewer tokens per sequence
+  // (the decode step's one token) one vector per warp, so that no lane computes empty slots
+  const int vpw = a.T >= TQ_VPW ? TQ_VPW : 1;
+  const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + vpw - 1) / vpw);
   if (warps <= 0) return cudaSuccess;
   if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(append_tq_keys_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TQ_SMEM);
+    e = cudaFuncSetAttribute(vpw == TQ_VPW ? (const void*)append_tq_keys_kernel<TQ_VPW> : (const void*)append_tq_keys_kernel<1>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)TQ_SMEM);
   if (e != cudaSuccess) return e;
   // the projection is loaded once per CTA: at most two CTAs per SM, each looping over warp groups
   const long long want = (warps + TQ_WARPS - 1) / TQ_WARPS;
   const long long cap = 2LL * (sms > 0 ? sms : 1);
-  append_tq_keys_kernel<<<(unsigned)(want < cap ? want : cap), TQ_WARPS * 32, TQ_SMEM, s>>>(a);
+  const unsigned grid = (unsigned)(want < cap ? want : cap);
+  if (vpw == TQ_VPW) append_tq_keys_kernel<TQ_VPW><<<grid, TQ_WARPS * 32, TQ_SMEM, s>>>(a);
+  else append_tq_keys_kernel<1><<<grid, TQ_WARPS * 32, TQ_SMEM, s>>>(a);
   return cudaGetLastError();
 }
 
