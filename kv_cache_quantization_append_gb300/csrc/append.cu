@@ -158,7 +158,7 @@ __device__ __forceinline__ void encode_vector(const AppendArgs& a, int lane, int
   }
 }
 
-__global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
+__device__ __forceinline__ void append_warps_body(const AppendArgs& a) {
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   // a dependent decode launch may start its set-up now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;");
@@ -193,6 +193,14 @@ __global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) 
 #pragma unroll
   for (int j = 0; j < VPW; ++j)
     if (j < nv) encode_vector(a, lane, kv, layer, b, h, t0 + j, p0 + t0 + j, x[j]);
+}
+
+// As append_bulk_kernel: launched for the values of a TurboQuant-key append (AFTER_KEYS) as a
+// programmatic dependent of the keys kernel, every thread waits for the keys grid before exiting.
+template <bool AFTER_KEYS>
+__global__ void __launch_bounds__(WARPS * 32) append_kernel(const AppendArgs a) {
+  append_warps_body(a);
+  if (AFTER_KEYS) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- TurboQuant keys
@@ -371,13 +379,21 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
 
 }  // namespace
 
-cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s) {
+cudaError_t launch_append_warps(const AppendArgs& a, cudaStream_t s, bool after_keys) {
   const long long warps = (long long)a.n_layers_call * a.batch * a.Hkv * ((a.T + VPW - 1) / VPW) * a.kv_n;
   const long long blocks = (warps + WARPS - 1) / WARPS;
   if (blocks <= 0) return cudaSuccess;
   if (warps > 0x7fffffffLL) return cudaErrorInvalidValue;
-  append_kernel<<<(unsigned)blocks, WARPS * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(WARPS * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_keys ? 1 : 0;
+  return after_keys ? cudaLaunchKernelEx(&cfg, append_kernel<true>, a) : cudaLaunchKernelEx(&cfg, append_kernel<false>, a);
 }
 
 cudaError_t launch_append_tq_keys(const AppendArgs& a, cudaStream_t s) {
@@ -417,22 +433,22 @@ cudaError_t launch_append(const AppendArgs& a0, cudaStream_t s) {
       if (e != cudaSuccess) return e;
       a.kv_lo = 1;
       a.kv_n = 1;
-      return launch_append_warps(a, s);
+      return launch_append_warps(a, s, true);
     }
     a.kv_lo = 0;
     a.kv_n = 2;
-    return launch_append_warps(a, s);
+    return launch_append_warps(a, s, false);
   }
   if (a.k_format == KVQ_TQ3_QJL) {
     const cudaError_t e = launch_append_tq_keys(a, s);
     if (e != cudaSuccess) return e;
     a.kv_lo = 1;
     a.kv_n = 1;
-    return launch_append_bulk(a, s);
+    return launch_append_bulk(a, s, true);
   }
   a.kv_lo = 0;
   a.kv_n = 2;
-  return launch_append_bulk(a, s);
+  return launch_append_bulk(a, s, false);
 }
 
 }  // namespace kvq

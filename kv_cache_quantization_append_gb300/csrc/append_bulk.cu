@@ -35,7 +35,7 @@ constexpr float RINT_MAGIC = 12582912.0f;                 // 1.5 * 2^23
 constexpr float FAST_Q_LIMIT = 0.5f - 7.62939453125e-6f;  // 0.5 - 2^-17
 constexpr float FAST_Q8_LIMIT = 0.5f - 3.0517578125e-5f;  // 0.5 - 2^-15
 
-__global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_constant__ AppendArgs a) {
+__device__ __forceinline__ void append_bulk_body(const AppendArgs& a) {
   const int lane = threadIdx.x & 31, wl = threadIdx.x >> 5;
   const int G = lane & 3, tv = lane >> 2;  // group (channels 32G ..) and token of this lane
   // a dependent decode launch may start its set-up now; it waits for this grid before reading
@@ -340,15 +340,34 @@ __global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_co
   }
 }
 
+// A TurboQuant-key append launches this kernel for the values (AFTER_KEYS) as a programmatic
+// dependent of the keys kernel (the two write disjoint bytes, so they may overlap); every thread then
+// waits for the keys grid before exiting, so that whatever waits for this grid (the decode) also
+// waits for the keys.
+template <bool AFTER_KEYS>
+__global__ void __launch_bounds__(BW * 32, 4) append_bulk_kernel(const __grid_constant__ AppendArgs a) {
+  append_bulk_body(a);
+  if (AFTER_KEYS) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace
 
-cudaError_t launch_append_bulk(const AppendArgs& a, cudaStream_t s) {
+cudaError_t launch_append_bulk(const AppendArgs& a, cudaStream_t s, bool after_keys) {
   const long long gx = ((long long)a.T / TPW + 2 + BW - 1) / BW;
   const long long gy = (long long)a.n_layers_call * a.Hkv * a.kv_n;
   if (gx <= 0 || gy <= 0 || a.batch <= 0) return cudaSuccess;
   if (gx > 0x7fffffffLL || gy > 65535 || a.batch > 65535) return cudaErrorInvalidValue;
-  append_bulk_kernel<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)a.batch), BW * 32, 0, s>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)gx, (unsigned)gy, (unsigned)a.batch);
+  cfg.blockDim = dim3(BW * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_keys ? 1 : 0;
+  return after_keys ? cudaLaunchKernelEx(&cfg, append_bulk_kernel<true>, a)
+                    : cudaLaunchKernelEx(&cfg, append_bulk_kernel<false>, a);
 }
 
 }  // namespace kvq

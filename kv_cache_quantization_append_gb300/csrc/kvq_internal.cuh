@@ -76,7 +76,9 @@ struct AppendArgs {
   int kv_lo, kv_n;  // vectors handled by one launch: K (0) and/or V (1), kv_lo .. kv_lo + kv_n - 1
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t s);
-cudaError_t launch_append_bulk(const AppendArgs& a, cudaStream_t s);
+// after_keys: the values of a TurboQuant-key append, launched right after the keys kernel as its
+// programmatic dependent (the two overlap; the values grid ends after the keys grid)
+cudaError_t launch_append_bulk(const AppendArgs& a, cudaStream_t s, bool after_keys = false);
 
 struct CalibArgs {
   DevPtrs p;
