@@ -273,8 +273,7 @@ __global__ void __launch_bounds__(TQ_WARPS * 32) append_tq_keys_kernel(const App
   // a dependent decode launch may start its set-up now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;");
   // the transposed projection, 64 KB: each thread's 16 rows of 16 bytes requested 8 at a time
-  // before any is stored (one at a time, the loads were 16 dependent round trips: most of a
-  // one-token append)
+  // before any is stored
   constexpr int STAGE_N = D * D / 4 / (TQ_WARPS * 32), STAGE_BATCH = 8;
   static_assert(STAGE_N % STAGE_BATCH == 0, "whole batches");
 #pragma unroll 1
