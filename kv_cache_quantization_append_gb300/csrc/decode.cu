@@ -41,7 +41,7 @@ constexpr unsigned long long WAIT_NS = 1000000000ull;  // give up a pipeline wai
 constexpr float LAZY_RAISE = 4.0f;  // log2 headroom of the softmax reference (weights up to 16)
 constexpr int MERGE_WARPS = 8;  // warps per CTA of the merge kernels
 constexpr long long WIDE_MERGE_RECORDS = 48;  // above this many records per unit, merge with a CTA per head
-constexpr int WIDE_MERGE_WARPS = 16;          // warps per CTA of merge_wide_kernel (each a slice of the records)
+constexpr int WIDE_MERGE_WARPS = 16;          // warps per CTA of merge_wide_kernel (15 on slices of the records, 1 on the window parts)
 
 // Per-format CTA geometry and shared-memory carve-up (bytes): consumer warps + 1 producer warp.
 // Q4G32 keys: 15 consumer warps with 2 stages each at 128 registers (more warps to hide the math's
