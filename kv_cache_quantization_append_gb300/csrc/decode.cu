@@ -223,15 +223,21 @@ struct Seq {
 // Relative costs used to split a call's steps over the warps, in sixteenths of a quantised
 // half-page step (measured with per-warp timestamps): a window chunk costs about as much as a
 // half-page, and the set-up of a unit (query rotation, its record) about two, charged to the
-// unit's first step.  Relative speeds of the consumer warps: the three (two) that share an SM
-// sub-partition with the producer warp get about 10 % more issue slots than the others and
-// finish their ranges that much earlier, so they get proportionally longer ranges.
-constexpr int COST_Q = 16, COST_WIN = 16, COST_UNIT = 32;
-constexpr int COST_MAX_STEP = COST_UNIT + COST_Q;
+// unit's first step; with TQ3 keys the set-up also projects each query head through the 128 x 128
+// QJL matrix, and a charge of eight half-pages measured best (cost 128: the all-layer call 2,250 →
+// 2,236 us; 64, 96, 160-256 no better).  Relative speeds of the consumer warps: the three (two) that
+// share an SM sub-partition with the producer warp get about 10 % more issue slots than the others
+// and finish their ranges that much earlier, so they get proportionally longer ranges.
+constexpr int COST_Q = 16, COST_WIN = 16;
+template <int KF>
+constexpr int cost_unit() { return KF == KVQ_TQ3_QJL ? 128 : 32; }
+template <int KF>
+constexpr int cost_max_step() { return cost_unit<KF>() + COST_Q; }
 constexpr int SPEED_NORMAL = 10, SPEED_FAST = 11;
 
 // ---- the shared-memory arrays behind Seq, filled by the decode kernel's set-up
 // sequence b of (validated) length L: its steps (window chunks first, then quantised half-pages)
+template <int KF>
 __device__ __forceinline__ void seq_steps(int b, int L, int W, int* sL, int* sNW, int* sS, int* sC) {
   const int Lq = W > 0 ? max(0, L - W) : L;
   const int nw = W > 0 ? (min(L, W) + WCHUNK - 1) / WCHUNK : 0;
@@ -239,7 +245,7 @@ __device__ __forceinline__ void seq_steps(int b, int L, int W, int* sL, int* sNW
   sL[b] = L;
   sNW[b] = nw;
   sS[b] = nw + nq;
-  sC[b] = (nw + nq) > 0 ? COST_UNIT + nw * COST_WIN + nq * COST_Q : 0;
+  sC[b] = (nw + nq) > 0 ? cost_unit<KF>() + nw * COST_WIN + nq * COST_Q : 0;
 }
 // warp 0: exclusive prefix sums of the steps and costs of the B sequences, totals at index B
 __device__ __forceinline__ void seq_prefix(int lane, int B, const int* sS, const int* sC, int* sPre, int* sCpre) {
@@ -359,7 +365,7 @@ struct Kernel {
     long long c = (long long)ll * C_layer + (long long)H * sq.cpre[b] + (long long)h * sq.C[b];
     if (local > 0) {
       const int nwin = sq.NW[b];
-      c += COST_UNIT + (long long)min(local, nwin) * COST_WIN + (long long)max(0, local - nwin) * COST_Q;
+      c += cost_unit<KF>() + (long long)min(local, nwin) * COST_WIN + (long long)max(0, local - nwin) * COST_Q;
     }
     return c;
   }
@@ -394,8 +400,8 @@ struct Kernel {
     p.h = (int)div_nn(r2, sq.C[lo]);
     const int r3 = (int)(r2 - (long long)p.h * sq.C[lo]);
     const int nwin = sq.NW[lo];
-    p.local = (r3 < COST_UNIT + nwin * COST_WIN) ? max(0, r3 - COST_UNIT) / COST_WIN
-                                                 : nwin + (r3 - COST_UNIT - nwin * COST_WIN) / COST_Q;
+    p.local = (r3 < cost_unit<KF>() + nwin * COST_WIN) ? max(0, r3 - cost_unit<KF>()) / COST_WIN
+                                                        : nwin + (r3 - cost_unit<KF>() - nwin * COST_WIN) / COST_Q;
     if (cost_at(p.ll, p.b, p.h, p.local) < y) advance(p, 1, B, H, sq);
     return p;
   }
@@ -408,7 +414,7 @@ struct Kernel {
     nw = 0;
     if (S > 0) {
       // every range, even a normal-speed one, must span at least the longest step
-      nw = max(1LL, min((long long)gridDim.x * NCW, C * SPEED_NORMAL / ((long long)COST_MAX_STEP * SPEED_FAST)));
+      nw = max(1LL, min((long long)gridDim.x * NCW, C * SPEED_NORMAL / ((long long)cost_max_step<KF>() * SPEED_FAST)));
       SPtot = speed_before(nw);
     }
   }
@@ -1384,7 +1390,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
         if (blockIdx.x == 0) atomicOr(a.p.status, KVQ_DEV_SEQLEN_RANGE);
         L = 0;
       }
-      seq_steps(b, L, W, sL, sNW, sS, sC);
+      seq_steps<KF>(b, L, W, sL, sNW, sS, sC);
     }
     __syncthreads();
     if (K.warp == 0) seq_prefix(K.lane, B, sS, sC, sPre, sCpre);
@@ -1426,7 +1432,7 @@ __global__ void __launch_bounds__(Geo<KF>::NTHREADS, 1) decode_kernel(const __gr
         }
         if (pass == 0 || L != sL[b]) {
           changed = true;
-          seq_steps(b, L, W, sL, sNW, sS, sC);
+          seq_steps<KF>(b, L, W, sL, sNW, sS, sC);
         }
       }
       if (!__syncthreads_or(changed)) continue;
