@@ -9,6 +9,7 @@ import pytest
 import torch
 
 from kv_cache_quantization_append_gb300 import synth
+from oracle import codec
 
 from . import harness, layout
 
@@ -359,6 +360,58 @@ def test_chunked_appends_at_odd_offsets(gpu_lib, variant):
             slots = np.arange(s1 - min(W, int(last_T[b])), s1) % W
             assert np.array_equal(rk[slots].view(np.uint32), ora.ring_k[0, b, h, slots].view(np.uint32))
             assert np.array_equal(rv[slots].view(np.uint32), ora.ring_v[0, b, h, slots].view(np.uint32))
+
+
+@pytest.mark.parametrize("k_format", ["q4g32", "q8g32"])
+def test_bulk_append_degenerate_groups(gpu_lib, k_format):
+    """Rotated groups whose codes clamp, whose zero overflows fp16, that are exactly zero, or that
+    span many decades, through the bulk kernel (bf16 inputs, starts inside a block): codes, scales
+    and zeros of K and V bit-exact with the oracle.
+
+    With s the rotation's signs and e_j the unit vectors, x = beta * s (.) (e_0 + e_32 + e_64 + e_96)
+    + gamma * s (.) e_1 rotates exactly to c (4 beta +- gamma) on channels 0..31 and c (+-gamma) on
+    the rest: group 0 holds two values 2 c gamma apart around 4 c beta, so its fp16 zero misses its
+    minimum by far more than its step when beta >> gamma (clamped codes), and overflows fp16 when
+    |4 c beta| > 65504.  x = alpha * s rotates to one non-zero channel: groups 1..3 are all zero."""
+    B, H, Hq, T = 2, 2, 4, 300
+    gpu, ora, _ = harness.make_pair(1, H, Hq, B, 512, window=64, k_format=k_format)
+    rng = np.random.default_rng(11)
+    sg = ora.signs.astype(np.float64)
+    xs = []
+    for _ in range(2):  # K, then V
+        x = rng.standard_normal((B, H, T, 128))
+        for t in range(T):
+            kind = t % 5
+            if kind in (1, 2):
+                beta = rng.uniform(100.0, 5000.0) if kind == 1 else -2.0e5
+                gamma = float(rng.choice([0.5, 1.0, 2.0]))
+                e = np.zeros(128)
+                e[[0, 32, 64, 96]] = beta
+                e[1] = gamma
+                x[:, :, t] = sg * e
+            elif kind == 3:
+                x[:, :, t] *= np.exp(rng.uniform(-12.0, 12.0, (B, H, 128)))
+            elif kind == 4:
+                x[:, :, t] = 0.375 * sg
+        xs.append(torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16).cuda())
+    k, v = xs
+    p0 = np.array([3, 64], np.int64)
+    gpu.append(0, k, v, torch.as_tensor(p0.astype(np.int32), device="cuda"))
+    ora.append(0, harness.to_np(k), harness.to_np(v), p0)
+    torch.cuda.synchronize()
+    assert gpu.status() == 0
+    names = (("k_code", "code"), ("k_scale", "scale")) + ((("k_zero", "zero"),) if k_format == "q4g32" else ())
+    for b in range(B):
+        s0 = int(p0[b])
+        for h in range(H):
+            got = layout.read_unit(gpu.buffer, gpu.cfg, 0, b, h, s0 + T)
+            for gname, oname in names:
+                assert np.array_equal(got[gname][s0:].view(np.uint8),
+                                      ora.k[oname][0, b, h, s0:s0 + T].view(np.uint8)), (gname, b, h)
+            for oname in ("code", "scale", "zero"):
+                assert np.array_equal(got["v_" + oname][s0:].view(np.uint8),
+                                      ora.v[oname][0, b, h, s0:s0 + T].view(np.uint8)), ("v_" + oname, b, h)
+            harness.compare_ring(gpu, ora, 0, b, h, s0 + T)
 
 
 def test_many_tiny_units(gpu_lib):
