@@ -370,10 +370,10 @@ def time_bulk_append(cache, w, layers, lens, dev, stream, peak, peak_src):
         raise RuntimeError("device status set during the bulk append")
     a_s = a0.elapsed_time(a1) / BULK_APPEND_REPS / 1e3
     a_bytes = bulk_append_bytes(w, layers, Tc)
+    bulk = "append_bulk_bf16_kernel" if w["in_dtype"] == "bf16" else "append_bulk_kernel"
     res = {"tokens_per_sequence": Tc, "us": a_s * 1e6, "algorithmic_bytes": a_bytes,
            "achieved_gbs": a_bytes / a_s / 1e9, "tokens_per_s": layers * B * Tc / a_s,
-           "kernel": ("append_tq_keys_kernel + append_bulk_kernel (values)" if w["k_format"] == "tq3_qjl"
-                      else "append_bulk_kernel")}
+           "kernel": f"append_tq_keys_kernel + {bulk} (values)" if w["k_format"] == "tq3_qjl" else bulk}
     res["roofline"] = {"bound": "hbm", "achieved": res["achieved_gbs"], "peak": peak, "unit": "GB/s",
                        "frac": res["achieved_gbs"] / peak, "peak_source": peak_src}
     if w["k_format"] == "tq3_qjl":
