@@ -12,26 +12,26 @@
 //    that of the plain add or subtract since the product by +-1 is exact);
 //  * the group min/max, scale, zero and codes need no other lane;
 //  * a lane holds 32 values (64 registers: 32 warps per SM), and the code is small.
-// A warp owns 8 consecutive positions (aligned to 8, so that a V token pair 2p, 2p+1 is always in
-// one warp) of one (layer, sequence, kv-head, K|V); inputs are read straight from global memory.
+//
+// Work unit: 8 consecutive positions (aligned to 8, so that a V token pair 2p, 2p+1 is always in
+// one warp) of one (layer, sequence, kv-head, K|V).  fp32 inputs: one unit per warp, inputs read
+// straight from global memory.  bf16 inputs: a pipelined form in which each warp codes 16
+// consecutive units and copies the next unit's inputs into shared memory (cp.async, one 512-byte
+// run of the unit per instruction) while it codes the current one, so the DRAM latency is paid
+// once per 16 units instead of once per unit.
 //
 // Code of y: the quotient (y - zero) / scale is formed as (y - zero) * rcp(scale), with rcp the
 // hardware reciprocal (within 1 ulp, relative 2^-23), which for |q| <= 16 is within 3.9e-6 of the
 // IEEE quotient RN((y - zero) / scale) (the product's and the quotient's roundings of relative
-// 2^-24 and the reciprocal's 2^-23); rint is taken on the FMA pipe as (q + 1.5 * 2^23) - 1.5 * 2^23.  Where q lies within 2^-17 of a half-integer, or the code falls outside [0, 15], the
-// lane recomputes its group from the IEEE division, so every code equals
-// clamp(rint(RN((y - zero) / scale)), 0, 15).  The scale itself, RN((max - min) / 15), is exact:
-// Markstein's correction step (P. Markstein, "Computation of elementary functions on the IBM RISC
-// System/6000 processor", IBM J. Res. Dev. 34(1), 1990) of the product by RN(1/15) with the exact
-// fma residual.  The fast quotient is monotone in y (a subtraction and
-// a product by a positive constant, each rounded), so all of a group's codes lie in [0, 15] when
-// those of its minimum and maximum do; the codes are then the low nibbles of the rint sums,
-// gathered a byte at a time.
-//
-// bf16 inputs take a pipelined form: each warp codes 16 consecutive 8-position blocks and copies the
-// next block's inputs into shared memory (cp.async, one 512-byte row of the block per instruction)
-// while it codes the current one, so the DRAM latency is paid once per 16 blocks instead of once
-// per block.
+// 2^-24 and the reciprocal's 2^-23); rint is taken on the FMA pipe as (q + 1.5 * 2^23) - 1.5 * 2^23.
+// Where q lies within 2^-17 of a half-integer, or the code falls outside [0, 15], the lane
+// recomputes its group from the IEEE division, so every code equals
+// clamp(rint(RN((y - zero) / scale)), 0, 15).  The fast quotient is monotone in y (a subtraction
+// and a product by a positive constant, each rounded), so all of a group's codes lie in [0, 15]
+// when those of its minimum and maximum do; the codes are then the low nibbles of the rint sums,
+// gathered a byte at a time.  The scale itself, RN((max - min) / 15), is exact: Markstein's
+// correction step (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990) of the product by RN(1/15) with the exact fma residual.
 #include <cfloat>
 
 #include "kvq_internal.cuh"
